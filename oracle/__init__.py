@@ -1,0 +1,150 @@
+"""fp64 CPU oracle of the selective scan — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import this
+package.  The product package never imports it, and it imports nothing from the product package.
+
+The arithmetic lives in ``oracle.c`` (plain C, double precision, sequential in time); this module
+only compiles it with gcc on first use and marshals numpy arrays into it.
+
+Parity status: every function here is pinned by the ``-m "not gpu"`` tests in
+``tests/test_oracle_pins.py`` (LTI convolution by brute force, the scalar-state closed form, the
+one-step formula, the Delta -> 0 and Delta -> infinity limits, linearity in the input, and the
+decode step against the scan).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16 = 0, 1
+_DT = {"f32": F32, "bf16": BF16}
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, -O2, OpenMP, strict IEEE double arithmetic)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                               "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB)
+            P, I, LL, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_double
+            L.oracle_scan_rows.restype = I
+            L.oracle_scan_rows.argtypes = [LL, P, P, I, I, LL, I, P, P, P, P, P, P, P, P, I, P, P, P, I]
+            L.oracle_state_step_rows.restype = I
+            L.oracle_state_step_rows.argtypes = [LL, P, P, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I]
+            L.oracle_version.restype = I
+            _lib = L
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def _storage(a, dt):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.uint16 if dt == BF16 else np.float32)
+
+
+def scan_rows(rows, dim, u_rows, delta_rows, z_rows, A, D, delta_bias, B, C, softplus=True,
+              dtype="f32", h0_rows=None, nthreads=0):
+    """Scan for the channels ``rows`` (flat b*dim + d).  u/delta/z_rows [nrows, L] in storage
+    dtype; B, C [batch, N, L].  Returns (y [nrows, L], state [nrows, N]) in float64."""
+    dt = _DT[dtype]
+    rows = np.asarray(rows, dtype=np.int64)
+    nrows = len(rows)
+    A = _c(A, np.float32)
+    N = A.shape[1]
+    L = np.asarray(u_rows).shape[-1]
+    rb = np.ascontiguousarray(rows // dim, dtype=np.int32)
+    rd = np.ascontiguousarray(rows % dim, dtype=np.int32)
+    u_rows, delta_rows, z_rows = (_storage(x, dt) for x in (u_rows, delta_rows, z_rows))
+    B, C = _storage(B, dt), _storage(C, dt)
+    D, delta_bias = _c(D, np.float32), _c(delta_bias, np.float32)
+    h0 = _c(h0_rows, np.float64)
+    y = np.empty((nrows, L), dtype=np.float64)
+    st = np.empty((nrows, N), dtype=np.float64)
+    rc = lib().oracle_scan_rows(nrows, _ptr(rb), _ptr(rd), dim, N, L, dt, _ptr(u_rows),
+                                _ptr(delta_rows), _ptr(z_rows), _ptr(A), _ptr(D), _ptr(delta_bias),
+                                _ptr(B), _ptr(C), int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(st),
+                                int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_scan_rows rejected its arguments (rc={rc})")
+    return y, st
+
+
+def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, dtype="f32", h0=None,
+         nthreads=0):
+    """Full scan.  u, delta, z [batch, dim, L]; returns y [batch, dim, L], last_state [batch, dim, N]
+    (float64)."""
+    bsz, dim, L = np.asarray(u).shape
+    N = np.asarray(A).shape[1]
+    rows = np.arange(bsz * dim)
+    r = lambda x: None if x is None else np.asarray(x).reshape(bsz * dim, L)
+    y, st = scan_rows(rows, dim, r(u), r(delta), r(z), A, D, delta_bias, B, C, softplus, dtype,
+                      None if h0 is None else np.asarray(h0, dtype=np.float64).reshape(bsz * dim, N),
+                      nthreads)
+    return y.reshape(bsz, dim, L), st.reshape(bsz, dim, N)
+
+
+def state_step_rows(rows, dim, state_rows, x_rows, delta_rows, z_rows, A, D, delta_bias, B, C,
+                    softplus=True, dtype="f32", nthreads=0):
+    """One decode step for channels ``rows``.  state_rows [nrows, N] float64 is updated IN PLACE;
+    x/delta/z_rows [nrows]; B, C [batch, N].  Returns y [nrows] float64."""
+    dt = _DT[dtype]
+    rows = np.asarray(rows, dtype=np.int64)
+    nrows = len(rows)
+    A = _c(A, np.float32)
+    N = A.shape[1]
+    if not (isinstance(state_rows, np.ndarray) and state_rows.dtype == np.float64
+            and state_rows.flags.c_contiguous and state_rows.shape == (nrows, N)):
+        raise TypeError("state_rows must be a C-contiguous float64 array [nrows, N]")
+    rb = np.ascontiguousarray(rows // dim, dtype=np.int32)
+    rd = np.ascontiguousarray(rows % dim, dtype=np.int32)
+    x_rows, delta_rows, z_rows = (_storage(x, dt) for x in (x_rows, delta_rows, z_rows))
+    B, C = _storage(B, dt), _storage(C, dt)
+    D, delta_bias = _c(D, np.float32), _c(delta_bias, np.float32)
+    y = np.empty(nrows, dtype=np.float64)
+    rc = lib().oracle_state_step_rows(nrows, _ptr(rb), _ptr(rd), dim, N, dt, _ptr(state_rows),
+                                      _ptr(x_rows), _ptr(delta_rows), _ptr(z_rows), _ptr(A), _ptr(D),
+                                      _ptr(delta_bias), _ptr(B), _ptr(C), int(bool(softplus)),
+                                      _ptr(y), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_state_step_rows rejected its arguments (rc={rc})")
+    return y
+
+
+def state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+               dtype="f32", nthreads=0):
+    """Full decode step.  state [batch, dim, N] float64 updated in place; x/delta/z [batch, dim];
+    B, C [batch, N].  Returns y [batch, dim] float64."""
+    bsz, dim, N = state.shape
+    rows = np.arange(bsz * dim)
+    st = state.reshape(bsz * dim, N)
+    r = lambda a: None if a is None else np.asarray(a).reshape(bsz * dim)
+    y = state_step_rows(rows, dim, st, r(x), r(delta), r(z), A, D, delta_bias, B, C, softplus,
+                        dtype, nthreads)
+    return y.reshape(bsz, dim)

@@ -1,0 +1,92 @@
+"""Plant plausible mistakes in the oracle's C source, on the CPU, and check that the pins catch them.
+
+Each mutant is a one-line textual change of ``oracle/oracle.c`` (a dropped term, a wrong sign or
+index, a transposed operand, a misplaced bias), compiled to a temporary library that replaces the
+oracle's for the duration of one check.  A mutant passes the check only if at least one pin in
+``test_oracle_pins.py`` fails on it.
+"""
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "readout_uses_B": ("acc += widen(C, bc, in_dtype) * h[n];", "acc += widen(B, bc, in_dtype) * h[n];"),
+    "skip_term_dropped": ("double y = acc + Dd * x;", "double y = acc;"),
+    "A_sign_flipped": ("const double Abar = exp(dt * a_n[n]);", "const double Abar = exp(-dt * a_n[n]);"),
+    "euler_A": ("const double Abar = exp(dt * a_n[n]);", "const double Abar = 1.0 + dt * a_n[n];"),
+    "Bbar_missing_delta": ("const double Bbar_x = dt * widen(B, bc, in_dtype) * x;",
+                           "const double Bbar_x = widen(B, bc, in_dtype) * x;"),
+    "BC_transposed": ("const long long bc = ((long long)b * dstate + n) * seqlen + t;",
+                      "const long long bc = ((long long)b * seqlen + t) * dstate + n;"),
+    "BC_batch_ignored": ("const long long bc = ((long long)b * dstate + n) * seqlen + t;",
+                         "const long long bc = ((long long)0 * dstate + n) * seqlen + t;"),
+    "A_channel_ignored": ("a_n[n] = (double)A[(long long)d * dstate + n];", "a_n[n] = (double)A[n];"),
+    "readout_before_update": ("h[n] = Abar * h[n] + Bbar_x;\n                acc += widen(C, bc, in_dtype) * h[n];",
+                              "acc += widen(C, bc, in_dtype) * h[n];\n                h[n] = Abar * h[n] + Bbar_x;"),
+    "bias_after_softplus": ("double d = raw + bias;\n    return softplus_flag ? softplus(d) : d;",
+                            "return softplus_flag ? softplus(raw) + bias : raw + bias;"),
+    "gate_is_sigmoid": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
+    "softplus_overflows": ("if (x > 0.0) return x + log1p(exp(-x));", "if (x > 1e300) return x;"),
+    "step_skip_dropped": ("double y = acc + (D ? (double)D[d] : 0.0) * x;", "double y = acc;"),
+    "step_A_sign": ("const double Abar = exp(dt * (double)A[(long long)d * dstate + n]);",
+                    "const double Abar = exp(-dt * (double)A[(long long)d * dstate + n]);"),
+    "bf16_widen_wrong_shift": ("((const uint16_t*)p)[i]) << 16;", "((const uint16_t*)p)[i]) << 15;"),
+}
+
+PINS = [
+    lambda: pins.test_lti_equals_convolution(1, 16, 4, 64),
+    pins.test_lti_tiny_workload_recipe,
+    lambda: pins.test_scalar_closed_form_time_varying(1),
+    lambda: pins.test_scalar_closed_form_time_varying(4),
+    pins.test_closed_form_without_softplus_and_with_initial_state,
+    pins.test_single_step_formula,
+    pins.test_softplus_and_bias_against_logaddexp,
+    pins.test_gate_against_expit,
+    pins.test_delta_zero_keeps_state_bit_for_bit,
+    pins.test_delta_zero_scan_gives_skip_only,
+    pins.test_huge_delta_is_memoryless,
+    pins.test_linear_in_u,
+    pins.test_decode_steps_equal_scan,
+    pins.test_bf16_widening_matches_fp32,
+]
+
+
+def _compile(src_text, out_dir):
+    c = os.path.join(out_dir, "mut.c")
+    so = os.path.join(out_dir, "libmut.so")
+    with open(c, "w") as f:
+        f.write(src_text)
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                           "-ffp-contract=off", "-o", so, c, "-lm"])
+    return so
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, monkeypatch):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutant anchor not found: {old!r}"
+    mutated = src.replace(old, new)
+    real = oracle.lib()
+    with tempfile.TemporaryDirectory() as td:
+        so = _compile(mutated, td)
+        mut = ctypes.CDLL(so)
+        for fn in ("oracle_scan_rows", "oracle_state_step_rows"):
+            getattr(mut, fn).restype = getattr(real, fn).restype
+            getattr(mut, fn).argtypes = getattr(real, fn).argtypes
+        monkeypatch.setattr(oracle, "_lib", mut)
+        caught = []
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError, FloatingPointError):
+                caught.append(pin)
+        assert caught, f"no pin caught mutant {name}"

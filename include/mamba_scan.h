@@ -1,0 +1,115 @@
+/*
+ * mamba_scan.h — C ABI of the B300 (sm_103a) selective-scan library, libmambascan.so.
+ *
+ * The library implements the data-parallel core of the selective state space layer described in
+ * "Mamba: Linear-Time Sequence Modeling with Selective State Spaces" (visual guide to Mamba and
+ * SSMs, sections 2.2-2.4 and 3.2-3.4; news write-up, "selection mechanism" and "hardware-aware
+ * algorithm" sections):
+ *
+ *   Delta_t = softplus(delta_t + delta_bias)   (or delta_t + delta_bias without the flag)
+ *   Abar_t  = exp(Delta_t * A),   Bbar_t x_t = Delta_t * B_t * x_t          (discretisation, 2.3)
+ *   h_t     = Abar_t (.) h_{t-1} + Bbar_t x_t                                (recurrence, 2.4)
+ *   y_t     = (C_t . h_t + D * x_t) * silu(z_t)                              (readout + skip, 2.2)
+ *
+ * A is diagonal and real (one value per channel and state), B, C and Delta vary with batch and
+ * position (selection, 3.2).  The discretisation, recurrence and readout run fused in one kernel
+ * that keeps h on chip and never writes Abar or Bbar to memory (hardware-aware algorithm, 3.4).
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library keeps none of them
+ *    after the call returns and allocates no persistent memory.  Layouts are dense row-major with
+ *    the last index contiguous.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as void*; NULL = the
+ *    legacy default stream).  Results are valid once the stream has reached that point.
+ *  - Return value: MAMBA_OK (0) or a negative error code.  No entry point aborts, traps or exits;
+ *    mamba_scan_last_error() gives a message for the calling thread's last failure.
+ *  - Misaligned pointers and any sequence length are accepted: such calls take a slower load path.
+ */
+#ifndef MAMBA_SCAN_H
+#define MAMBA_SCAN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MAMBA_SCAN_VERSION 1
+
+/* storage type of u / delta / z / B / C / y (A, D, delta_bias and all states are always fp32) */
+#define MAMBA_F32 0
+#define MAMBA_BF16 1
+
+#define MAMBA_OK 0
+#define MAMBA_ERR_ARG (-1)     /* bad argument: NULL required pointer, bad size, dtype, aliasing */
+#define MAMBA_ERR_CUDA (-2)    /* a CUDA call or kernel launch failed */
+#define MAMBA_ERR_TIMEOUT (-3) /* a kernel gave up a bounded wait (see mamba_scan_device_status) */
+
+#define MAMBA_MAX_DSTATE 64
+
+typedef struct {
+    int batch;          /* b  >= 1 */
+    int dim;            /* d (channels, d_inner) >= 1 */
+    int dstate;         /* N, 1 <= N <= MAMBA_MAX_DSTATE */
+    long long seqlen;   /* L >= 0 (ignored by mamba_state_step) */
+    int in_dtype;       /* MAMBA_F32 or MAMBA_BF16 */
+} mamba_scan_shape;
+
+/*
+ * Forward selective scan from a zero initial state.
+ *
+ *   u, delta, z   [b, d, L]  in_dtype.  z == NULL: no gate (y = C.h + D x).
+ *   A             [d, N]     fp32 (typically negative; Abar = exp(Delta A)).
+ *   B, C          [b, N, L]  in_dtype, shared by all channels of a batch row.
+ *   D             [d]        fp32 or NULL (= 0).
+ *   delta_bias    [d]        fp32 or NULL (= 0).
+ *   softplus_flag            nonzero: Delta = softplus(delta + bias); zero: Delta = delta + bias.
+ *   y             [b, d, L]  in_dtype, written (bf16 by round-to-nearest-even).  Must not overlap
+ *                            any input.
+ *   last_state    [b, d, N]  fp32 or NULL: h after the last position (zeros when L == 0).
+ *
+ * Sequences with few channels (b*d small against the GPU) are split along L: a first kernel
+ * computes per-segment carries into stream-ordered scratch memory (cudaMallocAsync on `stream`,
+ * freed on the same stream), a second kernel runs the fused scan per segment from its carry.
+ * Errors: MAMBA_ERR_ARG for bad arguments, MAMBA_ERR_CUDA if an allocation or launch fails.
+ */
+int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const void* delta, const float* A,
+                   const void* B, const void* C, const float* D, const void* z,
+                   const float* delta_bias, int softplus_flag, void* y, float* last_state,
+                   void* stream);
+
+/*
+ * One recurrent decoding step for every (batch, channel): constant work per token, no cache of
+ * past tokens (news write-up, "architecture" section; visual guide section 1.4).
+ *
+ *   state         [b, d, N]  fp32, updated IN PLACE: h <- exp(Delta A) h + Delta B x.
+ *   x, delta, z   [b, d]     in_dtype (z may be NULL).
+ *   A [d, N], D [d], delta_bias [d]: as for mamba_scan_fwd.
+ *   B, C          [b, N]     in_dtype.
+ *   y             [b, d]     in_dtype, y = (C.h + D x) silu(z) with the updated h.
+ * s->seqlen is ignored.  Errors as for mamba_scan_fwd.
+ */
+int mamba_state_step(const mamba_scan_shape* s, float* state, const void* x, const void* delta,
+                     const float* A, const void* B, const void* C, const float* D, const void* z,
+                     const float* delta_bias, int softplus_flag, void* y, void* stream);
+
+/* Message describing the calling thread's most recent failure ("" if none). */
+const char* mamba_scan_last_error(void);
+
+/* MAMBA_SCAN_VERSION of the loaded library. */
+int mamba_scan_version(void);
+
+/* Number of kernels this library has launched in this process so far (all threads, all devices);
+ * lets a caller count the GPU work behind a sequence of calls. */
+long long mamba_scan_launch_count(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status word on the current
+ * device.  Returns MAMBA_OK, MAMBA_ERR_TIMEOUT if any kernel since the last call abandoned a
+ * bounded wait on an asynchronous copy (its outputs are then invalid), or MAMBA_ERR_CUDA.
+ */
+int mamba_scan_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_SCAN_H */

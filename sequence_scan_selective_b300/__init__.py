@@ -1,0 +1,162 @@
+"""B300-native selective scan (the core of Mamba's selective SSM layer) behind libmambascan.so.
+
+This module only marshals arguments: it checks torch tensors (device memory), passes their data
+pointers and the current CUDA stream to the library, and raises on a negative status.  Every step of
+the computation runs in the library's sm_103a kernels; there is no fallback.  If the compiled
+library is missing, importing this package raises ImportError.
+
+Entry points (names as in include/mamba_scan.h):
+  mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, y=None, last_state=None)
+  mamba_state_step(state, x, delta, A, B, C, D, z, delta_bias, softplus, y=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmambascan.so")
+
+MAMBA_F32, MAMBA_BF16 = 0, 1
+MAMBA_OK, MAMBA_ERR_ARG, MAMBA_ERR_CUDA, MAMBA_ERR_TIMEOUT = 0, -1, -2, -3
+MAX_DSTATE = 64
+
+
+class MambaScanError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("dim", ctypes.c_int), ("dstate", ctypes.c_int),
+                ("seqlen", ctypes.c_longlong), ("in_dtype", ctypes.c_int)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmambascan.so is not built ({LIB_PATH}); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` or "
+                          "`python sequence_scan_selective_b300/build.py`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.mamba_scan_fwd.restype = I
+    lib.mamba_scan_fwd.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, I, P, P, P]
+    lib.mamba_state_step.restype = I
+    lib.mamba_state_step.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, I, P, P]
+    lib.mamba_scan_last_error.restype = ctypes.c_char_p
+    lib.mamba_scan_last_error.argtypes = []
+    lib.mamba_scan_version.restype = I
+    lib.mamba_scan_version.argtypes = []
+    lib.mamba_scan_device_status.restype = I
+    lib.mamba_scan_device_status.argtypes = [P]
+    lib.mamba_scan_launch_count.restype = ctypes.c_longlong
+    lib.mamba_scan_launch_count.argtypes = []
+    return lib
+
+
+_lib = _load()
+
+# symbols the header declares; the tests check that every one of them is exported
+EXPORTED = ("mamba_scan_fwd", "mamba_state_step", "mamba_scan_last_error", "mamba_scan_version",
+            "mamba_scan_device_status", "mamba_scan_launch_count")
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != MAMBA_OK:
+        raise MambaScanError(rc, _lib.mamba_scan_last_error().decode(errors="replace"))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MAMBA_F32
+    if t.dtype == torch.bfloat16:
+        return MAMBA_BF16
+    raise TypeError(f"unsupported storage dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _ptr(t: Optional[torch.Tensor], shape, dtype, name: str):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
+                   last_state=None, want_state=True, stream=None):
+    """Selective scan.  u, delta, z [b, d, L]; B, C [b, N, L] (float32 or bfloat16, all the same);
+    A [d, N], D [d], delta_bias [d] float32.  Returns (y [b, d, L] in the input dtype,
+    last_state [b, d, N] float32 or None)."""
+    bsz, dim, L = u.shape
+    N = A.shape[1]
+    dt = u.dtype
+    code = _dtype_code(u)
+    if y is None:
+        y = torch.empty_like(u)
+    if last_state is None and want_state:
+        last_state = torch.empty((bsz, dim, N), device=u.device, dtype=torch.float32)
+    shape = Shape(bsz, dim, N, L, code)
+    rc = _lib.mamba_scan_fwd(
+        ctypes.byref(shape), _ptr(u, (bsz, dim, L), dt, "u"), _ptr(delta, (bsz, dim, L), dt, "delta"),
+        _ptr(A, (dim, N), torch.float32, "A"), _ptr(B, (bsz, N, L), dt, "B"),
+        _ptr(C, (bsz, N, L), dt, "C"), _ptr(D, (dim,), torch.float32, "D"),
+        _ptr(z, (bsz, dim, L), dt, "z"), _ptr(delta_bias, (dim,), torch.float32, "delta_bias"),
+        int(bool(softplus)), _ptr(y, (bsz, dim, L), dt, "y"),
+        _ptr(last_state, (bsz, dim, N), torch.float32, "last_state"), _stream(stream))
+    _check(rc)
+    return y, last_state
+
+
+def mamba_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
+                     stream=None):
+    """One decode step.  state [b, d, N] float32 (updated in place); x, delta, z [b, d];
+    B, C [b, N]; returns y [b, d] in the input dtype."""
+    bsz, dim, N = state.shape
+    dt = x.dtype
+    code = _dtype_code(x)
+    if y is None:
+        y = torch.empty_like(x)
+    shape = Shape(bsz, dim, N, 1, code)
+    rc = _lib.mamba_state_step(
+        ctypes.byref(shape), _ptr(state, (bsz, dim, N), torch.float32, "state"),
+        _ptr(x, (bsz, dim), dt, "x"), _ptr(delta, (bsz, dim), dt, "delta"),
+        _ptr(A, (dim, N), torch.float32, "A"), _ptr(B, (bsz, N), dt, "B"), _ptr(C, (bsz, N), dt, "C"),
+        _ptr(D, (dim,), torch.float32, "D"), _ptr(z, (bsz, dim), dt, "z"),
+        _ptr(delta_bias, (dim,), torch.float32, "delta_bias"), int(bool(softplus)),
+        _ptr(y, (bsz, dim), dt, "y"), _stream(stream))
+    _check(rc)
+    return y
+
+
+def device_status(stream=None) -> None:
+    """Synchronise and raise if a kernel abandoned a bounded wait since the last check."""
+    _check(_lib.mamba_scan_device_status(_stream(stream)))
+
+
+def version() -> int:
+    return _lib.mamba_scan_version()
+
+
+def launch_count() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(_lib.mamba_scan_launch_count())

@@ -1,0 +1,98 @@
+"""The C-ABI library loads, exports every symbol include/*.h declares, and rejects bad arguments on
+the host before touching a GPU (no compute call is made here)."""
+import ctypes
+import glob
+import os
+import re
+import threading
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[\w ]+?\s*\*?\s*(mamba_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def ms():
+    import sequence_scan_selective_b300 as m
+    return m
+
+
+def test_header_declares_entry_points():
+    assert {"mamba_scan_fwd", "mamba_state_step", "mamba_scan_last_error", "mamba_scan_version",
+            "mamba_scan_launch_count", "mamba_scan_device_status"} <= _declared()
+
+
+def test_library_exports_every_declared_symbol(ms):
+    lib = ctypes.CDLL(ms.LIB_PATH)
+    missing = [n for n in sorted(_declared()) if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(ms.EXPORTED) >= _declared()
+
+
+def test_version(ms):
+    hdr = open(os.path.join(ROOT, "include", "mamba_scan.h")).read()
+    v = int(re.search(r"#define MAMBA_SCAN_VERSION (\d+)", hdr).group(1))
+    assert ms.version() == v
+
+
+def _shape(ms, **kw):
+    s = dict(batch=1, dim=4, dstate=16, seqlen=8, in_dtype=0)
+    s.update(kw)
+    return ms.Shape(**s)
+
+
+def test_host_argument_checks(ms):
+    lib = ms.lib()
+    P = ctypes.c_void_p
+    dummy = P(256)  # never dereferenced: every case below fails validation first
+    assert lib.mamba_scan_fwd(None, dummy, dummy, dummy, dummy, dummy, None, None, None, 1, P(4096), None, None) == -1
+    assert b"NULL" in lib.mamba_scan_last_error()
+    for bad in (dict(batch=0), dict(dim=-1), dict(dstate=0), dict(dstate=65), dict(seqlen=-1), dict(in_dtype=2)):
+        s = _shape(ms, **bad)
+        rc = lib.mamba_scan_fwd(ctypes.byref(s), dummy, dummy, dummy, dummy, dummy, None, None, None, 1, P(1 << 40),
+                                None, None)
+        assert rc == -1, bad
+        assert lib.mamba_scan_last_error()
+    s = _shape(ms)
+    assert lib.mamba_scan_fwd(ctypes.byref(s), None, dummy, dummy, dummy, dummy, None, None, None, 1, P(1 << 40),
+                              None, None) == -1
+    # y overlapping u
+    assert lib.mamba_scan_fwd(ctypes.byref(s), P(1 << 20), P(1 << 30), dummy, P(1 << 31), P(1 << 32), None, None,
+                              None, 1, P((1 << 20) + 8), None, None) == -1
+    assert b"overlap" in lib.mamba_scan_last_error()
+    assert lib.mamba_state_step(ctypes.byref(s), None, dummy, dummy, dummy, dummy, dummy, None, None, None, 1,
+                                dummy, None) == -1
+    assert lib.mamba_state_step(ctypes.byref(_shape(ms, dstate=100)), dummy, dummy, dummy, dummy, dummy, dummy,
+                                None, None, None, 1, dummy, None) == -1
+
+
+def test_error_message_is_thread_local(ms):
+    lib = ms.lib()
+    lib.mamba_scan_fwd(None, None, None, None, None, None, None, None, None, 1, None, None, None)
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(lib.mamba_scan_last_error()))
+    t.start()
+    t.join()
+    assert seen == [b""]
+    assert lib.mamba_scan_last_error() != b""
+
+
+def test_launch_counter_starts_without_gpu_work(ms):
+    assert ms.launch_count() >= 0
+
+
+def test_product_package_does_not_reach_the_oracle():
+    pkg = os.path.join(ROOT, "sequence_scan_selective_b300")
+    for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
+        if os.path.isfile(path) and path.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+            text = open(path, errors="replace").read()
+            assert "oracle" not in text.lower(), path

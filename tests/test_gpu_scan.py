@@ -1,0 +1,209 @@
+"""GPU parity of the fused forward scan against the fp64 oracle, through the C ABI.
+
+Tolerance (fixed for this method): max|y_gpu - y_oracle| / max|y_oracle| <= 1e-4 with fp32 storage
+and <= 2e-2 with bf16 storage (fp32 state either way); final states under the same bounds.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import TOL, dev_inputs, from_dev, oracle_scan_full, rel_err, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ms():
+    import sequence_scan_selective_b300 as m
+    return m
+
+
+class _env:
+    def __init__(self, **kv):
+        self.kv, self.old = kv, {}
+
+    def __enter__(self):
+        for k, v in self.kv.items():
+            self.old[k] = os.environ.get(k)
+            os.environ[k] = v
+
+    def __exit__(self, *exc):
+        for k, v in self.old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def _run_gpu(ms, d, softplus=True, with_state=True):
+    y, st = ms.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d.get("D"), d.get("z"),
+                              d.get("delta_bias"), softplus, want_state=with_state)
+    torch.cuda.synchronize()
+    ms.device_status()
+    return y, st
+
+
+def _check_full(ms, cfg, softplus=True, drop=(), env=None):
+    inp = synth.scan_inputs(cfg)
+    for k in drop:
+        inp[k] = None
+    with _env(**(env or {})):
+        y, st = _run_gpu(ms, dev_inputs(inp, cfg.dtype), softplus)
+    y_ref, st_ref = oracle_scan_full(inp, cfg.dtype, softplus)
+    ey, es = rel_err(from_dev(y), y_ref), rel_err(from_dev(st), st_ref)
+    assert ey <= TOL[cfg.dtype], f"y rel err {ey:.3e}"
+    assert es <= TOL[cfg.dtype], f"state rel err {es:.3e}"
+    return ey, es
+
+
+def test_tiny_workload(ms):
+    _check_full(ms, synth.CONFIGS["tiny"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [1, 7, 32, 77, 200, 1000])
+def test_ragged_lengths(ms, dtype, L):
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=40, seqlen=L, dtype=dtype, seed=10 + L)
+    _check_full(ms, cfg)
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 8, 15, 16, 17, 32, 33, 64])
+def test_state_sizes(ms, N):
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=35, dstate=N, seqlen=160, seed=20 + N)
+    _check_full(ms, cfg)
+
+
+@pytest.mark.parametrize("variant", ["0", "1"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tiling_variants(ms, variant, dtype):
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=70, seqlen=333, dtype=dtype, seed=21)
+    _check_full(ms, cfg, env={"MAMBA_SCAN_VARIANT": variant})
+
+
+@pytest.mark.parametrize("drop", [("z",), ("D",), ("delta_bias",), ("z", "D", "delta_bias")])
+def test_optional_inputs(ms, drop):
+    cfg = synth.CONFIGS["m130"].replace(batch=3, dim=33, seqlen=96, seed=5)
+    _check_full(ms, cfg, drop=drop)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_softplus_off(ms, dtype):
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=32, seqlen=128, dtype=dtype, seed=6)
+    inp = synth.scan_inputs(cfg)
+    # without softplus the raw delta must itself be a valid step size: |delta| scaled down
+    dl = (np.abs(synth.widen(inp["delta"], dtype)) * 0.01).astype(np.float32)
+    inp["delta"] = synth.f32_to_bf16_bits(dl) if dtype == "bf16" else dl
+    inp["delta_bias"] = np.zeros_like(inp["delta_bias"])
+    y, st = _run_gpu(ms, dev_inputs(inp, dtype), softplus=False)
+    y_ref, st_ref = oracle_scan_full(inp, dtype, softplus=False)
+    assert rel_err(from_dev(y), y_ref) <= TOL[dtype]
+    assert rel_err(from_dev(st), st_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_unaligned_rows_take_plain_load_path(ms, dtype):
+    # L * element size not a multiple of 16 bytes: no TMA descriptor is possible for these rows
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=36, seqlen=301, dtype=dtype, seed=7)
+    _check_full(ms, cfg)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_forced_plain_loads_match(ms, dtype):
+    cfg = synth.CONFIGS["b14"].replace(batch=2, dim=64, seqlen=256, dtype=dtype, seed=8)
+    _check_full(ms, cfg, env={"MAMBA_SCAN_NO_TMA": "1"})
+
+
+@pytest.mark.parametrize("nseg", [2, 3, 7])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_split_time_axis(ms, nseg, dtype):
+    """Splitting L into segments (carry pass + per-segment scan) regroups the associative scan
+    operator (guide section 3.3); results must stay within tolerance of the oracle."""
+    cfg = synth.CONFIGS["long"].replace(batch=2, dim=24, seqlen=4000, dtype=dtype, seed=9)
+    _check_full(ms, cfg, env={"MAMBA_SCAN_NSEG": str(nseg)})
+
+
+def test_split_with_plain_loads(ms):
+    cfg = synth.CONFIGS["long"].replace(batch=1, dim=40, seqlen=3001, seed=11)
+    _check_full(ms, cfg, env={"MAMBA_SCAN_NSEG": "3"})
+
+
+def test_segment_count_invariance(ms):
+    cfg = synth.CONFIGS["long"].replace(batch=1, dim=32, seqlen=8192, seed=12)
+    d = dev_inputs(synth.scan_inputs(cfg), cfg.dtype)
+    outs = []
+    for nseg in ("1", "4", "16"):
+        with _env(MAMBA_SCAN_NSEG=nseg):
+            y, st = _run_gpu(ms, d)
+        outs.append((from_dev(y), from_dev(st)))
+    for y, st in outs[1:]:
+        assert rel_err(y, outs[0][0]) <= 1e-5
+        assert rel_err(st, outs[0][1]) <= 1e-5
+
+
+def test_zero_length(ms):
+    d = {k: torch.zeros((2, 8, 0), device="cuda") for k in ("u", "delta", "z")}
+    st = torch.full((2, 8, 4), 7.0, device="cuda")
+    ms.mamba_scan_fwd(d["u"], d["delta"], -torch.ones((8, 4), device="cuda"), torch.zeros((2, 4, 0), device="cuda"),
+                      torch.zeros((2, 4, 0), device="cuda"), last_state=st)
+    torch.cuda.synchronize()
+    assert torch.all(st == 0)
+
+
+def test_delta_zero_gives_skip_only(ms):
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=20, seqlen=64, seed=13)
+    inp = synth.scan_inputs(cfg)
+    inp["delta"][:] = 0.0
+    inp["delta_bias"][:] = 0.0
+    y, st = _run_gpu(ms, dev_inputs(inp, cfg.dtype), softplus=False)
+    assert torch.all(st == 0)
+    y_ref, _ = oracle_scan_full(inp, cfg.dtype, softplus=False)
+    assert rel_err(from_dev(y), y_ref) <= 1e-6
+
+
+def test_linearity_in_u(ms):
+    """Doubling u doubles y exactly (every product scales by a power of two)."""
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=32, seqlen=256, seed=14)
+    d = dev_inputs(synth.scan_inputs(cfg), cfg.dtype)
+    y1, _ = _run_gpu(ms, d)
+    y2, _ = _run_gpu(ms, dict(d, u=d["u"] * 2.0))
+    assert rel_err(from_dev(y2), 2.0 * from_dev(y1)) <= 1e-6
+
+
+def test_bad_arguments_raise(ms):
+    x = torch.zeros((1, 4, 16), device="cuda")
+    A = -torch.ones((4, 4), device="cuda")
+    Bm = torch.zeros((1, 4, 16), device="cuda")
+    with pytest.raises(ms.MambaScanError):   # y aliases u
+        ms.mamba_scan_fwd(x, x.clone(), A, Bm, Bm.clone(), y=x)
+    with pytest.raises(ms.MambaScanError):   # too many states
+        ms.mamba_scan_fwd(torch.zeros((1, 4, 16), device="cuda"), torch.zeros((1, 4, 16), device="cuda"),
+                          -torch.ones((4, 65), device="cuda"), torch.zeros((1, 65, 16), device="cuda"),
+                          torch.zeros((1, 65, 16), device="cuda"))
+
+
+# ------------------------------------------------------------------------------ full-size workloads
+def _check_sampled(ms, cfg, nsample, seed=0):
+    inp = synth.scan_inputs(cfg)
+    y, st = _run_gpu(ms, dev_inputs(inp, cfg.dtype))
+    rows = sample_rows(cfg.batch * cfg.dim, nsample, seed)
+    sub = {k: inp[k].reshape(cfg.batch * cfg.dim, cfg.seqlen)[rows] for k in ("u", "delta", "z")}
+    y_ref, st_ref = oracle.scan_rows(rows, cfg.dim, sub["u"], sub["delta"], sub["z"], inp["A"], inp["D"],
+                                     inp["delta_bias"], inp["B"], inp["C"], True, cfg.dtype)
+    idx = torch.from_numpy(rows).cuda()
+    yg = from_dev(y.reshape(cfg.batch * cfg.dim, cfg.seqlen)[idx])
+    sg = from_dev(st.reshape(cfg.batch * cfg.dim, cfg.dstate)[idx])
+    ey, es = rel_err(yg, y_ref), rel_err(sg, st_ref)
+    assert ey <= TOL[cfg.dtype], f"y rel err {ey:.3e}"
+    assert es <= TOL[cfg.dtype], f"state rel err {es:.3e}"
+
+
+def test_mamba130m_layer_full_size(ms):
+    _check_sampled(ms, synth.CONFIGS["m130"], 192)
+
+
+def test_mamba14b_layer_full_size(ms):
+    _check_sampled(ms, synth.CONFIGS["b14"], 192)

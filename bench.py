@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Throughput of the selective-scan hot path on B300.
+
+One step = one pass of the whole path over one batch of the workload: the fused forward scan over
+the sequence (Delta map, discretisation, recurrence, readout, skip, gate, final state) followed by
+one recurrent decode step that continues from the scan's final state.  Default workload: the
+Mamba-130M layer shape (batch 8, d_inner 1536, N 16, L 2048, fp32); `--workload b14` selects the
+Mamba-1.4B layer shape (batch 4, d_inner 4096, bf16 inputs, fp32 state).
+
+Prints one JSON line (rank 0).  `value` = elements (batch * d_inner * (L + 1)) per second over all
+ranks, device-timed with CUDA events, inputs resident in HBM.  `e2e` = the same metric through the
+public API with the inputs copied from pinned host memory and the outputs read back inside the
+timed region.  `--impl reference` times the fp64 CPU oracle on the host cores instead.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload on its own GPU (the
+channels of a scan are independent, so the work shards with no collective); `scaling` is "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6400.0
+METRIC = "selective-scan elements (batch*d_inner*L)/s"
+WORKLOADS = {
+    "m130": "Mamba-130M layer scan+decode: batch 8, d_inner 1536, N 16, L 2048, fp32",
+    "b14": "Mamba-1.4B layer scan+decode: batch 4, d_inner 4096, N 16, L 2048, bf16 in, fp32 state",
+    "long": "million-token scan+decode: batch 1, d_inner 1536, N 16, L 1048576, fp32",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="m130")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def esize(dtype: str) -> int:
+    return 2 if dtype == "bf16" else 4
+
+
+def scan_bytes(cfg) -> int:
+    """Algorithmic bytes of one forward scan: u, delta, z read, y written, B and C read once per
+    batch row, A/D/bias read, final state written (Abar, Bbar and h are never stored)."""
+    s = esize(cfg.dtype)
+    b, d, n, L = cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen
+    return b * d * L * 4 * s + 2 * b * n * L * s + d * (n + 2) * 4 + b * d * n * 4
+
+
+def step_bytes(cfg) -> int:
+    """Algorithmic bytes of one decode step: state read + written, x/delta/z read, y written,
+    B and C read, A/D/bias read."""
+    s = esize(cfg.dtype)
+    b, d, n = cfg.batch, cfg.dim, cfg.dstate
+    return 2 * b * d * n * 4 + b * d * 4 * s + 2 * b * n * s + d * (n + 2) * 4
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sequence_scan_selective_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the scan kernel from the committed ncu record, if it was taken on
+    the current kernel sources; otherwise None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", f"scan_fwd_{workload}.json")) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_hash") != source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples the SM clock and clock-event reasons of this process's GPU (through NVML, located by
+    PCI bus id) while the timed region runs."""
+
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "hw_power_brake": 0x80, "sw_power_cap": 0x4}
+
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.cuda_index, self.period = cuda_index, period_s
+        self.samples, self.reasons = [], set()
+        self.max_mhz, self.error = None, None
+        self._stop = threading.Event()
+        self._t = None
+
+    def __enter__(self):
+        try:
+            import pynvml as nv
+            import torch
+            nv.nvmlInit()
+            pr = torch.cuda.get_device_properties(self.cuda_index)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+            self._nv, self._h = nv, nv.nvmlDeviceGetHandleByPciBusId(bus)
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self._h, nv.NVML_CLOCK_SM)
+        except Exception as e:  # noqa: BLE001
+            self.error = f"nvml: {e!r}"
+            return self
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+        return self
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                self.reasons.update(k for k, bit in self.REASONS.items() if r & bit)
+            except Exception as e:  # noqa: BLE001
+                self.error = f"nvml sample: {e!r}"
+            time.sleep(self.period)
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._t:
+            self._t.join()
+
+    def summary(self):
+        out = {"sm_mhz": float(statistics.median(self.samples)) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        if self.error:
+            out["error"] = self.error
+        return out
+
+
+# ------------------------------------------------------------------------------------ inputs
+def host_inputs(cfg):
+    inp = synth.scan_inputs(cfg)
+    dec = synth.decode_step_inputs(cfg.replace(decode_steps=1), 0)
+    return inp, dec
+
+
+def to_torch(a: np.ndarray, dtype: str, device=None, pin=False):
+    import torch
+    if dtype == "bf16" and a.dtype == np.uint16:
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    if pin:
+        t = t.pin_memory()
+    if device is not None:
+        t = t.to(device)
+    return t
+
+
+SCAN_KEYS = ("u", "delta", "z", "B", "C")
+DEC_KEYS = ("x", "delta", "z", "B", "C")
+
+
+# ------------------------------------------------------------------------------------ our arm
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+    import sequence_scan_selective_b300 as ms
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    inp, dec = host_inputs(cfg)
+    params = {k: to_torch(inp[k], "f32", dev) for k in ("A", "D", "delta_bias")}
+    # two input sets used alternately, so no step finds the previous step's inputs in L2
+    sets = [{k: to_torch(inp[k], cfg.dtype, dev) for k in SCAN_KEYS} for _ in range(2)]
+    dsets = {k: to_torch(dec[k], cfg.dtype, dev) for k in DEC_KEYS}
+    y = torch.empty_like(sets[0]["u"])
+    state = torch.empty((cfg.batch, cfg.dim, cfg.dstate), device=dev, dtype=torch.float32)
+    ydec = torch.empty((cfg.batch, cfg.dim), device=dev, dtype=sets[0]["u"].dtype)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        s = sets[i % 2]
+        if ev is not None:
+            ev[0].record(stream)
+        ms.mamba_scan_fwd(s["u"], s["delta"], params["A"], s["B"], s["C"], params["D"], s["z"],
+                          params["delta_bias"], True, y=y, last_state=state)
+        if ev is not None:
+            ev[1].record(stream)
+        ms.mamba_state_step(state, dsets["x"], dsets["delta"], params["A"], dsets["B"], dsets["C"], params["D"],
+                            dsets["z"], params["delta_bias"], True, y=ydec)
+
+    W = max(args.warmup, 3)
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    ms.device_status()
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n0 = ms.launch_count()
+    with ClockSampler(local_rank) as clk:
+        t_start.record(stream)
+        for i in range(K):
+            step(i, evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    launches = ms.launch_count() - n0
+    if dist:
+        dist.barrier()
+    ms.device_status()
+    total_ms = t_start.elapsed_time(t_end)
+    scan_avg_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    if dist:
+        t = torch.tensor([total_ms, scan_avg_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, scan_avg_ms = float(t[0]), float(t[1])
+        lt = torch.tensor([launches], device=dev, dtype=torch.float64)
+        dist.all_reduce(lt)
+        launches = int(lt.item())
+
+    elems_step = cfg.batch * cfg.dim * (cfg.seqlen + 1)
+    value = elems_step * K * world / (total_ms * 1e-3)
+    e2e = None if args.no_e2e else run_e2e(args, cfg, inp, dec, params, dev, world, dist)
+
+    peaks, kind = measured_peaks()
+    sb = scan_bytes(cfg)
+    achieved = sb / (scan_avg_ms * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
+                "peak_source": f"{kind} hbm_gbs", "kernel": "scan_fwd_kernel",
+                "algorithmic_bytes_per_launch": sb, "kernel_avg_us": round(scan_avg_ms * 1e3, 2)}
+    line = {
+        "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded, recipe of the workload)",
+        "config": {"workload": WORKLOADS[args.workload], "batch": cfg.batch, "d_inner": cfg.dim,
+                   "d_state": cfg.dstate, "seq_len": cfg.seqlen, "storage": cfg.dtype,
+                   "step": "fwd scan (last_state) + 1 decode step from it",
+                   "elements_per_step": elems_step, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2; two input sets alternate"},
+        "roofline": roofline,
+        "clocks": clk.summary(),
+        "gpu_launches": launches,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, dec)
+    if dist:
+        dist.destroy_process_group()
+    return line
+
+
+def run_e2e(args, cfg, inp, dec, params, dev, world, dist):
+    """Public API with host buffers: pinned host -> device copies of the step's inputs, the scan and
+    the decode step, device -> host copy of both outputs, all inside the timed region."""
+    import torch
+    import sequence_scan_selective_b300 as ms
+
+    host = {k: to_torch(inp[k], cfg.dtype, pin=True) for k in SCAN_KEYS}
+    hdec = {k: to_torch(dec[k], cfg.dtype, pin=True) for k in DEC_KEYS}
+    d = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    dd = {k: torch.empty_like(v, device=dev) for k, v in hdec.items()}
+    y = torch.empty_like(d["u"])
+    ydec = torch.empty_like(dd["x"])
+    state = torch.empty((cfg.batch, cfg.dim, cfg.dstate), device=dev)
+    y_host = torch.empty_like(host["u"]).pin_memory()
+    ydec_host = torch.empty_like(hdec["x"]).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in list(host.values()) + list(hdec.values()))
+    d2h = y_host.numel() * y_host.element_size() + ydec_host.numel() * ydec_host.element_size()
+
+    def step():
+        for k in SCAN_KEYS:
+            d[k].copy_(host[k], non_blocking=True)
+        for k in DEC_KEYS:
+            dd[k].copy_(hdec[k], non_blocking=True)
+        ms.mamba_scan_fwd(d["u"], d["delta"], params["A"], d["B"], d["C"], params["D"], d["z"],
+                          params["delta_bias"], True, y=y, last_state=state)
+        ms.mamba_state_step(state, dd["x"], dd["delta"], params["A"], dd["B"], dd["C"], params["D"], dd["z"],
+                            params["delta_bias"], True, y=ydec)
+        y_host.copy_(y, non_blocking=True)
+        ydec_host.copy_(ydec, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    K = max(1, args.e2e_steps)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(K):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms_tot = a.elapsed_time(b)
+    if dist:
+        t = torch.tensor([ms_tot], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_tot = float(t[0])
+    elems = cfg.batch * cfg.dim * (cfg.seqlen + 1) * K * world
+    return {"value": elems / (ms_tot * 1e-3), "unit": "elements/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": ms_tot / K}
+
+
+# ------------------------------------------------------------------------------------ CPU oracle
+def _oracle_step(cfg, inp, dec, rows, nthreads):
+    import oracle
+    L = cfg.seqlen
+    flat = {k: inp[k].reshape(cfg.batch * cfg.dim, L)[rows] for k in ("u", "delta", "z")}
+    _, st = oracle.scan_rows(rows, cfg.dim, flat["u"], flat["delta"], flat["z"], inp["A"], inp["D"],
+                             inp["delta_bias"], inp["B"], inp["C"], True, cfg.dtype, nthreads=nthreads)
+    rb, rd = rows // cfg.dim, rows % cfg.dim
+    oracle.state_step_rows(rows, cfg.dim, st, dec["x"][rb, rd], dec["delta"][rb, rd], dec["z"][rb, rd], inp["A"],
+                           inp["D"], inp["delta_bias"], dec["B"], dec["C"], True, cfg.dtype, nthreads=nthreads)
+
+
+def _sample_rows(cfg, budget_rows):
+    n = cfg.batch * cfg.dim
+    k = int(max(1, min(n, budget_rows)))
+    return np.unique(np.linspace(0, n - 1, k).astype(np.int64))
+
+
+def cpu_baseline(cfg, inp, dec, target_s=15.0):
+    """The fp64 oracle as it stands, on the host cores, over a bounded sample of the workload's
+    channels (full sequence length each)."""
+    nthreads = os.cpu_count() or 1
+    probe = _sample_rows(cfg, max(nthreads, 16))
+    t = time.perf_counter()
+    _oracle_step(cfg, inp, dec, probe, nthreads)
+    per_row = max(time.perf_counter() - t, 1e-4) / len(probe)
+    rows = _sample_rows(cfg, target_s / per_row)
+    t = time.perf_counter()
+    _oracle_step(cfg, inp, dec, rows, nthreads)
+    dt = time.perf_counter() - t
+    return {"value": len(rows) * (cfg.seqlen + 1) / dt, "unit": "elements/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{len(rows)} of {cfg.batch * cfg.dim} channels (evenly spaced), full L={cfg.seqlen} "
+                      f"scan + 1 decode step each, {dt:.1f} s wall"}
+
+
+def run_reference(args, cfg, rank):
+    """Reference arm: the fp64 CPU oracle on the host cores, same metric and workload; each step is
+    a bounded sample of the workload's channels so the whole run ends within a few minutes."""
+    if rank != 0:
+        return None
+    inp, dec = host_inputs(cfg)
+    nthreads = os.cpu_count() or 1
+    K, W = max(1, args.steps), max(0, args.warmup)
+    probe = _sample_rows(cfg, max(nthreads, 8))
+    t = time.perf_counter()
+    _oracle_step(cfg, inp, dec, probe, nthreads)
+    per_row = max(time.perf_counter() - t, 1e-4) / len(probe)
+    rows = _sample_rows(cfg, max(1.0, (120.0 / (K + W)) / per_row))
+    for _ in range(W):
+        _oracle_step(cfg, inp, dec, rows, nthreads)
+    t = time.perf_counter()
+    for _ in range(K):
+        _oracle_step(cfg, inp, dec, rows, nthreads)
+    dt = time.perf_counter() - t
+    value = len(rows) * (cfg.seqlen + 1) * K / dt
+    sample = f"{len(rows)} of {cfg.batch * cfg.dim} channels per step, full L={cfg.seqlen} scan + 1 decode step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": args.gpus,
+        "steps": K, "warmup": W, "ms_per_step": dt / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, recipe of the workload)",
+        "config": {"workload": WORKLOADS[args.workload], "batch": cfg.batch, "d_inner": cfg.dim,
+                   "d_state": cfg.dstate, "seq_len": cfg.seqlen, "storage": cfg.dtype},
+        "cpu_baseline": {"value": value, "unit": "elements/s", "cores": nthreads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = synth.CONFIGS[args.workload]
+    line = run_reference(args, cfg, rank) if args.impl == "reference" else run_ours(args, cfg, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -47,7 +47,7 @@ WORKLOADS = {
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="m130")
@@ -120,6 +120,7 @@ class ClockSampler:
         self.cuda_index, self.period = cuda_index, period_s
         self.samples, self.reasons = [], set()
         self.max_mhz, self.error = None, None
+        self.t0 = self.t1 = time.time()
         self._stop = threading.Event()
         self._t = None
 
@@ -144,7 +145,7 @@ class ClockSampler:
     def _start_smi(self, why: str):
         """Fallback: nvidia-smi sampling every 20 ms in a child process."""
         self.error = why + "; sampled with nvidia-smi"
-        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+        q = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.hw_power_brake_slowdown,"
              "clocks_event_reasons.sw_power_cap")
         try:
@@ -168,6 +169,13 @@ class ClockSampler:
                 self.error = f"nvml sample: {e!r}"
             time.sleep(self.period)
 
+    def mark(self, begin: bool):
+        """Wall-clock bounds of the timed region (nvidia-smi samples outside them are dropped)."""
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
     def __exit__(self, *exc):
         self._stop.set()
         if self._t:
@@ -177,16 +185,20 @@ class ClockSampler:
             smi.terminate()
             out, _ = smi.communicate(timeout=10)
             names = ["hw_slowdown", "sw_thermal_slowdown", "hw_thermal_slowdown", "hw_power_brake", "sw_power_cap"]
+            import datetime
             for ln in out.splitlines():
                 f = [x.strip() for x in ln.split(",")]
-                if len(f) < 7:
+                if len(f) < 8:
                     continue
                 try:
-                    self.samples.append(float(f[0]))
-                    self.max_mhz = float(f[1])
+                    ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    mhz, self.max_mhz = float(f[1]), float(f[2])
                 except ValueError:
                     continue
-                self.reasons.update(n for n, v in zip(names, f[2:7]) if v.lower() == "active")
+                if not (self.t0 - 0.05 <= ts <= self.t1 + 0.05):
+                    continue  # keep samples taken while the timed region ran
+                self.samples.append(mhz)
+                self.reasons.update(n for n, v in zip(names, f[3:8]) if v.lower() == "active")
 
     def summary(self):
         out = {"sm_mhz": float(statistics.median(self.samples)) if self.samples else None,
@@ -267,11 +279,13 @@ def run_ours(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     n0 = ms.launch_count()
     with ClockSampler(local_rank) as clk:
+        clk.mark(True)
         t_start.record(stream)
         for i in range(K):
             step(i, evs[i])
         t_end.record(stream)
         torch.cuda.synchronize()
+        clk.mark(False)
     launches = ms.launch_count() - n0
     if dist:
         dist.barrier()

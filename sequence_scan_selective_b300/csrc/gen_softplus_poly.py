@@ -1,7 +1,7 @@
 """Derive the polynomial used by the kernels' softplus.
 
 softplus(x) = max(x, 0) + log1p(e) with e = exp(-|x|) in (0, 1].  log1p(e) = e * P(e), where P is
-the degree-8 Chebyshev interpolant of log1p(e)/e on [0, 1], rewritten in the monomial basis and
+the degree-6 Chebyshev interpolant of log1p(e)/e on [0, 1], rewritten in the monomial basis and
 rounded to fp32.  Run this script to print the coefficients (lowest order first) and the fp32
 Horner error against numpy's log1p.
 """
@@ -9,7 +9,7 @@ import numpy as np
 from numpy.polynomial import chebyshev as Ch
 from numpy.polynomial import polynomial as Po
 
-DEG = 8
+DEG = 6
 
 
 def coefficients(deg=DEG):

@@ -13,6 +13,7 @@
 #include <string>
 
 #include "mamba_scan.h"
+#include "common.cuh"
 #include "scan_fwd.cuh"
 #include "state_step.cuh"
 
@@ -50,9 +51,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 3-D map over a dense [d2][d1][d0] tensor (d0 contiguous) with box [b1 rows x b0 cols].
+// 3-D map over a dense [d2][d1][d0] tensor (d0 contiguous), box [b1 rows x b0 cols], 128-byte
+// swizzle (b0 * esize must be 128).
 static bool encode_3d(CUtensorMap* m, const void* base, int esize, long long d0, long long d1, long long d2,
-                      int b0, int b1, bool swizzle64) {
+                      int b0, int b1) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
@@ -61,68 +63,143 @@ static bool encode_3d(CUtensorMap* m, const void* base, int esize, long long d0,
     cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType dt = esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUresult r = fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// ---------------------------------------------------------------------------- forward launch
-template <typename TIn, int NP, int G, int CH, int TC, int NSTAGE, bool TMA, bool AGG>
-static int launch_fwd_one(const FwdArgs& a, dim3 grid, const CUtensorMap* maps, cudaStream_t st) {
-    using SM = FwdSmem<TIn, NP, G, CH, TC, NSTAGE>;
-    auto kern = scan_fwd_kernel<TIn, NP, G, CH, TC, NSTAGE, TMA, AGG>;
-    const int smem_bytes = SM::kBytes + 1024;  // slack to align the swizzled tiles
-    static bool attr_set = false;              // benign race: every caller sets the same value
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-        attr_set = true;
+static int env_int(const char* name, int dflt) {
+    const char* v = getenv(name);
+    return (v && *v) ? atoi(v) : dflt;
+}
+
+// ---------------------------------------------------------------------------- forward plan
+constexpr int kSmemLimit = 227 * 1024;
+
+struct FwdPlan {
+    int nseg;
+    long long seg_len;
+    int upr, kcta, wmax, wlo, nstage;
+    int stage_bytes, bc_off, quad_off, scratch_off, bar_off, smem_bytes;
+};
+
+// Work split.  Units (8 channels of one batch row, one consumer warp each) are the grain.  The
+// time axis is split into segments only when the units alone cannot give every SM several warps
+// (a split costs one extra pass over delta, u and B for all but the last segment).  Each
+// (segment, batch row) gets kcta CTAs with an even share of its units, so that the grid is about
+// one CTA per SM and the per-SM work differs by at most one unit.
+template <typename TIn, int NP>
+static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
+    constexpr int TC = Chunk<TIn>::TC;
+    const long long L = s->seqlen;
+    p.upr = (s->dim + kUnitCh - 1) / kUnitCh;
+    const long long units = (long long)s->batch * p.upr;
+    long long want = env_int("MAMBA_SCAN_NSEG", 0);
+    if (want <= 0) {
+        want = 1;
+        const long long target = (long long)nsm * 10;  // consumer warps that keep every SM busy
+        if (units * 2 < target) want = (target + units - 1) / units;
     }
-    kern<<<grid, CH * (NP / G) + 32, smem_bytes, st>>>(a, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5]);
+    long long maxseg = L / (8LL * TC);
+    if (maxseg < 1) maxseg = 1;
+    if (want > maxseg) want = maxseg;
+    if (want > 4096) want = 4096;
+    p.nseg = 1;
+    p.seg_len = L;
+    if (want > 1) {
+        long long seg = (L + want - 1) / want;
+        seg = (seg + TC - 1) / TC * TC;
+        p.seg_len = seg;
+        p.nseg = (int)((L + seg - 1) / seg);
+    }
+    const long long rows = (long long)s->batch * p.nseg;
+    const int wforce = env_int("MAMBA_SCAN_WMAX", 0);
+    long long k;
+    if (wforce > 0) {
+        k = (p.upr + wforce - 1) / wforce;
+    } else {
+        k = rows >= nsm ? 1 : nsm / rows;
+        if (k > p.upr) k = p.upr;
+        if ((p.upr + k - 1) / k > kMaxConsumerWarps) k = (p.upr + kMaxConsumerWarps - 1) / kMaxConsumerWarps;
+    }
+    if (k < 1) k = 1;
+    p.kcta = (int)k;
+    p.wmax = (int)((p.upr + k - 1) / k);
+    if (p.wmax > kMaxConsumerWarps) return fail(MAMBA_ERR_ARG, "MAMBA_SCAN_WMAX above %d", kMaxConsumerWarps);
+    p.wlo = p.upr / p.kcta;
+    if (rows * k > 0x7fffffffLL) return fail(MAMBA_ERR_ARG, "grid too large");
+
+    // shared memory: NS stages of [u | delta | z tiles (1 KB per unit each) | B, C tiles | quads],
+    // then per-warp scratch, then 3 NS mbarriers
+    p.bc_off = 3 * p.wmax * 1024;
+    p.quad_off = p.bc_off + 2 * NP * 128;
+    p.stage_bytes = (p.quad_off + TC * (NP / 2) * 16 + 1023) / 1024 * 1024;
+    const int fixed = p.wmax * kWarpScratch + 1024 /* alignment slack */;
+    int ns = env_int("MAMBA_SCAN_STAGES", 4);
+    while (ns > 2 && fixed + ns * (p.stage_bytes + 24) > kSmemLimit) --ns;
+    if (ns < 2) ns = 2;
+    p.nstage = ns;
+    p.scratch_off = ns * p.stage_bytes;
+    p.bar_off = p.scratch_off + p.wmax * kWarpScratch;
+    p.smem_bytes = p.bar_off + 3 * ns * 8 + 1024;
+    if (p.smem_bytes > kSmemLimit) return fail(MAMBA_ERR_ARG, "tiling needs %d bytes of shared memory", p.smem_bytes);
+    return MAMBA_OK;
+}
+
+// Raises a kernel's dynamic shared memory limit once per device (the attribute is per function
+// and context; setting it on every call costs tens of microseconds of host time).
+template <typename K>
+static int allow_smem(K kern, std::atomic<unsigned long long>& done_mask) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (done_mask.load(std::memory_order_acquire) & bit) return MAMBA_OK;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    done_mask.fetch_or(bit, std::memory_order_acq_rel);
+    return MAMBA_OK;
+}
+
+template <typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE>
+static int launch_fwd_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
+    static std::atomic<unsigned long long> attr_done{0};
+    auto kern = scan_fwd_kernel<TIn, NP, TMA, AGG, SP, GATE>;
+    int rc = allow_smem(kern, attr_done);
+    if (rc) return rc;
+    kern<<<grid, 32 * (a.wmax + 1), smem_bytes, st>>>(a, maps);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "scan_fwd_kernel launch");
     return MAMBA_OK;
 }
 
-struct FwdPlan {
-    int nseg;
-    long long seg_len;
-};
-
-// Split the time axis only when the channels alone cannot fill the GPU: a split costs one extra
-// pass over delta, u and B for all but the last segment.
-static FwdPlan plan_split(long long channels, int threads_per_channel, long long L, int TC, int nsm) {
-    FwdPlan p{1, L};
-    const char* force = getenv("MAMBA_SCAN_NSEG");
-    long long want = 1;
-    if (force && atoi(force) > 0) {
-        want = atoi(force);
+// Selects the instantiation for the runtime flags (data path, softplus, gate).
+template <typename TIn, int NP, bool AGG>
+static int launch_fwd(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, bool tma, bool sp,
+                      bool gate, cudaStream_t st) {
+    if constexpr (AGG) {  // the aggregate pass reads no z
+        if (tma) return sp ? launch_fwd_one<TIn, NP, true, true, true, false>(a, maps, grid, smem_bytes, st)
+                           : launch_fwd_one<TIn, NP, true, true, false, false>(a, maps, grid, smem_bytes, st);
+        return sp ? launch_fwd_one<TIn, NP, false, true, true, false>(a, maps, grid, smem_bytes, st)
+                  : launch_fwd_one<TIn, NP, false, true, false, false>(a, maps, grid, smem_bytes, st);
     } else {
-        const long long target = (long long)nsm * 192;  // scan threads that keep every SM busy
-        const long long have = channels * threads_per_channel;
-        if (have < target / 2) want = (target + have - 1) / have;
+        if (tma) {
+            if (sp) return gate ? launch_fwd_one<TIn, NP, true, false, true, true>(a, maps, grid, smem_bytes, st)
+                                : launch_fwd_one<TIn, NP, true, false, true, false>(a, maps, grid, smem_bytes, st);
+            return gate ? launch_fwd_one<TIn, NP, true, false, false, true>(a, maps, grid, smem_bytes, st)
+                        : launch_fwd_one<TIn, NP, true, false, false, false>(a, maps, grid, smem_bytes, st);
+        }
+        if (sp) return gate ? launch_fwd_one<TIn, NP, false, false, true, true>(a, maps, grid, smem_bytes, st)
+                            : launch_fwd_one<TIn, NP, false, false, true, false>(a, maps, grid, smem_bytes, st);
+        return gate ? launch_fwd_one<TIn, NP, false, false, false, true>(a, maps, grid, smem_bytes, st)
+                    : launch_fwd_one<TIn, NP, false, false, false, false>(a, maps, grid, smem_bytes, st);
     }
-    const long long min_seg = 16LL * TC;
-    long long maxseg = L / min_seg;
-    if (maxseg < 1) maxseg = 1;
-    if (want > maxseg) want = maxseg;
-    if (want > 4096) want = 4096;
-    if (want <= 1) return p;
-    long long seg = (L + want - 1) / want;
-    seg = (seg + TC - 1) / TC * TC;
-    p.seg_len = seg;
-    p.nseg = (int)((L + seg - 1) / seg);
-    return p;
 }
 
-// One tiling of the forward kernel: G states per thread, CH channels per CTA, TC steps per chunk,
-// NSTAGE-deep TMA ring.
-template <typename TIn, int NP, int G, int CH, int TC, int NSTAGE>
-static int fwd_run(const mamba_scan_shape* s, FwdArgs a, cudaStream_t st) {
-    constexpr int S = NP / G;
+template <typename TIn, int NP>
+static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gate, cudaStream_t st) {
+    constexpr int TC = Chunk<TIn>::TC;
     const int esize = (int)sizeof(TIn);
     const long long L = s->seqlen;
 
@@ -130,42 +207,54 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, cudaStream_t st) {
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
 
+    FwdPlan p;
+    int rc = plan_fwd<TIn, NP>(s, nsm, p);
+    if (rc) return rc;
+
     const bool tma_ok = encode_fn() != nullptr && (L * esize) % 16 == 0 && aligned16(a.u) && aligned16(a.delta) &&
                         aligned16(a.B) && aligned16(a.C) && aligned16(a.y) && (a.z == nullptr || aligned16(a.z)) &&
                         L < (1LL << 31) && getenv("MAMBA_SCAN_NO_TMA") == nullptr;
-    CUtensorMap maps[6];
-    memset(maps, 0, sizeof maps);
+    FwdMaps maps;
+    memset(&maps, 0, sizeof maps);
     if (tma_ok) {
         const void* zb = a.z ? a.z : a.u;
-        bool ok = encode_3d(&maps[0], a.u, esize, L, s->dim, s->batch, TC, CH, true) &&
-                  encode_3d(&maps[1], a.delta, esize, L, s->dim, s->batch, TC, CH, true) &&
-                  encode_3d(&maps[2], zb, esize, L, s->dim, s->batch, TC, CH, true) &&
-                  encode_3d(&maps[3], a.B, esize, L, s->dstate, s->batch, TC, s->dstate, false) &&
-                  encode_3d(&maps[4], a.C, esize, L, s->dstate, s->batch, TC, s->dstate, false) &&
-                  encode_3d(&maps[5], a.y, esize, L, s->dim, s->batch, TC, CH, true);
+        const void* src[3] = {a.u, a.delta, zb};
+        CUtensorMap* dst[3] = {maps.u, maps.d, maps.z};
+        bool ok = true;
+        for (int m = 0; m < 3 && ok; ++m)
+            for (int w = 0; w < 2 && ok; ++w) {
+                const int rowsbox = kUnitCh * (w == 0 ? (p.wlo > 0 ? p.wlo : 1) : p.wlo + 1);
+                ok = encode_3d(&dst[m][w], src[m], esize, L, s->dim, s->batch, TC, rowsbox > 256 ? 256 : rowsbox);
+            }
+        ok = ok && encode_3d(&maps.B, a.B, esize, L, s->dstate, s->batch, TC, s->dstate) &&
+             encode_3d(&maps.C, a.C, esize, L, s->dstate, s->batch, TC, s->dstate);
         if (!ok) return fail(MAMBA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
 
-    const long long nblk = (s->dim + CH - 1) / CH;
-    const FwdPlan plan = plan_split((long long)s->batch * s->dim, S, L, TC, nsm);
-    a.nseg = plan.nseg;
-    a.seg_len = plan.seg_len;
+    a.nseg = p.nseg;
+    a.seg_len = p.seg_len;
+    a.upr = p.upr;
+    a.kcta = p.kcta;
+    a.wmax = p.wmax;
+    a.wlo = p.wlo;
+    a.nstage = p.nstage;
+    a.stage_bytes = p.stage_bytes;
+    a.bc_off = p.bc_off;
+    a.quad_off = p.quad_off;
+    a.scratch_off = p.scratch_off;
+    a.bar_off = p.bar_off;
     a.agg = nullptr;
-    if (plan.nseg > 65535 || s->batch > 65535) return fail(MAMBA_ERR_ARG, "grid too large");
 
-    int rc = MAMBA_OK;
-    if (plan.nseg > 1) {
-        const size_t bytes = (size_t)(plan.nseg - 1) * s->batch * s->dim * s->dstate * sizeof(float2);
+    if (p.nseg > 1) {
+        const size_t bytes = (size_t)(p.nseg - 1) * s->batch * s->dim * s->dstate * sizeof(float2);
         cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&a.agg), bytes, st);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (segment carries)");
-        dim3 g1((unsigned)nblk, (unsigned)s->batch, (unsigned)(plan.nseg - 1));
-        rc = tma_ok ? launch_fwd_one<TIn, NP, G, CH, TC, NSTAGE, true, true>(a, g1, maps, st)
-                    : launch_fwd_one<TIn, NP, G, CH, TC, NSTAGE, false, true>(a, g1, maps, st);
+        const unsigned g1 = (unsigned)((long long)s->batch * (p.nseg - 1) * p.kcta);
+        rc = launch_fwd<TIn, NP, true>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
     }
     if (rc == MAMBA_OK) {
-        dim3 g2((unsigned)nblk, (unsigned)s->batch, (unsigned)plan.nseg);
-        rc = tma_ok ? launch_fwd_one<TIn, NP, G, CH, TC, NSTAGE, true, false>(a, g2, maps, st)
-                    : launch_fwd_one<TIn, NP, G, CH, TC, NSTAGE, false, false>(a, g2, maps, st);
+        const unsigned g2 = (unsigned)((long long)s->batch * p.nseg * p.kcta);
+        rc = launch_fwd<TIn, NP, false>(a, maps, g2, p.smem_bytes, tma_ok, softplus, gate, st);
     }
     if (a.agg) {
         cudaError_t e = cudaFreeAsync(a.agg, st);
@@ -174,20 +263,9 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, cudaStream_t st) {
     return rc;
 }
 
-static int variant() {
-    const char* v = getenv("MAMBA_SCAN_VARIANT");
-    return v ? atoi(v) : 0;
-}
-
 template <typename TIn, int NP>
-static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, cudaStream_t st) {
-    // 64-byte tile rows: 32 bf16 or 16 fp32 steps per chunk
-    constexpr int TC = sizeof(TIn) == 2 ? 32 : 16;
-    constexpr int NSTAGE = sizeof(TIn) == 2 ? 3 : 4;
-    if constexpr (NP == 16) {
-        if (variant() == 1) return fwd_run<TIn, 16, 4, 32, TC, NSTAGE>(s, a, st);
-    }
-    return fwd_run<TIn, NP, 8, 32, TC, NSTAGE>(s, a, st);
+static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, bool gate, cudaStream_t st) {
+    return fwd_run<TIn, NP>(s, a, softplus, gate, st);
 }
 
 // ---------------------------------------------------------------------------- checks
@@ -260,12 +338,13 @@ extern "C" int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const vo
     a.y = y; a.last_state = last_state;
     a.batch = s->batch; a.dim = s->dim; a.dstate = s->dstate;
     a.L = s->seqlen;
-    a.softplus = softplus_flag != 0;
-    a.has_z = z != nullptr;
+    const bool sp = softplus_flag != 0, gate = z != nullptr;
     const bool bf = s->in_dtype == MAMBA_BF16;
-    if (s->dstate <= 16) return bf ? fwd_dispatch<uint16_t, 16>(s, a, st) : fwd_dispatch<float, 16>(s, a, st);
-    if (s->dstate <= 32) return bf ? fwd_dispatch<uint16_t, 32>(s, a, st) : fwd_dispatch<float, 32>(s, a, st);
-    return bf ? fwd_dispatch<uint16_t, 64>(s, a, st) : fwd_dispatch<float, 64>(s, a, st);
+    if (s->dstate <= 16)
+        return bf ? fwd_dispatch<uint16_t, 16>(s, a, sp, gate, st) : fwd_dispatch<float, 16>(s, a, sp, gate, st);
+    if (s->dstate <= 32)
+        return bf ? fwd_dispatch<uint16_t, 32>(s, a, sp, gate, st) : fwd_dispatch<float, 32>(s, a, sp, gate, st);
+    return bf ? fwd_dispatch<uint16_t, 64>(s, a, sp, gate, st) : fwd_dispatch<float, 64>(s, a, sp, gate, st);
 }
 
 extern "C" int mamba_state_step(const mamba_scan_shape* s, float* state, const void* x, const void* delta,

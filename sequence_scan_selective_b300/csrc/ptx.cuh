@@ -101,6 +101,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// MUFU reciprocal (flush-to-zero).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
     float2 d;
     asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
@@ -129,6 +136,12 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
+}
+
+// Byte offset of (row, byte) in a tile written by TMA with the 128-byte swizzle: the 16-byte chunk
+// index (bits 4-6) is XORed with the row index modulo 8 (bits 7-9 of a 1024-byte aligned tile).
+__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t byte) {
+    return row * 128u + ((((byte >> 4) ^ row) & 7u) << 4) + (byte & 15u);
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` lands in the low half.

@@ -1,40 +1,55 @@
-// Fused selective-scan forward kernel: discretisation + diagonal recurrence + readout + skip + gate.
+// Fused selective-scan forward kernel: step-size map + discretisation + diagonal recurrence +
+// readout + skip + gate, with the state kept in registers.
 //
 // Follows the hardware-aware design described for Mamba's selective SSM (visual guide to Mamba and
-// SSMs, section 3.4; news write-up, "hardware-aware algorithm"): the step-size map, the
-// discretisation Abar = exp(Delta A) / Bbar x = Delta B x, the recurrence and the multiplication by C
-// run in one kernel; the expanded state h [b, d, N, L] and Abar, Bbar never leave the chip.
+// SSMs, section 3.4; news write-up, "hardware-aware algorithm"): Abar = exp(Delta A) and
+// Bbar x = Delta B x are formed on chip, the recurrence h_t = Abar_t h_{t-1} + Bbar_t x_t runs
+// there, and only y = (C h + D x) silu(z) and the final state leave the SM.  The expanded state
+// [b, d, N, L] and Abar, Bbar never touch memory.
 //
-// B300 mapping (warp-specialised)
-//  * A CTA owns CH = 32 channels of one batch row and walks its time range in chunks of TC steps.
-//  * One helper warp (lane = channel) moves data and does the per-element work:
-//      - issues TMA loads (cp.async.bulk.tensor, 64-byte swizzle) of u, delta, z [CH x TC] and
-//        B, C [N x TC] into an NSTAGE-deep ring guarded by mbarriers;
-//      - produce: per slot of U = 8 steps, turns (delta, u) into (Delta, Delta, Delta*u, Delta*u)
-//        fp32 quads (softplus + bias), B and C into (B_n, B_n+1, C_n, C_n+1) quads per step, and
-//        z, u into (D*u, silu(z)) pairs, all in a ring of R slot buffers;
-//      - post: sums the scan threads' partial C.h of a slot, applies the skip term and the gate,
-//        writes the output tile (same swizzle) and sends each finished chunk to y by TMA store.
-//  * Scan warps: each thread holds G states of one channel in registers and advances them
-//    sequentially in time with packed fp32x2 arithmetic (MUFU ex2 for Abar); S = NP/G threads
-//    share a channel and leave their partial sums per step in the slot.  They never touch global
-//    memory in the loop and synchronise with the helper only through the slot mbarriers.
-//  * Few channels (long sequences): the time axis is split into segments.  An AGG launch computes
-//    each segment's carry (prod Abar = exp(A * sum Delta), h_end from zero); the full launch folds
-//    the carries of the preceding segments into its initial state (the scan operator is
-//    associative; guide section 3.3).
+// B300 mapping
+//  * Work unit = 8 channels of one batch row, owned by one warp for the whole time range.  Each
+//    channel's N states are split over 4 lanes (G = N/4 consecutive states per lane), so one lane
+//    holds G fp32 states and advances them sequentially in time with packed f32x2 arithmetic and
+//    the MUFU base-2 exponential.  Lane (c, g) = (lane % 8, lane / 8).
+//  * CTA = one producer warp + up to 15 consumer warps covering a contiguous range of units of
+//    one batch row.  The host sizes the grid so that one CTA runs per SM and splits each batch
+//    row's units evenly over its CTAs (work per SM differs by at most one unit).
+//  * The producer streams chunks of TC steps (128 bytes of each row: 32 fp32 / 64 bf16 steps) of
+//    u, delta, z (one [8 x units, TC] box each) and B, C ([N, TC]) with TMA (128-byte swizzle)
+//    into an NS-deep ring of stages, guarded by mbarriers, and rewrites the chunk's B, C as
+//    (B_n, B_n+1, C_n, C_n+1) fp32 quads per step so that consumers read one quad per state pair.
+//  * Consumers walk each chunk in slots of 16 steps, in three phases per slot:
+//      A  lane (c, g) forms Delta = softplus(delta + bias), Delta*u, D*u and silu(z) for its 4
+//         owned steps (16-byte tile reads), and publishes (Delta, Delta, Delta*u, Delta*u)
+//         quads in the warp's scratch;
+//      B  all lanes advance their G states through the 16 steps (one quad of Delta per step, one
+//         B/C quad per state pair), leaving per-step partial sums of C.h;
+//      C  lane (c, g) sums the 4 partials of its owned steps, adds D*u, applies the gate and
+//         stores y with one 128-bit (fp32) or 64-bit (bf16) store.
+//  * Few channels (long sequences): the time axis is split into segments.  An aggregate launch
+//    computes each segment's carry (prod Abar = 2^(A log2e sum Delta), h_end from zero); the full
+//    launch folds the carries of the preceding segments into its initial state.  This regroups
+//    the scan operator (a2, b2) o (a1, b1) = (a1 a2, a2 b1 + b2), which is associative (guide
+//    section 3.3).
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
 
-#include "ptx.cuh"
+#include "common.cuh"
 
 namespace mscan {
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s bound on any wait
-
-__device__ int g_status;  // nonzero: some kernel abandoned a bounded wait
+constexpr int kUnitCh = 8;      // channels per work unit (one warp)
+constexpr int kLanesPerCh = 4;  // lanes sharing one channel's states
+constexpr int kSlot = 16;       // steps per slot
+constexpr int kOwned = kSlot / kLanesPerCh;  // steps whose per-element work a lane does
+constexpr int kQPitch = kSlot * 16 + 16;     // bytes per channel row of Delta quads (padded)
+constexpr int kYPitch = kSlot * 4 + 16;      // bytes per (lane group, channel) row of partials
+constexpr int kQBuf = kUnitCh * kQPitch;       // one buffer of Delta quads (8 channels)
+constexpr int kWarpScratch = 2 * kQBuf + kLanesPerCh * kUnitCh * kYPitch;  // 6912 bytes
+constexpr int kMaxConsumerWarps = 15;
+constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
 
 struct FwdArgs {
     const void* u;
@@ -47,361 +62,202 @@ struct FwdArgs {
     const float* bias;
     void* y;
     float* last_state;
-    float2* agg;  // [nseg-1][batch][dim][dstate] (prod Abar, h_end)
+    float2* agg;  // [nseg-1][batch][dim][dstate]: (prod Abar, h_end) of each segment
     int batch, dim, dstate;
     long long L;
-    long long seg_len;  // multiple of TC
+    long long seg_len;  // multiple of the chunk length
     int nseg;
-    int softplus;
-    int has_z;
+    int upr;     // work units per batch row = ceil(dim / 8)
+    int kcta;    // CTAs per (segment, batch row)
+    int wmax;    // consumer warps per CTA; warp wmax is the producer
+    int wlo;     // CTAs with this many units use the narrow u/delta/z maps (index 0)
+    int nstage;  // stages in the ring
+    int stage_bytes, bc_off, quad_off, scratch_off, bar_off;
 };
 
-// ------------------------------------------------------------------------------ element access
-template <typename TIn>
-struct In;
-template <>
-struct In<float> {
-    __device__ static __forceinline__ float to_f32(float x) { return x; }
-    // 8 consecutive values from two 16-byte chunks
-    __device__ static __forceinline__ void unpack8(const uint4& a, const uint4& b, float* v) {
-        v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y); v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
-        v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y); v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
-    }
-    __device__ static __forceinline__ void pack8(const float* v, uint4& a, uint4& b) {
-        a = make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
-        b = make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]), __float_as_uint(v[6]), __float_as_uint(v[7]));
-    }
-};
-template <>
-struct In<uint16_t> {
-    __device__ static __forceinline__ float to_f32(uint16_t x) { return bf16_bits_to_f32(x); }
-    __device__ static __forceinline__ void unpack8(const uint4& a, const uint4&, float* v) {
-        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[2 * i] = __uint_as_float(w[i] << 16);
-            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-        }
-    }
-    __device__ static __forceinline__ void pack8(const float* v, uint4& a, uint4&) {
-        a = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                       pack_bf16x2(v[6], v[7]));
-    }
+// u, delta, z maps: [0] box of 8*wlo rows, [1] box of 8*(wlo+1) rows; B, C: box [N, TC].
+struct FwdMaps {
+    CUtensorMap u[2], d[2], z[2], B, C;
 };
 
+// Steps per chunk: one 128-byte row of each input.
 template <typename TIn>
-__device__ __forceinline__ void store_out(TIn* p, float v);
+struct Chunk {
+    static constexpr int TC = 128 / (int)sizeof(TIn);
+    static constexpr int SPC = TC / kSlot;  // slots per chunk
+};
+
+// 4 consecutive elements at byte `byte` of row `row` of a 128-byte-swizzled tile -> fp32
+template <typename TIn>
+__device__ __forceinline__ void tile_load4(const unsigned char* tile, int row, int byte, float* v);
 template <>
-__device__ __forceinline__ void store_out<float>(float* p, float v) { *p = v; }
+__device__ __forceinline__ void tile_load4<float>(const unsigned char* tile, int row, int byte, float* v) {
+    const float4 q = *reinterpret_cast<const float4*>(tile + swz128(row, byte));
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
 template <>
-__device__ __forceinline__ void store_out<uint16_t>(uint16_t* p, float v) {
-    *p = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xffffu);
+__device__ __forceinline__ void tile_load4<uint16_t>(const unsigned char* tile, int row, int byte, float* v) {
+    const uint2 q = *reinterpret_cast<const uint2*>(tile + swz128(row, byte));
+    v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
 }
 
-// ------------------------------------------------------------------------------ step size, gate
-// softplus(x) = max(x, 0) + log1p(e), e = exp(-|x|) in (0, 1]; log1p(e) = e * P(e) with P the
-// degree-8 Chebyshev interpolant of log1p(e)/e on [0, 1] (coefficients from gen_softplus_poly.py;
-// fp32 relative error of the log1p term below 3e-7).  NaN propagates through e.
-__device__ __forceinline__ float2 softplus2(float2 x) {
-    const float2 e = make_float2(ex2_approx(-fabsf(x.x) * kLog2e), ex2_approx(-fabsf(x.y) * kLog2e));
-    float2 p = make_float2(0.005126102f, 0.005126102f);
-    p = ffma2(p, e, make_float2(-0.029074065f, -0.029074065f));
-    p = ffma2(p, e, make_float2(0.07751609f, 0.07751609f));
-    p = ffma2(p, e, make_float2(-0.13602248f, -0.13602248f));
-    p = ffma2(p, e, make_float2(0.19076881f, 0.19076881f));
-    p = ffma2(p, e, make_float2(-0.24835399f, -0.24835399f));
-    p = ffma2(p, e, make_float2(0.3331812f, 0.3331812f));
-    p = ffma2(p, e, make_float2(-0.49999446f, -0.49999446f));
-    p = ffma2(p, e, make_float2(0.99999994f, 0.99999994f));
-    return ffma2(e, p, make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+// 4 outputs at p (aligned to 4 elements)
+template <typename TIn>
+__device__ __forceinline__ void store4(TIn* p, const float* v);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, const float* v) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void store4<uint16_t>(uint16_t* p, const float* v) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
 }
 
-__device__ __forceinline__ float softplus1(float x) { return softplus2(make_float2(x, x)).x; }
-
-// silu(z) = z * sigmoid(z) = z / (1 + e^-z)
-__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.f + ex2_approx(-z * kLog2e)); }
-
-// ------------------------------------------------------------------------------ smem geometry
-// Tiles of u, delta, z and y are [CH rows][TC cols] with 64-byte rows stored with the TMA 64-byte
-// swizzle: the 16-byte chunk index (address bits 4-5) is XORed with address bits 7-8.  Rows are
-// read and written whole by one helper lane each, so 8 lanes touching the same logical chunk of 8
-// consecutive rows hit 8 different bank groups.
-__device__ __forceinline__ uint32_t swz64(uint32_t off) { return off ^ (((off >> 7) & 3u) << 4); }
-
-template <typename TIn, int NP, int G, int CH, int TC, int NS>
-struct FwdSmem {
-    static constexpr int S = NP / G;
-    static constexpr int U = 8;                                  // steps per slot
-    static constexpr int R = 2;                                  // slots in the ring
-    static constexpr int kRow = TC * (int)sizeof(TIn);           // bytes per tile row (64)
-    static constexpr int kTile = CH * kRow;                      // one u/delta/z tile
-    static constexpr int kBC = NP * kRow;                        // one B or C tile (N <= NP rows)
-    static constexpr int kStage = (3 * kTile + 2 * kBC + 1023) / 1024 * 1024;
-    static constexpr int kQPitch = U * 16 + 16;                  // (Dt,Dt,Du,Du) quads per channel
-    static constexpr int kBCPitch = NP * 8 + 16;                 // (B,B,C,C) quads per step
-    static constexpr int kYPitch = U * 4 + 16;                   // partial sums per scan thread
-    static constexpr int kZPitch = U * 8 + 16;                   // (D u, silu z) per channel
-    static constexpr int kSlotQ = CH * kQPitch;
-    static constexpr int kSlotBC = U * kBCPitch;
-    static constexpr int kSlotY = CH * S * kYPitch;
-    static constexpr int kSlotZ = CH * kZPitch;
-    static constexpr int kSlot = kSlotQ + kSlotBC + kSlotY + kSlotZ;
-    static constexpr int kOffSlots = NS * kStage;
-    static constexpr int kOffOut = (kOffSlots + R * kSlot + 1023) / 1024 * 1024;  // 2 output tiles
-    static constexpr int kOffBar = kOffOut + 2 * kTile;
-    static constexpr int kBars = NS + 2 * R;
-    static constexpr int kBytes = kOffBar + kBars * 8;
-    static_assert(kRow == 64, "tile rows must be 64 bytes (64-byte TMA swizzle)");
-    static_assert(kSlot % 16 == 0 && kTile % 1024 == 0, "alignment");
-};
-
-template <typename TIn, int NP, int G, int CH, int TC, int NSTAGE, bool TMA, bool AGG>
-__global__ void __launch_bounds__(CH*(NP / G) + 32, 1)
-    scan_fwd_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tm_u,
-                    const __grid_constant__ CUtensorMap tm_d, const __grid_constant__ CUtensorMap tm_z,
-                    const __grid_constant__ CUtensorMap tm_B, const __grid_constant__ CUtensorMap tm_C,
-                    const __grid_constant__ CUtensorMap tm_y) {
-    using SM = FwdSmem<TIn, NP, G, CH, TC, NSTAGE>;
-    constexpr int S = SM::S;         // scan threads per channel
-    constexpr int NSCAN = CH * S;    // scan threads (warps 0 .. NSCAN/32-1); the last warp helps
-    constexpr int U = SM::U;
-    constexpr int R = SM::R;
-    constexpr int NS = NSTAGE;
-    constexpr int SPC = TC / U;      // slots per chunk
-    constexpr int VPR = U * (int)sizeof(TIn) / 16;  // 16-byte chunks per slot row (1 bf16, 2 fp32)
-    static_assert(CH == 32, "one helper warp: lane = channel");
-    static_assert(G % 2 == 0 && 32 % S == 0 && NSCAN % 32 == 0 && TC % U == 0 && NS >= 2, "shape");
+template <typename TIn, int NP, bool TMA, bool AGG, bool SOFTPLUS, bool GATE>
+__global__ void __launch_bounds__(kMaxThreads, 1)
+    scan_fwd_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps) {
+    constexpr int G = NP / kLanesPerCh;  // states per lane
+    constexpr int NPAIR = NP / 2;
+    constexpr int TC = Chunk<TIn>::TC;
+    constexpr int SPC = Chunk<TIn>::SPC;
+    constexpr int ES = (int)sizeof(TIn);
+    static_assert(G % 2 == 0 && TC % kSlot == 0, "shape");
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // swizzled TMA tiles need 1024-byte alignment; the launch reserves 1 KB of slack for this
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint64_t* tma_full = reinterpret_cast<uint64_t*>(smem + SM::kOffBar);
-    uint64_t* full = tma_full + NS;
-    uint64_t* done = full + R;
+    const int NS = a.nstage;
+    const int W = a.wmax;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.bar_off);
+    uint64_t* qready = full + NS;
+    uint64_t* empty = qready + NS;
 
-    const int tid = threadIdx.x;
-    const int d0 = blockIdx.x * CH;
-    const int b = blockIdx.y;
-    const int seg = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int kc = a.kcta;
+    const int rrow = blockIdx.x / kc, ci = blockIdx.x % kc;
+    const int seg = rrow / a.batch;
+    const int b = rrow % a.batch;
+    const int u0 = (int)((long long)ci * a.upr / kc);
+    const int u1 = (int)((long long)(ci + 1) * a.upr / kc);
+    const int nunits = u1 - u0;
     const int N = a.dstate;
     const long long t_begin = (long long)seg * a.seg_len;
     const long long t_end = min(a.L, t_begin + a.seg_len);
     const int nchunks = (int)((t_end - t_begin + TC - 1) / TC);
-    const int nslots = (int)((t_end - t_begin + U - 1) / U);
-    const bool has_z = !AGG && a.has_z;
+    constexpr bool has_z = !AGG && GATE;
 
     if (tid == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(&tma_full[s], 1);
-        for (int r = 0; r < R; ++r) {
-            mbar_init(&full[r], 32);
-            mbar_init(&done[r], NSCAN);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&qready[s], 32);
+            mbar_init(&empty[s], 32 * nunits);
         }
         mbar_fence_init();
         fence_proxy_async_smem();
     }
     __syncthreads();
 
-    if (tid >= NSCAN) {
-        // =============================================================== helper warp (lane = channel)
-        const int lane = tid - NSCAN;
-        const int dch = d0 + lane;
-        const bool cvalid = dch < a.dim;
-        const float bias = (a.bias != nullptr && cvalid) ? a.bias[dch] : 0.f;
-        const float Dd = (!AGG && a.D != nullptr && cvalid) ? a.D[dch] : 0.f;
-        const uint32_t tile_bytes = (uint32_t)SM::kTile;
-        const uint32_t bc_bytes = (uint32_t)(N * SM::kRow);
-        const uint32_t stage_tx = (AGG ? 2u : (has_z ? 3u : 2u)) * tile_bytes + (AGG ? 1u : 2u) * bc_bytes;
-
-        auto issue_loads = [&](int k) {  // chunk k -> stage k % NS (lane 0 only)
-            unsigned char* st = smem + (k % NS) * SM::kStage;
+    if (wid == W) {
+        // ================================================================== producer warp
+        const int mi = nunits == a.wlo ? 0 : 1;
+        const uint32_t tx = (uint32_t)(nunits * kUnitCh * 128 * (has_z ? 3 : 2) + (AGG ? 1 : 2) * N * 128);
+        auto issue = [&](int k) {  // lane 0: TMA loads of chunk k into stage k % NS
+            const int s = k % NS;
+            unsigned char* st = smem + s * a.stage_bytes;
             const int t0 = (int)(t_begin + (long long)k * TC);
-            uint64_t* bar = &tma_full[k % NS];
-            mbar_arrive_expect_tx(bar, stage_tx);
-            tma_load_3d(st, &tm_u, bar, t0, d0, b);
-            tma_load_3d(st + SM::kTile, &tm_d, bar, t0, d0, b);
-            if (has_z) tma_load_3d(st + 2 * SM::kTile, &tm_z, bar, t0, d0, b);
-            tma_load_3d(st + 3 * SM::kTile, &tm_B, bar, t0, 0, b);
-            if (!AGG) tma_load_3d(st + 3 * SM::kTile + SM::kBC, &tm_C, bar, t0, 0, b);
+            mbar_arrive_expect_tx(&full[s], tx);
+            const int r0 = u0 * kUnitCh;
+            tma_load_3d(st, &maps.u[mi], &full[s], t0, r0, b);
+            tma_load_3d(st + W * 1024, &maps.d[mi], &full[s], t0, r0, b);
+            if (has_z) tma_load_3d(st + 2 * W * 1024, &maps.z[mi], &full[s], t0, r0, b);
+            tma_load_3d(st + a.bc_off, &maps.B, &full[s], t0, 0, b);
+            if (!AGG) tma_load_3d(st + a.bc_off + NP * 128, &maps.C, &full[s], t0, 0, b);
         };
-        // plain-load fallback (unaligned shapes): same swizzled layout, one row per lane
-        auto plain_load = [&](int k) {
-            unsigned char* st = smem + (k % NS) * SM::kStage;
-            const long long t0 = t_begin + (long long)k * TC;
-            const int tv = (int)min((long long)TC, t_end - t0);
-            const TIn* src[3] = {static_cast<const TIn*>(a.u), static_cast<const TIn*>(a.delta),
-                                 static_cast<const TIn*>(a.z)};
-            for (int m = 0; m < (has_z ? 3 : 2); ++m) {
-                unsigned char* tile = st + m * SM::kTile;
-                for (int t = 0; t < TC; ++t) {
-                    TIn v = TIn(0);
-                    if (cvalid && t < tv) v = src[m][((long long)b * a.dim + dch) * a.L + t0 + t];
-                    *reinterpret_cast<TIn*>(tile + swz64(lane * SM::kRow + t * (int)sizeof(TIn))) = v;
+        // chunk k's B, C as (B_n, B_n+1, C_n, C_n+1) quads per step
+        auto build_quads = [&](int k) {
+            unsigned char* st = smem + (k % NS) * a.stage_bytes;
+            float4* qd = reinterpret_cast<float4*>(st + a.quad_off);
+            constexpr int NTQ = TC / 4;
+            for (int item = lane; item < NPAIR * NTQ; item += 32) {
+                const int p = item % NPAIR, tq = item / NPAIR;
+                const int n0 = 2 * p, n1 = n0 + 1;
+                float b0[4] = {0.f, 0.f, 0.f, 0.f}, b1[4] = {0.f, 0.f, 0.f, 0.f};
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                if (TMA) {
+                    const unsigned char* tB = st + a.bc_off;
+                    const unsigned char* tC = tB + NP * 128;
+                    if (n0 < N) { tile_load4<TIn>(tB, n0, tq * 4 * ES, b0); if (!AGG) tile_load4<TIn>(tC, n0, tq * 4 * ES, c0); }
+                    if (n1 < N) { tile_load4<TIn>(tB, n1, tq * 4 * ES, b1); if (!AGG) tile_load4<TIn>(tC, n1, tq * 4 * ES, c1); }
+                } else {
+                    const TIn* gB = static_cast<const TIn*>(a.B);
+                    const TIn* gC = static_cast<const TIn*>(a.C);
+                    const long long tb = t_begin + (long long)k * TC + tq * 4;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (tb + i >= t_end) break;
+                        if (n0 < N) {
+                            b0[i] = In<TIn>::to_f32(gB[((long long)b * N + n0) * a.L + tb + i]);
+                            if (!AGG) c0[i] = In<TIn>::to_f32(gC[((long long)b * N + n0) * a.L + tb + i]);
+                        }
+                        if (n1 < N) {
+                            b1[i] = In<TIn>::to_f32(gB[((long long)b * N + n1) * a.L + tb + i]);
+                            if (!AGG) c1[i] = In<TIn>::to_f32(gC[((long long)b * N + n1) * a.L + tb + i]);
+                        }
+                    }
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) qd[(tq * 4 + i) * NPAIR + p] = make_float4(b0[i], b1[i], c0[i], c1[i]);
             }
-            for (int m = 0; m < (AGG ? 1 : 2); ++m) {
-                const TIn* gsrc = static_cast<const TIn*>(m == 0 ? a.B : a.C);
-                TIn* tile = reinterpret_cast<TIn*>(st + 3 * SM::kTile + m * SM::kBC);
-                for (int j = lane; j < N * TC; j += 32) {
-                    const int n = j / TC, t = j % TC;
-                    tile[j] = t < tv ? gsrc[((long long)b * N + n) * a.L + t0 + t] : TIn(0);
-                }
-            }
-            __syncwarp();
         };
-
-        if (TMA && lane == 0)
-            for (int k = 0; k < NS && k < nchunks; ++k) issue_loads(k);
 
         bool ok = true;
-        // post: finish slot i (its partial sums are complete) -> output tile
-        auto post = [&](int i) {
-            const int r = i % R;
-            ok = __all_sync(0xffffffffu, mbar_wait_bounded(&done[r], (uint32_t)((i / R) & 1), kWaitLimitNs));
-            if (!ok) return;
-            const int k = i / SPC, j = i % SPC;
-            unsigned char* slot = smem + SM::kOffSlots + r * SM::kSlot;
-            const unsigned char* yp = slot + SM::kSlotQ + SM::kSlotBC;
-            const float2* zz = reinterpret_cast<const float2*>(slot + SM::kSlotQ + SM::kSlotBC + SM::kSlotY + lane * SM::kZPitch);
-            float y[U];
-#pragma unroll
-            for (int q = 0; q < U; q += 4) {
-                float4 acc = *reinterpret_cast<const float4*>(yp + (lane * S) * SM::kYPitch + q * 4);
-#pragma unroll
-                for (int gg = 1; gg < S; ++gg) {
-                    const float4 v = *reinterpret_cast<const float4*>(yp + (lane * S + gg) * SM::kYPitch + q * 4);
-                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-                }
-                const float4 z01 = *reinterpret_cast<const float4*>(zz + q);
-                const float4 z23 = *reinterpret_cast<const float4*>(zz + q + 2);
-                y[q] = (acc.x + z01.x) * z01.y;
-                y[q + 1] = (acc.y + z01.z) * z01.w;
-                y[q + 2] = (acc.z + z23.x) * z23.y;
-                y[q + 3] = (acc.w + z23.z) * z23.w;
-            }
-            unsigned char* out = smem + SM::kOffOut + (k & 1) * SM::kTile;
-            uint4 c0, c1;
-            In<TIn>::pack8(y, c0, c1);
-            const uint32_t off = lane * SM::kRow + j * U * (int)sizeof(TIn);
-            *reinterpret_cast<uint4*>(out + swz64(off)) = c0;
-            if (VPR == 2) *reinterpret_cast<uint4*>(out + swz64(off + 16)) = c1;
-            if (j == SPC - 1 || i == nslots - 1) {
-                const long long t0 = t_begin + (long long)k * TC;
-                if (TMA) {
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(&tm_y, out, (int)t0, d0, b);
-                        bulk_commit();
-                        bulk_wait_read<1>();  // the other output tile may be overwritten next
-                    }
-                    __syncwarp();
-                } else {
-                    const int tv = (int)min((long long)TC, t_end - t0);
-                    TIn* gy = static_cast<TIn*>(a.y);
-                    if (cvalid)
-                        for (int t = 0; t < tv; ++t)
-                            gy[((long long)b * a.dim + dch) * a.L + t0 + t] =
-                                *reinterpret_cast<const TIn*>(out + swz64(lane * SM::kRow + t * (int)sizeof(TIn)));
-                }
-            }
-        };
-        // produce: slot i's operands from the staged tiles
-        auto produce = [&](int i) {
-            const int r = i % R;
-            const int k = i / SPC, j = i % SPC;
-            if (j == 0) {
-                if (TMA) {
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&tma_full[k % NS], (uint32_t)((k / NS) & 1), kWaitLimitNs));
-                    if (!ok) return;
-                } else {
-                    plain_load(k);
-                }
-            }
-            const unsigned char* st = smem + (k % NS) * SM::kStage;
-            unsigned char* slot = smem + SM::kOffSlots + r * SM::kSlot;
-            const long long t0 = t_begin + (long long)k * TC + j * U;
-            const int tv = (int)min((long long)U, t_end - t0);
-            const uint32_t off = lane * SM::kRow + j * U * (int)sizeof(TIn);
-            float uv[U], dv[U];
-            {
-                const uint4 u0 = *reinterpret_cast<const uint4*>(st + swz64(off));
-                const uint4 u1 = VPR == 2 ? *reinterpret_cast<const uint4*>(st + swz64(off + 16)) : u0;
-                const uint4 e0 = *reinterpret_cast<const uint4*>(st + SM::kTile + swz64(off));
-                const uint4 e1 = VPR == 2 ? *reinterpret_cast<const uint4*>(st + SM::kTile + swz64(off + 16)) : e0;
-                In<TIn>::unpack8(u0, u1, uv);
-                In<TIn>::unpack8(e0, e1, dv);
-            }
-            float4* q = reinterpret_cast<float4*>(slot + lane * SM::kQPitch);
-#pragma unroll
-            for (int t = 0; t < U; t += 2) {
-                float2 dt = make_float2(dv[t] + bias, dv[t + 1] + bias);
-                if (a.softplus) dt = softplus2(dt);
-                if (t >= tv) dt.x = 0.f;
-                if (t + 1 >= tv) dt.y = 0.f;
-                const float2 du = fmul2(dt, make_float2(uv[t], uv[t + 1]));
-                q[t] = make_float4(dt.x, dt.x, du.x, du.x);
-                q[t + 1] = make_float4(dt.y, dt.y, du.y, du.y);
-            }
-            if (!AGG) {
-                float zv[U];
-                if (has_z) {
-                    const uint4 z0 = *reinterpret_cast<const uint4*>(st + 2 * SM::kTile + swz64(off));
-                    const uint4 z1 = VPR == 2 ? *reinterpret_cast<const uint4*>(st + 2 * SM::kTile + swz64(off + 16)) : z0;
-                    In<TIn>::unpack8(z0, z1, zv);
-                }
-                float4* zz = reinterpret_cast<float4*>(slot + SM::kSlotQ + SM::kSlotBC + SM::kSlotY + lane * SM::kZPitch);
-#pragma unroll
-                for (int t = 0; t < U; t += 2) {
-                    const float g0 = has_z ? silu_f(zv[t]) : 1.f;
-                    const float g1 = has_z ? silu_f(zv[t + 1]) : 1.f;
-                    zz[t / 2] = make_float4(Dd * uv[t], g0, Dd * uv[t + 1], g1);
-                }
-            }
-            // B, C of the slot's steps as fp32 quads; states >= N are zero
-            const TIn* tB = reinterpret_cast<const TIn*>(st + 3 * SM::kTile);
-            const TIn* tC = reinterpret_cast<const TIn*>(st + 3 * SM::kTile + SM::kBC);
-            unsigned char* bcq = slot + SM::kSlotQ;
-#pragma unroll
-            for (int e = lane; e < U * (NP / 2); e += 32) {
-                const int t = e % U, p = e / U;
-                const int n0 = 2 * p, n1 = n0 + 1, tt = j * U + t;
-                float4 w;
-                w.x = n0 < N ? In<TIn>::to_f32(tB[n0 * TC + tt]) : 0.f;
-                w.y = n1 < N ? In<TIn>::to_f32(tB[n1 * TC + tt]) : 0.f;
-                w.z = (!AGG && n0 < N) ? In<TIn>::to_f32(tC[n0 * TC + tt]) : 0.f;
-                w.w = (!AGG && n1 < N) ? In<TIn>::to_f32(tC[n1 * TC + tt]) : 0.f;
-                *reinterpret_cast<float4*>(bcq + t * SM::kBCPitch + p * 16) = w;
-            }
-            mbar_arrive(&full[r]);
-            if (j == SPC - 1) {
-                // every lane has read stage k: refill it with chunk k + NS
-                __syncwarp();
-                if (TMA && lane == 0 && k + NS < nchunks) issue_loads(k + NS);
-            }
-        };
-
-        for (int i = 0; i < nslots + R && ok; ++i) {
-            if (i >= R) {
-                if (AGG) {  // slot free once the scan threads are done with it
-                    const int r = (i - R) % R;
-                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&done[r], (uint32_t)(((i - R) / R) & 1), kWaitLimitNs));
-                } else {
-                    post(i - R);
-                }
+        int issued = 0, landed = 0;  // chunks whose loads were issued / observed complete
+        if (TMA) {
+            issued = min(NS, nchunks);
+            if (lane == 0)
+                for (int k = 0; k < issued; ++k) issue(k);
+        }
+        for (int k = 0; k < nchunks && ok; ++k) {
+            const int s = k % NS;
+            if (TMA) {
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[s], (uint32_t)((k / NS) & 1), kWaitLimitNs));
+                if (!ok) break;
+                landed = k + 1;
+            } else if (k >= NS) {
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (uint32_t)((k / NS - 1) & 1), kWaitLimitNs));
                 if (!ok) break;
             }
-            if (i < nslots) produce(i);
+            build_quads(k);
+            mbar_arrive(&qready[s]);
+            // refill the stage of chunk k-1 with chunk k-1+NS once every consumer has left it
+            if (TMA && k >= 1 && k - 1 + NS < nchunks) {
+                const int sp = (k - 1) % NS;
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[sp], (uint32_t)(((k - 1) / NS) & 1), kWaitLimitNs));
+                if (!ok) break;
+                if (lane == 0) issue(k - 1 + NS);
+                ++issued;
+            }
         }
-        if (TMA && !AGG && lane == 0) bulk_wait_all<0>();
-        if (!ok && lane == 0) atomicExch(&g_status, 1);
+        if (!ok) {
+            if (lane == 0) atomicExch(&g_status, 1);
+            // let the copies still in flight land before the CTA can exit
+            for (int k = landed; k < issued; ++k)
+                if (!mbar_wait_bounded(&full[k % NS], (uint32_t)((k / NS) & 1), kWaitLimitNs)) break;
+        }
         return;
     }
+    if (wid >= nunits) return;
 
-    // =================================================================== scan threads
-    const int c = tid / S;
-    const int g = tid % S;
-    const int dch = d0 + c;
+    // ====================================================================== consumer warps
+    const int c = lane & 7;
+    const int g = lane >> 3;
+    const int dch = (u0 + wid) * kUnitCh + c;
     const bool cvalid = dch < a.dim;
+    const long long row = (long long)b * a.dim + (cvalid ? dch : 0);
+    const float bias = (cvalid && a.bias != nullptr) ? a.bias[dch] : 0.f;
+    const float Dd = (!AGG && cvalid && a.D != nullptr) ? a.D[dch] : 0.f;
+
     float2 A2[G / 2];
     float2 h[G / 2];
 #pragma unroll
@@ -411,8 +267,8 @@ __global__ void __launch_bounds__(CH*(NP / G) + 32, 1)
         A2[p].y = (cvalid && n1 < N) ? a.A[(long long)dch * N + n1] * kLog2e : 0.f;
         h[p] = make_float2(0.f, 0.f);
     }
-    if (seg > 0 && cvalid) {
-        // fold the carries of segments 0..seg-1 in order: h <- prodAbar * h + h_end
+    if (!AGG && seg > 0 && cvalid) {
+        // fold the carries of segments 0 .. seg-1 in order: h <- prod Abar * h + h_end
         for (int q = 0; q < seg; ++q) {
             const float2* ag = a.agg + (((long long)q * a.batch + b) * a.dim + dch) * N;
 #pragma unroll
@@ -423,60 +279,171 @@ __global__ void __launch_bounds__(CH*(NP / G) + 32, 1)
             }
         }
     }
+
+    // warp scratch: two buffers of Delta quads (slot parity) and one of partial sums
+    unsigned char* wsq = smem + a.scratch_off + wid * kWarpScratch;
+    unsigned char* wsy = wsq + 2 * kQBuf;
+    const int nslots = (int)((t_end - t_begin + kSlot - 1) / kSlot);
     float sumdt = 0.f;
     bool ok = true;
-    for (int i = 0; i < nslots; ++i) {
-        const int r = i % R;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[r], (uint32_t)((i / R) & 1), kWaitLimitNs));
-        if (!ok) break;
-        unsigned char* slot = smem + SM::kOffSlots + r * SM::kSlot;
-        const float4* qrow = reinterpret_cast<const float4*>(slot + c * SM::kQPitch);
-        const float4* bcg = reinterpret_cast<const float4*>(slot + SM::kSlotQ) + g * (G / 2);
-        constexpr int kBCQ = SM::kBCPitch / 16;
-        float yp[U];
+
+    auto wait_tiles = [&](int k) -> bool {  // u, delta, z tiles of chunk k have landed
+        if (!TMA) return true;
+        return __all_sync(0xffffffffu, mbar_wait_bounded(&full[k % NS], (uint32_t)((k / NS) & 1), kWaitLimitNs));
+    };
+    auto wait_quads = [&](int k) -> bool {  // the producer has written chunk k's B/C quads
+        return __all_sync(0xffffffffu, mbar_wait_bounded(&qready[k % NS], (uint32_t)((k / NS) & 1), kWaitLimitNs));
+    };
+
+    // Phase A of slot i: Delta, Delta*u of the 4 owned steps -> quads in wsq[i & 1]; returns
+    // D*u and the gate of the owned steps for phase C.
+    auto phase_a = [&](int i, float2& skip01, float2& skip23, float2& gate01, float2& gate23) {
+        const int k = i / SPC, sl = i % SPC;
+        const long long to = t_begin + (long long)i * kSlot + g * kOwned;  // first owned step
+        const unsigned char* st = smem + (k % NS) * a.stage_bytes;
+        float dv[4], uv[4], zv[4];
+        if (TMA) {
+            const int byte = (sl * kSlot + g * kOwned) * ES;
+            tile_load4<TIn>(st + (W + wid) * 1024, c, byte, dv);
+            tile_load4<TIn>(st + wid * 1024, c, byte, uv);
+            if (has_z) tile_load4<TIn>(st + (2 * W + wid) * 1024, c, byte, zv);
+        } else {
+            const TIn* gd = static_cast<const TIn*>(a.delta) + row * a.L;
+            const TIn* gu = static_cast<const TIn*>(a.u) + row * a.L;
+            const TIn* gz = static_cast<const TIn*>(a.z) + row * a.L;
 #pragma unroll
-        for (int t = 0; t < U; ++t) {
+            for (int j = 0; j < 4; ++j) {
+                const bool in = cvalid && to + j < t_end;
+                dv[j] = in ? In<TIn>::to_f32(gd[to + j]) : 0.f;
+                uv[j] = in ? In<TIn>::to_f32(gu[to + j]) : 0.f;
+                zv[j] = (in && has_z) ? In<TIn>::to_f32(gz[to + j]) : 0.f;
+            }
+        }
+        float2 dt01 = make_float2(dv[0] + bias, dv[1] + bias);
+        float2 dt23 = make_float2(dv[2] + bias, dv[3] + bias);
+        if (SOFTPLUS) {
+            dt01 = softplus2(dt01);
+            dt23 = softplus2(dt23);
+        }
+        if (to + 4 > t_end) {  // steps past the end (or past this segment) leave h unchanged
+            const long long nv = t_end - to;
+            if (nv < 1) dt01.x = 0.f;
+            if (nv < 2) dt01.y = 0.f;
+            if (nv < 3) dt23.x = 0.f;
+            dt23.y = 0.f;
+        }
+        const float2 du01 = fmul2(dt01, make_float2(uv[0], uv[1]));
+        const float2 du23 = fmul2(dt23, make_float2(uv[2], uv[3]));
+        float4* qw = reinterpret_cast<float4*>(wsq + (i & 1) * kQBuf + c * kQPitch + g * kOwned * 16);
+        qw[0] = make_float4(dt01.x, dt01.x, du01.x, du01.x);
+        qw[1] = make_float4(dt01.y, dt01.y, du01.y, du01.y);
+        qw[2] = make_float4(dt23.x, dt23.x, du23.x, du23.x);
+        qw[3] = make_float4(dt23.y, dt23.y, du23.y, du23.y);
+        if (!AGG) {
+            skip01 = fmul2(make_float2(Dd, Dd), make_float2(uv[0], uv[1]));
+            skip23 = fmul2(make_float2(Dd, Dd), make_float2(uv[2], uv[3]));
+            if (has_z) {
+                gate01 = silu2(make_float2(zv[0], zv[1]));
+                gate23 = silu2(make_float2(zv[2], zv[3]));
+            } else {
+                gate01 = gate23 = make_float2(1.f, 1.f);
+            }
+        }
+    };
+
+    // Phase B of slot i: advance the lane's G states through the slot's 16 steps; yp[t] is the
+    // lane's share of C.h at step t.
+    auto phase_b = [&](int i, float* yp) {
+        const int k = i / SPC, sl = i % SPC;
+        const float4* qrow = reinterpret_cast<const float4*>(wsq + (i & 1) * kQBuf + c * kQPitch);
+        const float4* bc = reinterpret_cast<const float4*>(smem + (k % NS) * a.stage_bytes + a.quad_off) +
+                           sl * kSlot * NPAIR + g * (G / 2);
+#pragma unroll
+        for (int t = 0; t < kSlot; ++t) {
             const float4 q = qrow[t];  // (Delta, Delta, Delta*u, Delta*u)
-            float2 y0 = make_float2(0.f, 0.f), y1 = make_float2(0.f, 0.f);
+            if (AGG) sumdt += q.x;
+            float2 ya;
 #pragma unroll
             for (int p = 0; p < G / 2; ++p) {
-                const float4 w = bcg[t * kBCQ + p];
+                const float4 w = bc[t * NPAIR + p];  // (B_n, B_n+1, C_n, C_n+1)
                 const float2 x = fmul2(make_float2(q.x, q.y), A2[p]);
                 const float2 abar = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                 const float2 bx = fmul2(make_float2(q.z, q.w), make_float2(w.x, w.y));
                 h[p] = ffma2(abar, h[p], bx);
-                if (!AGG) {
-                    if (p & 1) y1 = ffma2(make_float2(w.z, w.w), h[p], y1);
-                    else       y0 = ffma2(make_float2(w.z, w.w), h[p], y0);
-                }
+                if (!AGG) ya = p == 0 ? fmul2(make_float2(w.z, w.w), h[p]) : ffma2(make_float2(w.z, w.w), h[p], ya);
             }
-            if (AGG) sumdt += q.x;
-            const float2 ys = fadd2(y0, y1);
-            yp[t] = ys.x + ys.y;
+            if (!AGG) yp[t] = ya.x + ya.y;
         }
+    };
+
+    // Phase C of slot i: sum the 4 lanes' partials of the owned steps, skip term, gate, store.
+    auto phase_c = [&](int i, float2 skip01, float2 skip23, float2 gate01, float2 gate23) {
+        const long long to = t_begin + (long long)i * kSlot + g * kOwned;
+        float4 acc = *reinterpret_cast<const float4*>(wsy + c * kYPitch + g * 16);
+#pragma unroll
+        for (int gg = 1; gg < kLanesPerCh; ++gg) {
+            const float4 v = *reinterpret_cast<const float4*>(wsy + (gg * kUnitCh + c) * kYPitch + g * 16);
+            const float2 lo = fadd2(make_float2(acc.x, acc.y), make_float2(v.x, v.y));
+            const float2 hi = fadd2(make_float2(acc.z, acc.w), make_float2(v.z, v.w));
+            acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+        const float2 y01 = fmul2(fadd2(make_float2(acc.x, acc.y), skip01), gate01);
+        const float2 y23 = fmul2(fadd2(make_float2(acc.z, acc.w), skip23), gate23);
+        const float yv[4] = {y01.x, y01.y, y23.x, y23.y};
+        TIn* gy = static_cast<TIn*>(a.y) + row * a.L + to;
+        if (TMA && to + 4 <= t_end) {
+            if (cvalid) store4<TIn>(gy, yv);
+        } else if (cvalid) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (to + j < t_end) store_out<TIn>(gy + j, yv[j]);
+        }
+    };
+
+    // Software pipeline over slots: phase A of slot i+1 and phase B of slot i share one region
+    // without warp barriers (so their instructions interleave), as does phase C of slot i with
+    // the next region.
+    float2 sk01 = make_float2(0.f, 0.f), sk23 = sk01, gt01 = sk01, gt23 = sk01;
+    ok = wait_tiles(0);
+    if (ok) phase_a(0, sk01, sk23, gt01, gt23);
+    __syncwarp();
+#pragma unroll 1
+    for (int i = 0; i < nslots && ok; ++i) {
+        const int k = i / SPC, sl = i % SPC;
+        const bool next = i + 1 < nslots;
+        if (sl == 0) ok = wait_quads(k);
+        if (ok && next && sl == SPC - 1) ok = wait_tiles(k + 1);
+        if (!ok) break;
+        float2 nk01 = make_float2(0.f, 0.f), nk23 = nk01, nt01 = nk01, nt23 = nk01;
+        if (next) phase_a(i + 1, nk01, nk23, nt01, nt23);
+        float yp[kSlot];
+        phase_b(i, yp);
+        __syncwarp();
+        if (sl == SPC - 1 || !next) mbar_arrive(&empty[k % NS]);  // this lane is done with chunk k's stage
         if (!AGG) {
-            float4* yd = reinterpret_cast<float4*>(slot + SM::kSlotQ + SM::kSlotBC + tid * SM::kYPitch);
-            yd[0] = make_float4(yp[0], yp[1], yp[2], yp[3]);
-            yd[1] = make_float4(yp[4], yp[5], yp[6], yp[7]);
+            float4* yw = reinterpret_cast<float4*>(wsy + (g * kUnitCh + c) * kYPitch);
+#pragma unroll
+            for (int j = 0; j < kSlot / 4; ++j) yw[j] = make_float4(yp[4 * j], yp[4 * j + 1], yp[4 * j + 2], yp[4 * j + 3]);
         }
-        mbar_arrive(&done[r]);
+        __syncwarp();
+        if (!AGG) phase_c(i, sk01, sk23, gt01, gt23);
+        sk01 = nk01; sk23 = nk23; gt01 = nt01; gt23 = nt23;
     }
     if (!ok) {
-        if (tid == 0) atomicExch(&g_status, 1);
+        if (lane == 0) atomicExch(&g_status, 1);
         return;
     }
+    if (!cvalid) return;
     if (AGG) {
-        if (cvalid) {
-            float2* ag = a.agg + (((long long)seg * a.batch + b) * a.dim + dch) * N;
+        float2* ag = a.agg + (((long long)seg * a.batch + b) * a.dim + dch) * N;
 #pragma unroll
-            for (int p = 0; p < G / 2; ++p) {
-                const int n0 = g * G + 2 * p, n1 = n0 + 1;
-                if (n0 < N) ag[n0] = make_float2(ex2_approx(A2[p].x * sumdt), h[p].x);
-                if (n1 < N) ag[n1] = make_float2(ex2_approx(A2[p].y * sumdt), h[p].y);
-            }
+        for (int p = 0; p < G / 2; ++p) {
+            const int n0 = g * G + 2 * p, n1 = n0 + 1;
+            if (n0 < N) ag[n0] = make_float2(ex2_approx(A2[p].x * sumdt), h[p].x);
+            if (n1 < N) ag[n1] = make_float2(ex2_approx(A2[p].y * sumdt), h[p].y);
         }
-    } else if (a.last_state != nullptr && cvalid && seg == a.nseg - 1) {
-        float* ls = a.last_state + ((long long)b * a.dim + dch) * N;
+    } else if (a.last_state != nullptr && seg == a.nseg - 1) {
+        float* ls = a.last_state + row * N;
 #pragma unroll
         for (int p = 0; p < G / 2; ++p) {
             const int n0 = g * G + 2 * p, n1 = n0 + 1;

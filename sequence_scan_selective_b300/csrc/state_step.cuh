@@ -10,7 +10,7 @@
 #include <stdint.h>
 
 #include "ptx.cuh"
-#include "scan_fwd.cuh"
+#include "common.cuh"
 
 namespace mscan {
 

@@ -77,11 +77,12 @@ def test_state_sizes(ms, N):
     _check_full(ms, cfg)
 
 
-@pytest.mark.parametrize("variant", ["0", "1"])
+@pytest.mark.parametrize("wmax,stages", [("1", "2"), ("3", "3"), ("15", "4"), ("0", "2")])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_tiling_variants(ms, variant, dtype):
-    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=70, seqlen=333, dtype=dtype, seed=21)
-    _check_full(ms, cfg, env={"MAMBA_SCAN_VARIANT": variant})
+def test_tiling_variants(ms, wmax, stages, dtype):
+    """Consumer warps per CTA (work units per CTA) and ring depth change only the schedule."""
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=130, seqlen=333, dtype=dtype, seed=21)
+    _check_full(ms, cfg, env={"MAMBA_SCAN_WMAX": wmax, "MAMBA_SCAN_STAGES": stages})
 
 
 @pytest.mark.parametrize("drop", [("z",), ("D",), ("delta_bias",), ("z", "D", "delta_bias")])

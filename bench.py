@@ -109,30 +109,57 @@ def ncu_traffic(workload: str):
 
 
 # ------------------------------------------------------------------------------------ clocks
+class _Nvml:
+    """The few NVML calls the sampler needs, through ctypes on the driver's libnvidia-ml."""
+
+    def __init__(self, bus_id: str):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByPciBusId_v2 failed")
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sm_clock(self, maximum=False) -> int:
+        v = self.ct.c_uint()
+        fn = self.lib.nvmlDeviceGetMaxClockInfo if maximum else self.lib.nvmlDeviceGetClockInfo
+        if fn(self.h, 1, self.ct.byref(v)) != 0:  # NVML_CLOCK_SM
+            raise RuntimeError("nvml clock query failed")
+        return int(v.value)
+
+    def reasons(self) -> int:
+        v = self.ct.c_ulonglong()
+        if self.reason_fn(self.h, self.ct.byref(v)) != 0:
+            raise RuntimeError("nvml clock-event query failed")
+        return int(v.value)
+
+
 class ClockSampler:
-    """Samples the SM clock and clock-event reasons of this process's GPU (through NVML, located by
-    PCI bus id) while the timed region runs."""
+    """Samples the SM clock and clock-event reasons of this process's GPU (NVML through ctypes,
+    located by PCI bus id; nvidia-smi as a fallback) while the timed region runs."""
 
     REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
                "hw_power_brake": 0x80, "sw_power_cap": 0x4}
 
-    def __init__(self, cuda_index: int, period_s: float = 0.002):
+    def __init__(self, cuda_index: int, period_s: float = 0.02):
         self.cuda_index, self.period = cuda_index, period_s
         self.samples, self.reasons = [], set()
         self.max_mhz, self.error = None, None
         self.t0 = self.t1 = time.time()
+        self._active = False
         self._stop = threading.Event()
         self._t = None
 
     def __enter__(self):
         try:
-            import pynvml as nv
-            import torch
-            nv.nvmlInit()
-            self._nv, self._h = nv, nv.nvmlDeviceGetHandleByPciBusId(self._bus_id())
-            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self._h, nv.NVML_CLOCK_SM)
+            self._nv = _Nvml(self._bus_id())
+            self.max_mhz = self._nv.sm_clock(maximum=True)
         except Exception as e:  # noqa: BLE001
-            return self._start_smi(f"nvml unavailable ({e.__class__.__name__})")
+            return self._start_smi(f"nvml unavailable ({e.__class__.__name__}: {e})")
         self._t = threading.Thread(target=self._run, daemon=True)
         self._t.start()
         return self
@@ -143,14 +170,14 @@ class ClockSampler:
         return f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
 
     def _start_smi(self, why: str):
-        """Fallback: nvidia-smi sampling every 20 ms in a child process."""
+        """Fallback: nvidia-smi sampling every 100 ms in a child process."""
         self.error = why + "; sampled with nvidia-smi"
         q = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.hw_power_brake_slowdown,"
              "clocks_event_reasons.sw_power_cap")
         try:
             self._smi = subprocess.Popen(["nvidia-smi", "-i", self._bus_id(), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             time.sleep(0.3)
         except Exception as e:  # noqa: BLE001
@@ -159,21 +186,23 @@ class ClockSampler:
         return self
 
     def _run(self):
-        nv = self._nv
         while not self._stop.is_set():
             try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
-                self.reasons.update(k for k, bit in self.REASONS.items() if r & bit)
+                mhz, r = self._nv.sm_clock(), self._nv.reasons()
+                if self._active:  # inside the timed region
+                    self.samples.append(mhz)
+                    self.reasons.update(k for k, bit in self.REASONS.items() if r & bit)
             except Exception as e:  # noqa: BLE001
                 self.error = f"nvml sample: {e!r}"
             time.sleep(self.period)
 
     def mark(self, begin: bool):
-        """Wall-clock bounds of the timed region (nvidia-smi samples outside them are dropped)."""
+        """Wall-clock bounds of the timed region (samples outside them are dropped)."""
         if begin:
             self.t0 = time.time()
+            self._active = True
         else:
+            self._active = False
             self.t1 = time.time()
 
     def __exit__(self, *exc):
@@ -253,17 +282,19 @@ def run_ours(args, cfg, rank, world, local_rank):
     state = torch.empty((cfg.batch, cfg.dim, cfg.dstate), device=dev, dtype=torch.float32)
     ydec = torch.empty((cfg.batch, cfg.dim), device=dev, dtype=sets[0]["u"].dtype)
     stream = torch.cuda.current_stream()
+    # the public API's prepared form: arguments are checked once, each launch is one C call
+    scans = [ms.prepare_scan_fwd(s["u"], s["delta"], params["A"], s["B"], s["C"], params["D"], s["z"],
+                                 params["delta_bias"], True, y=y, last_state=state)[0] for s in sets]
+    decode = ms.prepare_state_step(state, dsets["x"], dsets["delta"], params["A"], dsets["B"], dsets["C"],
+                                   params["D"], dsets["z"], params["delta_bias"], True, y=ydec)[0]
 
     def step(i, ev=None):
-        s = sets[i % 2]
         if ev is not None:
             ev[0].record(stream)
-        ms.mamba_scan_fwd(s["u"], s["delta"], params["A"], s["B"], s["C"], params["D"], s["z"],
-                          params["delta_bias"], True, y=y, last_state=state)
+        scans[i % 2]()
         if ev is not None:
             ev[1].record(stream)
-        ms.mamba_state_step(state, dsets["x"], dsets["delta"], params["A"], dsets["B"], dsets["C"], params["D"],
-                            dsets["z"], params["delta_bias"], True, y=ydec)
+        decode()
 
     W = max(args.warmup, 3)
     for i in range(W):

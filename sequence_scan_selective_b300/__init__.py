@@ -96,10 +96,30 @@ def _ptr(t: Optional[torch.Tensor], shape, dtype, name: str):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream) -> ctypes.c_void_p:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device=None) -> ctypes.c_void_p:
     if stream is None:
+        if _raw_stream is not None:
+            idx = device.index if device is not None and device.index is not None else torch.cuda.current_device()
+            return ctypes.c_void_p(_raw_stream(idx))
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+class PreparedCall:
+    """A validated call into the library: the argument tuple is built once, so each launch costs
+    only the C call (tensor checks, shape struct and stream lookup are not repeated).  The tensors
+    passed at preparation must stay alive and in place while the object is used."""
+
+    def __init__(self, fn, args, keep):
+        self._fn, self._args, self._keep = fn, args, keep
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != MAMBA_OK:
+            _check(rc)
 
 
 def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
@@ -107,6 +127,11 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     """Selective scan.  u, delta, z [b, d, L]; B, C [b, N, L] (float32 or bfloat16, all the same);
     A [d, N], D [d], delta_bias [d] float32.  Returns (y [b, d, L] in the input dtype,
     last_state [b, d, N] float32 or None)."""
+    return _scan(_lib.mamba_scan_fwd, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
+                 want_state, stream)
+
+
+def _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream):
     bsz, dim, L = u.shape
     N = A.shape[1]
     dt = u.dtype
@@ -116,41 +141,71 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
     if last_state is None and want_state:
         last_state = torch.empty((bsz, dim, N), device=u.device, dtype=torch.float32)
     shape = Shape(bsz, dim, N, L, code)
-    rc = _lib.mamba_scan_fwd(
+    args = (
         ctypes.byref(shape), _ptr(u, (bsz, dim, L), dt, "u"), _ptr(delta, (bsz, dim, L), dt, "delta"),
         _ptr(A, (dim, N), torch.float32, "A"), _ptr(B, (bsz, N, L), dt, "B"),
         _ptr(C, (bsz, N, L), dt, "C"), _ptr(D, (dim,), torch.float32, "D"),
         _ptr(z, (bsz, dim, L), dt, "z"), _ptr(delta_bias, (dim,), torch.float32, "delta_bias"),
         int(bool(softplus)), _ptr(y, (bsz, dim, L), dt, "y"),
-        _ptr(last_state, (bsz, dim, N), torch.float32, "last_state"), _stream(stream))
-    _check(rc)
+        _ptr(last_state, (bsz, dim, N), torch.float32, "last_state"), _stream(stream, u.device))
+    return args, shape, y, last_state
+
+
+def _scan(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream):
+    args, _shape, y, last_state = _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
+                                             want_state, stream)
+    _check(fn(*args))
     return y, last_state
 
 
-def mamba_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
-                     stream=None):
-    """One decode step.  state [b, d, N] float32 (updated in place); x, delta, z [b, d];
-    B, C [b, N]; returns y [b, d] in the input dtype."""
+def prepare_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
+                     last_state=None, want_state=True, stream=None):
+    """mamba_scan_fwd with its arguments checked once.  Returns (call, y, last_state); call()
+    enqueues the scan on the stream current at preparation."""
+    fn = _lib.mamba_scan_fwd
+    args, shape, y, last_state = _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
+                                            want_state, stream)
+    keep = (shape, u, delta, A, B, C, D, z, delta_bias, y, last_state)
+    return PreparedCall(fn, args, keep), y, last_state
+
+
+def _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream):
     bsz, dim, N = state.shape
     dt = x.dtype
     code = _dtype_code(x)
     if y is None:
         y = torch.empty_like(x)
     shape = Shape(bsz, dim, N, 1, code)
-    rc = _lib.mamba_state_step(
+    args = (
         ctypes.byref(shape), _ptr(state, (bsz, dim, N), torch.float32, "state"),
         _ptr(x, (bsz, dim), dt, "x"), _ptr(delta, (bsz, dim), dt, "delta"),
         _ptr(A, (dim, N), torch.float32, "A"), _ptr(B, (bsz, N), dt, "B"), _ptr(C, (bsz, N), dt, "C"),
         _ptr(D, (dim,), torch.float32, "D"), _ptr(z, (bsz, dim), dt, "z"),
         _ptr(delta_bias, (dim,), torch.float32, "delta_bias"), int(bool(softplus)),
-        _ptr(y, (bsz, dim), dt, "y"), _stream(stream))
-    _check(rc)
+        _ptr(y, (bsz, dim), dt, "y"), _stream(stream, state.device))
+    return args, shape, y
+
+
+def mamba_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
+                     stream=None):
+    """One decode step.  state [b, d, N] float32 (updated in place); x, delta, z [b, d];
+    B, C [b, N]; returns y [b, d] in the input dtype."""
+    args, _shape, y = _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream)
+    _check(_lib.mamba_state_step(*args))
     return y
+
+
+def prepare_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
+                       stream=None):
+    """mamba_state_step with its arguments checked once.  Returns (call, y)."""
+    args, shape, y = _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream)
+    keep = (shape, state, x, delta, A, B, C, D, z, delta_bias, y)
+    return PreparedCall(_lib.mamba_state_step, args, keep), y
 
 
 def device_status(stream=None) -> None:
     """Synchronise and raise if a kernel abandoned a bounded wait since the last check."""
-    _check(_lib.mamba_scan_device_status(_stream(stream)))
+    _check(_lib.mamba_scan_device_status(_stream(stream, torch.device("cuda", torch.cuda.current_device()))))
 
 
 def version() -> int:

@@ -114,35 +114,40 @@ static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
         p.nseg = (int)((L + seg - 1) / seg);
     }
     const long long rows = (long long)s->batch * p.nseg;
+    // shared memory: NS stages of [u | delta | z tiles (1 KB per unit each) | B, C tiles | quads],
+    // then per-warp scratch, then 3 NS mbarriers.  Consumer warps per CTA are capped so that two
+    // stages fit.
+    const int bc_bytes = 2 * NP * 128, quad_bytes = TC * (NP / 2) * 16;
+    auto stage_of = [&](int w) { return (3 * w * 1024 + bc_bytes + quad_bytes + 1023) / 1024 * 1024; };
+    auto smem_of = [&](int w, int ns) { return ns * stage_of(w) + w * kWarpScratch + 3 * ns * 8 + 1024; };
+    int wcap = kMaxConsumerWarps;
+    while (wcap > 1 && smem_of(wcap, 2) > kSmemLimit) --wcap;
     const int wforce = env_int("MAMBA_SCAN_WMAX", 0);
+    if (wforce > wcap) return fail(MAMBA_ERR_ARG, "MAMBA_SCAN_WMAX above %d", wcap);
     long long k;
     if (wforce > 0) {
         k = (p.upr + wforce - 1) / wforce;
     } else {
         k = rows >= nsm ? 1 : nsm / rows;
         if (k > p.upr) k = p.upr;
-        if ((p.upr + k - 1) / k > kMaxConsumerWarps) k = (p.upr + kMaxConsumerWarps - 1) / kMaxConsumerWarps;
+        if ((p.upr + k - 1) / k > wcap) k = (p.upr + wcap - 1) / wcap;
     }
     if (k < 1) k = 1;
     p.kcta = (int)k;
     p.wmax = (int)((p.upr + k - 1) / k);
-    if (p.wmax > kMaxConsumerWarps) return fail(MAMBA_ERR_ARG, "MAMBA_SCAN_WMAX above %d", kMaxConsumerWarps);
     p.wlo = p.upr / p.kcta;
     if (rows * k > 0x7fffffffLL) return fail(MAMBA_ERR_ARG, "grid too large");
 
-    // shared memory: NS stages of [u | delta | z tiles (1 KB per unit each) | B, C tiles | quads],
-    // then per-warp scratch, then 3 NS mbarriers
     p.bc_off = 3 * p.wmax * 1024;
-    p.quad_off = p.bc_off + 2 * NP * 128;
-    p.stage_bytes = (p.quad_off + TC * (NP / 2) * 16 + 1023) / 1024 * 1024;
-    const int fixed = p.wmax * kWarpScratch + 1024 /* alignment slack */;
+    p.quad_off = p.bc_off + bc_bytes;
+    p.stage_bytes = stage_of(p.wmax);
     int ns = env_int("MAMBA_SCAN_STAGES", 4);
-    while (ns > 2 && fixed + ns * (p.stage_bytes + 24) > kSmemLimit) --ns;
     if (ns < 2) ns = 2;
+    while (ns > 2 && smem_of(p.wmax, ns) > kSmemLimit) --ns;
     p.nstage = ns;
     p.scratch_off = ns * p.stage_bytes;
     p.bar_off = p.scratch_off + p.wmax * kWarpScratch;
-    p.smem_bytes = p.bar_off + 3 * ns * 8 + 1024;
+    p.smem_bytes = smem_of(p.wmax, ns);
     if (p.smem_bytes > kSmemLimit) return fail(MAMBA_ERR_ARG, "tiling needs %d bytes of shared memory", p.smem_bytes);
     return MAMBA_OK;
 }
@@ -198,7 +203,10 @@ static int launch_fwd(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int 
 }
 
 template <typename TIn, int NP>
-static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gate, cudaStream_t st) {
+// `scratch`/`scratch_cap`: when scratch is non-NULL the segment carries live there (no allocation);
+// otherwise they come from cudaMallocAsync on `st`.
+static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gate, float2* scratch,
+                   size_t scratch_cap, cudaStream_t st) {
     constexpr int TC = Chunk<TIn>::TC;
     const int esize = (int)sizeof(TIn);
     const long long L = s->seqlen;
@@ -245,10 +253,19 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
     a.bar_off = p.bar_off;
     a.agg = nullptr;
 
+    bool owned = false;
     if (p.nseg > 1) {
         const size_t bytes = (size_t)(p.nseg - 1) * s->batch * s->dim * s->dstate * sizeof(float2);
-        cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&a.agg), bytes, st);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (segment carries)");
+        if (scratch != nullptr) {
+            if (bytes > scratch_cap)
+                return fail(MAMBA_ERR_ARG, "this shape splits the sequence into %d segments whose carries need %zu bytes "
+                            "of scratch; the fixed scratch holds %zu bytes", p.nseg, bytes, scratch_cap);
+            a.agg = scratch;
+        } else {
+            cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&a.agg), bytes, st);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (segment carries)");
+            owned = true;
+        }
         const unsigned g1 = (unsigned)((long long)s->batch * (p.nseg - 1) * p.kcta);
         rc = launch_fwd<TIn, NP, true>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
     }
@@ -256,7 +273,7 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
         const unsigned g2 = (unsigned)((long long)s->batch * p.nseg * p.kcta);
         rc = launch_fwd<TIn, NP, false>(a, maps, g2, p.smem_bytes, tma_ok, softplus, gate, st);
     }
-    if (a.agg) {
+    if (owned) {
         cudaError_t e = cudaFreeAsync(a.agg, st);
         if (e != cudaSuccess && rc == MAMBA_OK) rc = cuda_fail(e, "cudaFreeAsync (segment carries)");
     }
@@ -264,8 +281,9 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
 }
 
 template <typename TIn, int NP>
-static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, bool gate, cudaStream_t st) {
-    return fwd_run<TIn, NP>(s, a, softplus, gate, st);
+static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, bool gate, float2* scratch,
+                        size_t scratch_cap, cudaStream_t st) {
+    return fwd_run<TIn, NP>(s, a, softplus, gate, scratch, scratch_cap, st);
 }
 
 // ---------------------------------------------------------------------------- checks
@@ -308,10 +326,9 @@ static int step_dispatch(const StepArgs& a, cudaStream_t st) {
 
 using namespace mscan;
 
-extern "C" int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const void* delta, const float* A,
-                              const void* B, const void* C, const float* D, const void* z,
-                              const float* delta_bias, int softplus_flag, void* y, float* last_state,
-                              void* stream) {
+static int scan_fwd_impl(const mamba_scan_shape* s, const void* u, const void* delta, const float* A, const void* B,
+                         const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                         void* y, float* last_state, float2* scratch, size_t scratch_cap, void* stream) {
     t_err.clear();
     int rc = check_shape(s, true);
     if (rc) return rc;
@@ -341,10 +358,17 @@ extern "C" int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const vo
     const bool sp = softplus_flag != 0, gate = z != nullptr;
     const bool bf = s->in_dtype == MAMBA_BF16;
     if (s->dstate <= 16)
-        return bf ? fwd_dispatch<uint16_t, 16>(s, a, sp, gate, st) : fwd_dispatch<float, 16>(s, a, sp, gate, st);
+        return bf ? fwd_dispatch<uint16_t, 16>(s, a, sp, gate, scratch, scratch_cap, st) : fwd_dispatch<float, 16>(s, a, sp, gate, scratch, scratch_cap, st);
     if (s->dstate <= 32)
-        return bf ? fwd_dispatch<uint16_t, 32>(s, a, sp, gate, st) : fwd_dispatch<float, 32>(s, a, sp, gate, st);
-    return bf ? fwd_dispatch<uint16_t, 64>(s, a, sp, gate, st) : fwd_dispatch<float, 64>(s, a, sp, gate, st);
+        return bf ? fwd_dispatch<uint16_t, 32>(s, a, sp, gate, scratch, scratch_cap, st) : fwd_dispatch<float, 32>(s, a, sp, gate, scratch, scratch_cap, st);
+    return bf ? fwd_dispatch<uint16_t, 64>(s, a, sp, gate, scratch, scratch_cap, st) : fwd_dispatch<float, 64>(s, a, sp, gate, scratch, scratch_cap, st);
+}
+
+extern "C" int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const void* delta, const float* A,
+                              const void* B, const void* C, const float* D, const void* z,
+                              const float* delta_bias, int softplus_flag, void* y, float* last_state,
+                              void* stream) {
+    return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, nullptr, 0, stream);
 }
 
 extern "C" int mamba_state_step(const mamba_scan_shape* s, float* state, const void* x, const void* delta,

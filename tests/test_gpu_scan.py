@@ -208,3 +208,9 @@ def test_mamba130m_layer_full_size(ms):
 
 def test_mamba14b_layer_full_size(ms):
     _check_sampled(ms, synth.CONFIGS["b14"], 192)
+
+
+def test_wide_state_many_channels(ms):
+    """N = 64 with many channels: the plan caps warps per CTA so the tiles fit in shared memory."""
+    cfg = synth.CONFIGS["m130"].replace(batch=1, dim=2048, dstate=64, seqlen=256, seed=15)
+    _check_full(ms, cfg)

@@ -91,6 +91,33 @@ int mamba_state_step(const mamba_scan_shape* s, float* state, const void* x, con
                      const float* A, const void* B, const void* C, const float* D, const void* z,
                      const float* delta_bias, int softplus_flag, void* y, void* stream);
 
+/*
+ * Allocation-free variant of mamba_scan_fwd.  The pages describe nothing like it: it exists for
+ * callers that must not have the library allocate device memory, for example a process that hands
+ * all device memory to its own pool allocator up front, or one that runs under a fixed, audited
+ * memory budget and forbids third-party code from calling the CUDA allocator.
+ *
+ * Arguments, layouts, results and errors are those of mamba_scan_fwd.  The only difference: when
+ * the shape makes the library split the time axis into segments (few channels, long sequences),
+ * the per-segment carries go to a fixed scratch array of MAMBA_NOALLOC_SCRATCH_BYTES that the
+ * library holds in device memory on every GPU where it is loaded, until the process exits.  No
+ * cudaMalloc, cudaMallocAsync, cudaFree or other allocating call is made.
+ *  - A shape whose carries need more than MAMBA_NOALLOC_SCRATCH_BYTES
+ *    ((segments - 1) * batch * dim * dstate * 8 bytes) is rejected with MAMBA_ERR_ARG and a message
+ *    stating both sizes; nothing is launched.
+ *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *    with that device current, then caches it; make that first call before any stream capture.
+ *  - All calls on a device share the one array and it keeps the last call's contents.  Every
+ *    carry a call reads is written earlier in the same call, so nothing needs clearing.  Calls
+ *    that can run at the same time on the GPU (for example on two streams with no ordering between
+ *    them) race on it: order them on one stream or with events.
+ */
+#define MAMBA_NOALLOC_SCRATCH_BYTES (4u << 20)
+int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, const void* delta, const float* A,
+                           const void* B, const void* C, const float* D, const void* z,
+                           const float* delta_bias, int softplus_flag, void* y, float* last_state,
+                           void* stream);
+
 /* Message describing the calling thread's most recent failure ("" if none). */
 const char* mamba_scan_last_error(void);
 

@@ -7,6 +7,7 @@ library is missing, importing this package raises ImportError.
 
 Entry points (names as in include/mamba_scan.h):
   mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, y=None, last_state=None)
+  mamba_scan_fwd_noalloc(...)   same arguments; the library allocates no device memory
   mamba_state_step(state, x, delta, A, B, C, D, z, delta_bias, softplus, y=None)
 """
 from __future__ import annotations
@@ -43,8 +44,9 @@ def _load() -> ctypes.CDLL:
                           "`python sequence_scan_selective_b300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     P, I = ctypes.c_void_p, ctypes.c_int
-    lib.mamba_scan_fwd.restype = I
-    lib.mamba_scan_fwd.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, I, P, P, P]
+    for name in ("mamba_scan_fwd", "mamba_scan_fwd_noalloc"):
+        getattr(lib, name).restype = I
+        getattr(lib, name).argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, I, P, P, P]
     lib.mamba_state_step.restype = I
     lib.mamba_state_step.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, I, P, P]
     lib.mamba_scan_last_error.restype = ctypes.c_char_p
@@ -61,7 +63,7 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 
 # symbols the header declares; the tests check that every one of them is exported
-EXPORTED = ("mamba_scan_fwd", "mamba_state_step", "mamba_scan_last_error", "mamba_scan_version",
+EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_state_step", "mamba_scan_last_error", "mamba_scan_version",
             "mamba_scan_device_status", "mamba_scan_launch_count")
 
 
@@ -131,6 +133,15 @@ def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=
                  want_state, stream)
 
 
+def mamba_scan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
+                           last_state=None, want_state=True, stream=None):
+    """The same scan through the allocation-free entry point: the library itself allocates no
+    device memory (split-sequence carries use its fixed scratch array).  Pass y and last_state to
+    keep this wrapper from allocating them with torch."""
+    return _scan(_lib.mamba_scan_fwd_noalloc, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
+                 want_state, stream)
+
+
 def _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream):
     bsz, dim, L = u.shape
     N = A.shape[1]
@@ -159,10 +170,10 @@ def _scan(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want
 
 
 def prepare_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
-                     last_state=None, want_state=True, stream=None):
-    """mamba_scan_fwd with its arguments checked once.  Returns (call, y, last_state); call()
-    enqueues the scan on the stream current at preparation."""
-    fn = _lib.mamba_scan_fwd
+                     last_state=None, want_state=True, stream=None, noalloc=False):
+    """mamba_scan_fwd (or mamba_scan_fwd_noalloc) with its arguments checked once.  Returns
+    (call, y, last_state); call() enqueues the scan on the stream current at preparation."""
+    fn = _lib.mamba_scan_fwd_noalloc if noalloc else _lib.mamba_scan_fwd
     args, shape, y, last_state = _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
                                             want_state, stream)
     keep = (shape, u, delta, A, B, C, D, z, delta_bias, y, last_state)

@@ -371,6 +371,46 @@ extern "C" int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const vo
     return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, nullptr, 0, stream);
 }
 
+// ---------------------------------------------------------------------------- allocation-free variant
+// Scratch of mamba_scan_fwd_noalloc: the segment carries of a split time axis.  A file-scope
+// device array, so it exists on every device that loads this library, from module load to exit.
+static __device__ __align__(256) float2 g_noalloc_scratch[MAMBA_NOALLOC_SCRATCH_BYTES / sizeof(float2)];
+
+// Device address of g_noalloc_scratch on the current device.  In host code the symbol is only a
+// host-side stand-in, so its device address is looked up once per device (with that device
+// current) and cached.
+static int noalloc_scratch(float2** out) {
+    static std::mutex mu;
+    static float2* addr[256] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 256) return fail(MAMBA_ERR_ARG, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+        addr[dev] = static_cast<float2*>(p);
+    }
+    *out = addr[dev];
+    return MAMBA_OK;
+}
+
+extern "C" int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, const void* delta, const float* A,
+                                      const void* B, const void* C, const float* D, const void* z,
+                                      const float* delta_bias, int softplus_flag, void* y, float* last_state,
+                                      void* stream) {
+    t_err.clear();
+    int rc = check_shape(s, true);
+    if (rc) return rc;
+    float2* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, scratch,
+                         (size_t)MAMBA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 extern "C" int mamba_state_step(const mamba_scan_shape* s, float* state, const void* x, const void* delta,
                                 const float* A, const void* B, const void* C, const float* D, const void* z,
                                 const float* delta_bias, int softplus_flag, void* y, void* stream) {

@@ -435,24 +435,32 @@ def _sample_rows(cfg, budget_rows):
     return np.unique(np.linspace(0, n - 1, k).astype(np.int64))
 
 
-def cpu_baseline(cfg, inp, dec, target_s=15.0):
-    """The fp64 oracle as it stands, on the host cores, over a bounded sample of the workload's
-    channels (full sequence length each)."""
-    nthreads = os.cpu_count() or 1
-    probe = _sample_rows(cfg, max(nthreads, 16))
+def _oracle_rate(cfg, inp, dec, nthreads):
+    """Channels per second of the oracle on all host threads, from a probe of several channels per
+    thread (so the probe itself runs in parallel like the timed sample)."""
+    probe = _sample_rows(cfg, max(4 * nthreads, 16))
     t = time.perf_counter()
     _oracle_step(cfg, inp, dec, probe, nthreads)
-    per_row = max(time.perf_counter() - t, 1e-4) / len(probe)
-    rows = _sample_rows(cfg, target_s / per_row)
-    passes = max(1, min(50, int(target_s / max(per_row * len(rows), 1e-3))))
+    return len(probe) / max(time.perf_counter() - t, 1e-4)
+
+
+def cpu_baseline(cfg, inp, dec, target_s=15.0):
+    """The fp64 oracle as it stands, on the host cores, over a bounded sample of the workload
+    (evenly spaced channels, full sequence length each; repeated passes when the whole workload
+    takes less than the target time)."""
+    nthreads = os.cpu_count() or 1
+    rate = _oracle_rate(cfg, inp, dec, nthreads)
+    n = cfg.batch * cfg.dim
+    rows = _sample_rows(cfg, target_s * rate)
+    passes = max(1, min(100, int(round(target_s * rate / len(rows)))))
     t = time.perf_counter()
     for _ in range(passes):
         _oracle_step(cfg, inp, dec, rows, nthreads)
     dt = time.perf_counter() - t
     return {"value": passes * len(rows) * (cfg.seqlen + 1) / dt, "unit": "elements/s", "cores": nthreads,
             "kind": "oracle",
-            "sample": f"{passes} pass(es) over {len(rows)} of {cfg.batch * cfg.dim} channels (evenly spaced), "
-                      f"full L={cfg.seqlen} scan + 1 decode step each, {dt:.1f} s wall"}
+            "sample": f"{passes} pass(es) over {len(rows)} of {n} channels (evenly spaced), "
+                      f"full L={cfg.seqlen} scan + 1 decode step each, {dt:.1f} s wall on {nthreads} threads"}
 
 
 def run_reference(args, cfg, rank):
@@ -463,11 +471,8 @@ def run_reference(args, cfg, rank):
     inp, dec = host_inputs(cfg)
     nthreads = os.cpu_count() or 1
     K, W = max(1, args.steps), max(0, args.warmup)
-    probe = _sample_rows(cfg, max(nthreads, 8))
-    t = time.perf_counter()
-    _oracle_step(cfg, inp, dec, probe, nthreads)
-    per_row = max(time.perf_counter() - t, 1e-4) / len(probe)
-    rows = _sample_rows(cfg, max(1.0, (120.0 / (K + W)) / per_row))
+    rate = _oracle_rate(cfg, inp, dec, nthreads)
+    rows = _sample_rows(cfg, max(1.0, (120.0 / (K + W)) * rate))
     for _ in range(W):
         _oracle_step(cfg, inp, dec, rows, nthreads)
     t = time.perf_counter()

@@ -15,6 +15,7 @@
 #include "mamba_scan.h"
 #include "common.cuh"
 #include "scan_fwd.cuh"
+#include "scan_fwd_tm.cuh"
 #include "state_step.cuh"
 
 namespace mscan {
@@ -81,7 +82,7 @@ struct FwdPlan {
     int nseg;
     long long seg_len;
     int upr, kcta, wmax, wlo, nstage;
-    int stage_bytes, bc_off, quad_off, scratch_off, bar_off, smem_bytes;
+    int stage_bytes, bc_off, quad_off, scratch_off, src_off, bar_off, smem_bytes;
 };
 
 // Work split.  Units (8 channels of one batch row, one consumer warp each) are the grain.  The
@@ -89,7 +90,7 @@ struct FwdPlan {
 // (a split costs one extra pass over delta, u and B for all but the last segment).  Each
 // (segment, batch row) gets kcta CTAs with an even share of its units, so that the grid is about
 // one CTA per SM and the per-SM work differs by at most one unit.
-template <typename TIn, int NP>
+template <typename TIn, int NP, bool TM>
 static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     constexpr int TC = Chunk<TIn>::TC;
     const long long L = s->seqlen;
@@ -117,9 +118,12 @@ static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     // shared memory: NS stages of [u | delta | z tiles (1 KB per unit each) | B, C tiles | quads],
     // then per-warp scratch, then 3 NS mbarriers.  Consumer warps per CTA are capped so that two
     // stages fit.
-    const int bc_bytes = 2 * NP * 128, quad_bytes = TC * (NP / 2) * 16;
+    // (tensor-memory variant: no quads in the stages; two 8 KB copy sources; 4 more mbarriers)
+    const int bc_bytes = 2 * NP * 128, quad_bytes = TM ? 0 : TC * (NP / 2) * 16;
+    const int wscratch = TM ? kWarpScratchT : kWarpScratch;
+    const int extra = TM ? 2 * kSrcBytes + 4 * 8 + 16 : 0;
     auto stage_of = [&](int w) { return (3 * w * 1024 + bc_bytes + quad_bytes + 1023) / 1024 * 1024; };
-    auto smem_of = [&](int w, int ns) { return ns * stage_of(w) + w * kWarpScratch + 3 * ns * 8 + 1024; };
+    auto smem_of = [&](int w, int ns) { return ns * stage_of(w) + w * wscratch + extra + 3 * ns * 8 + 1024; };
     int wcap = kMaxConsumerWarps;
     while (wcap > 1 && smem_of(wcap, 2) > kSmemLimit) --wcap;
     const int wforce = env_int("MAMBA_SCAN_WMAX", 0);
@@ -146,7 +150,8 @@ static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     while (ns > 2 && smem_of(p.wmax, ns) > kSmemLimit) --ns;
     p.nstage = ns;
     p.scratch_off = ns * p.stage_bytes;
-    p.bar_off = p.scratch_off + p.wmax * kWarpScratch;
+    p.src_off = p.scratch_off + p.wmax * wscratch;
+    p.bar_off = p.src_off + (TM ? 2 * kSrcBytes : 0);
     p.smem_bytes = smem_of(p.wmax, ns);
     if (p.smem_bytes > kSmemLimit) return fail(MAMBA_ERR_ARG, "tiling needs %d bytes of shared memory", p.smem_bytes);
     return MAMBA_OK;
@@ -166,10 +171,10 @@ static int allow_smem(K kern, std::atomic<unsigned long long>& done_mask) {
     return MAMBA_OK;
 }
 
-template <typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE>
+template <typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE, bool TM>
 static int launch_fwd_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
     static std::atomic<unsigned long long> attr_done{0};
-    auto kern = scan_fwd_kernel<TIn, NP, TMA, AGG, SP, GATE>;
+    auto kern = TM ? scan_fwd_tm_kernel<TIn, TMA, AGG, SP, GATE> : scan_fwd_kernel<TIn, NP, TMA, AGG, SP, GATE>;
     int rc = allow_smem(kern, attr_done);
     if (rc) return rc;
     kern<<<grid, 32 * (a.wmax + 1), smem_bytes, st>>>(a, maps);
@@ -180,31 +185,31 @@ static int launch_fwd_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, 
 }
 
 // Selects the instantiation for the runtime flags (data path, softplus, gate).
-template <typename TIn, int NP, bool AGG>
+template <typename TIn, int NP, bool AGG, bool TM>
 static int launch_fwd(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, bool tma, bool sp,
                       bool gate, cudaStream_t st) {
     if constexpr (AGG) {  // the aggregate pass reads no z
-        if (tma) return sp ? launch_fwd_one<TIn, NP, true, true, true, false>(a, maps, grid, smem_bytes, st)
-                           : launch_fwd_one<TIn, NP, true, true, false, false>(a, maps, grid, smem_bytes, st);
-        return sp ? launch_fwd_one<TIn, NP, false, true, true, false>(a, maps, grid, smem_bytes, st)
-                  : launch_fwd_one<TIn, NP, false, true, false, false>(a, maps, grid, smem_bytes, st);
+        if (tma) return sp ? launch_fwd_one<TIn, NP, true, true, true, false, TM>(a, maps, grid, smem_bytes, st)
+                           : launch_fwd_one<TIn, NP, true, true, false, false, TM>(a, maps, grid, smem_bytes, st);
+        return sp ? launch_fwd_one<TIn, NP, false, true, true, false, TM>(a, maps, grid, smem_bytes, st)
+                  : launch_fwd_one<TIn, NP, false, true, false, false, TM>(a, maps, grid, smem_bytes, st);
     } else {
         if (tma) {
-            if (sp) return gate ? launch_fwd_one<TIn, NP, true, false, true, true>(a, maps, grid, smem_bytes, st)
-                                : launch_fwd_one<TIn, NP, true, false, true, false>(a, maps, grid, smem_bytes, st);
-            return gate ? launch_fwd_one<TIn, NP, true, false, false, true>(a, maps, grid, smem_bytes, st)
-                        : launch_fwd_one<TIn, NP, true, false, false, false>(a, maps, grid, smem_bytes, st);
+            if (sp) return gate ? launch_fwd_one<TIn, NP, true, false, true, true, TM>(a, maps, grid, smem_bytes, st)
+                                : launch_fwd_one<TIn, NP, true, false, true, false, TM>(a, maps, grid, smem_bytes, st);
+            return gate ? launch_fwd_one<TIn, NP, true, false, false, true, TM>(a, maps, grid, smem_bytes, st)
+                        : launch_fwd_one<TIn, NP, true, false, false, false, TM>(a, maps, grid, smem_bytes, st);
         }
-        if (sp) return gate ? launch_fwd_one<TIn, NP, false, false, true, true>(a, maps, grid, smem_bytes, st)
-                            : launch_fwd_one<TIn, NP, false, false, true, false>(a, maps, grid, smem_bytes, st);
-        return gate ? launch_fwd_one<TIn, NP, false, false, false, true>(a, maps, grid, smem_bytes, st)
-                    : launch_fwd_one<TIn, NP, false, false, false, false>(a, maps, grid, smem_bytes, st);
+        if (sp) return gate ? launch_fwd_one<TIn, NP, false, false, true, true, TM>(a, maps, grid, smem_bytes, st)
+                            : launch_fwd_one<TIn, NP, false, false, true, false, TM>(a, maps, grid, smem_bytes, st);
+        return gate ? launch_fwd_one<TIn, NP, false, false, false, true, TM>(a, maps, grid, smem_bytes, st)
+                    : launch_fwd_one<TIn, NP, false, false, false, false, TM>(a, maps, grid, smem_bytes, st);
     }
 }
 
-template <typename TIn, int NP>
 // `scratch`/`scratch_cap`: when scratch is non-NULL the segment carries live there (no allocation);
 // otherwise they come from cudaMallocAsync on `st`.
+template <typename TIn, int NP, bool TM>
 static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gate, float2* scratch,
                    size_t scratch_cap, cudaStream_t st) {
     constexpr int TC = Chunk<TIn>::TC;
@@ -216,7 +221,7 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
 
     FwdPlan p;
-    int rc = plan_fwd<TIn, NP>(s, nsm, p);
+    int rc = plan_fwd<TIn, NP, TM>(s, nsm, p);
     if (rc) return rc;
 
     const bool tma_ok = encode_fn() != nullptr && (L * esize) % 16 == 0 && aligned16(a.u) && aligned16(a.delta) &&
@@ -250,6 +255,7 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
     a.bc_off = p.bc_off;
     a.quad_off = p.quad_off;
     a.scratch_off = p.scratch_off;
+    a.src_off = p.src_off;
     a.bar_off = p.bar_off;
     a.agg = nullptr;
 
@@ -267,11 +273,11 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
             owned = true;
         }
         const unsigned g1 = (unsigned)((long long)s->batch * (p.nseg - 1) * p.kcta);
-        rc = launch_fwd<TIn, NP, true>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
+        rc = launch_fwd<TIn, NP, true, TM>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
     }
     if (rc == MAMBA_OK) {
         const unsigned g2 = (unsigned)((long long)s->batch * p.nseg * p.kcta);
-        rc = launch_fwd<TIn, NP, false>(a, maps, g2, p.smem_bytes, tma_ok, softplus, gate, st);
+        rc = launch_fwd<TIn, NP, false, TM>(a, maps, g2, p.smem_bytes, tma_ok, softplus, gate, st);
     }
     if (owned) {
         cudaError_t e = cudaFreeAsync(a.agg, st);
@@ -283,7 +289,11 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
 template <typename TIn, int NP>
 static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, bool gate, float2* scratch,
                         size_t scratch_cap, cudaStream_t st) {
-    return fwd_run<TIn, NP>(s, a, softplus, gate, scratch, scratch_cap, st);
+    // N <= 16 with MAMBA_SCAN_TMEM=1: the variant that feeds B/C through tensor memory (not the
+    // default: slower on the measured workloads)
+    if constexpr (NP == 16)
+        if (getenv("MAMBA_SCAN_TMEM") != nullptr) return fwd_run<TIn, NP, true>(s, a, softplus, gate, scratch, scratch_cap, st);
+    return fwd_run<TIn, NP, false>(s, a, softplus, gate, scratch, scratch_cap, st);
 }
 
 // ---------------------------------------------------------------------------- checks

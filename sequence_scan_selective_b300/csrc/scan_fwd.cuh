@@ -72,7 +72,7 @@ struct FwdArgs {
     int wmax;    // consumer warps per CTA; warp wmax is the producer
     int wlo;     // CTAs with this many units use the narrow u/delta/z maps (index 0)
     int nstage;  // stages in the ring
-    int stage_bytes, bc_off, quad_off, scratch_off, bar_off;
+    int stage_bytes, bc_off, quad_off, scratch_off, src_off, bar_off;
 };
 
 // u, delta, z maps: [0] box of 8*wlo rows, [1] box of 8*(wlo+1) rows; B, C: box [N, TC].

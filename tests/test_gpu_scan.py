@@ -214,3 +214,19 @@ def test_wide_state_many_channels(ms):
     """N = 64 with many channels: the plan caps warps per CTA so the tiles fit in shared memory."""
     cfg = synth.CONFIGS["m130"].replace(batch=1, dim=2048, dstate=64, seqlen=256, seed=15)
     _check_full(ms, cfg)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", ["plain", "split", "ragged"])
+def test_tensor_memory_variant(ms, dtype, case):
+    """The variant that stages B/C in tensor memory (tcgen05.cp / tcgen05.ld) computes the same scan."""
+    if case == "plain":
+        cfg = synth.CONFIGS["m130"].replace(batch=2, dim=130, seqlen=512, dtype=dtype, seed=16)
+        env = {"MAMBA_SCAN_TMEM": "1"}
+    elif case == "split":
+        cfg = synth.CONFIGS["long"].replace(batch=1, dim=40, seqlen=6000, dtype=dtype, seed=17)
+        env = {"MAMBA_SCAN_TMEM": "1", "MAMBA_SCAN_NSEG": "3"}
+    else:
+        cfg = synth.CONFIGS["m130"].replace(batch=2, dim=33, dstate=5, seqlen=301, dtype=dtype, seed=18)
+        env = {"MAMBA_SCAN_TMEM": "1"}
+    _check_full(ms, cfg, env=env)

@@ -323,16 +323,10 @@ def run_ours(args, cfg, rank, world, local_rank):
     ms.device_status()
     total_ms = t_start.elapsed_time(t_end)
     scan_avg_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
-    if dist:
-        t = torch.tensor([total_ms, scan_avg_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, scan_avg_ms = float(t[0]), float(t[1])
-        lt = torch.tensor([launches], device=dev, dtype=torch.float64)
-        dist.all_reduce(lt)
-        launches = int(lt.item())
+    total_ms, scan_avg_ms, launches = aggregate_ranks(dist, dev, total_ms, scan_avg_ms, launches)
 
     elems_step = cfg.batch * cfg.dim * (cfg.seqlen + 1)
-    value = elems_step * K * world / (total_ms * 1e-3)
+    value = whole_job_rate(elems_step, K, world, total_ms)
     e2e = None if args.no_e2e else run_e2e(args, cfg, inp, dec, params, dev, world, dist)
 
     peaks, kind = measured_peaks()
@@ -362,6 +356,26 @@ def run_ours(args, cfg, rank, world, local_rank):
     if dist:
         dist.destroy_process_group()
     return line
+
+
+def aggregate_ranks(dist, device, total_ms: float, scan_avg_ms: float, launches: int):
+    """Whole-job view of a timed region run by every rank on its own replica: the slowest rank's
+    times (max over ranks) and the kernel launches of all ranks (sum).  `dist` is None for one
+    process; any backend works (NCCL tensors on the GPU, gloo on the CPU)."""
+    if dist is None:
+        return total_ms, scan_avg_ms, launches
+    import torch
+    t = torch.tensor([total_ms, scan_avg_ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    lt = torch.tensor([launches], device=device, dtype=torch.float64)
+    dist.all_reduce(lt)
+    return float(t[0]), float(t[1]), int(lt.item())
+
+
+def whole_job_rate(elems_per_step: int, steps: int, world: int, total_ms: float) -> float:
+    """Elements per second of all ranks together: each rank processed elems_per_step * steps
+    elements of its own replica within the (max over ranks) timed region."""
+    return elems_per_step * steps * world / (total_ms * 1e-3)
 
 
 def run_e2e(args, cfg, inp, dec, params, dev, world, dist):
@@ -485,7 +499,7 @@ def run_reference(args, cfg, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": args.gpus,
         "steps": K, "warmup": W, "ms_per_step": dt / K * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, recipe of the workload)",
-        "config": {"workload": WORKLOADS[args.workload], "batch": cfg.batch, "d_inner": cfg.dim,
+        "config": {"workload": WORKLOADS.get(args.workload, cfg.name), "batch": cfg.batch, "d_inner": cfg.dim,
                    "d_state": cfg.dstate, "seq_len": cfg.seqlen, "storage": cfg.dtype},
         "cpu_baseline": {"value": value, "unit": "elements/s", "cores": nthreads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

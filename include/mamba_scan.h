@@ -77,6 +77,23 @@ int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const void* delta, 
                    void* stream);
 
 /*
+ * Forward selective scan from a given state: mamba_scan_fwd with the recurrence started from h0
+ * instead of zero, so that a long prompt can be scanned in pieces and handed on to decoding
+ * (recurrent inference carries only the state: news write-up, "architecture" section; visual
+ * guide section 2.4).
+ *
+ *   h0            [b, d, N]  fp32 or NULL (= zero): h before position 0.  It may be the same
+ *                            buffer as last_state (the call then advances that state in place);
+ *                            partial overlap with last_state, or any overlap with y, is
+ *                            MAMBA_ERR_ARG.
+ *   With L == 0, last_state receives h0 (or zeros).  Everything else as for mamba_scan_fwd.
+ */
+int mamba_scan_fwd_state(const mamba_scan_shape* s, const void* u, const void* delta, const float* A,
+                         const void* B, const void* C, const float* D, const void* z,
+                         const float* delta_bias, int softplus_flag, const float* h0, void* y,
+                         float* last_state, void* stream);
+
+/*
  * One recurrent decoding step for every (batch, channel): constant work per token, no cache of
  * past tokens (news write-up, "architecture" section; visual guide section 1.4).
  *

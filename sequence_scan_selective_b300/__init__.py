@@ -47,6 +47,8 @@ def _load() -> ctypes.CDLL:
     for name in ("mamba_scan_fwd", "mamba_scan_fwd_noalloc"):
         getattr(lib, name).restype = I
         getattr(lib, name).argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, I, P, P, P]
+    lib.mamba_scan_fwd_state.restype = I
+    lib.mamba_scan_fwd_state.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, I, P, P, P, P]
     lib.mamba_state_step.restype = I
     lib.mamba_state_step.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, I, P, P]
     lib.mamba_scan_last_error.restype = ctypes.c_char_p
@@ -63,7 +65,7 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 
 # symbols the header declares; the tests check that every one of them is exported
-EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_state_step", "mamba_scan_last_error", "mamba_scan_version",
+EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_state", "mamba_state_step", "mamba_scan_last_error", "mamba_scan_version",
             "mamba_scan_device_status", "mamba_scan_launch_count")
 
 
@@ -125,10 +127,14 @@ class PreparedCall:
 
 
 def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
-                   last_state=None, want_state=True, stream=None):
+                   last_state=None, want_state=True, stream=None, h0=None):
     """Selective scan.  u, delta, z [b, d, L]; B, C [b, N, L] (float32 or bfloat16, all the same);
-    A [d, N], D [d], delta_bias [d] float32.  Returns (y [b, d, L] in the input dtype,
-    last_state [b, d, N] float32 or None)."""
+    A [d, N], D [d], delta_bias [d] float32; h0 [b, d, N] float32 initial state (None = zero; it may
+    be the last_state tensor itself).  Returns (y [b, d, L] in the input dtype, last_state
+    [b, d, N] float32 or None)."""
+    if h0 is not None:
+        return _scan(_lib.mamba_scan_fwd_state, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
+                     want_state, stream, h0)
     return _scan(_lib.mamba_scan_fwd, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
                  want_state, stream)
 
@@ -142,7 +148,7 @@ def mamba_scan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=None, s
                  want_state, stream)
 
 
-def _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream):
+def _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream, h0=None):
     bsz, dim, L = u.shape
     N = A.shape[1]
     dt = u.dtype
@@ -157,14 +163,17 @@ def _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
         _ptr(A, (dim, N), torch.float32, "A"), _ptr(B, (bsz, N, L), dt, "B"),
         _ptr(C, (bsz, N, L), dt, "C"), _ptr(D, (dim,), torch.float32, "D"),
         _ptr(z, (bsz, dim, L), dt, "z"), _ptr(delta_bias, (dim,), torch.float32, "delta_bias"),
-        int(bool(softplus)), _ptr(y, (bsz, dim, L), dt, "y"),
-        _ptr(last_state, (bsz, dim, N), torch.float32, "last_state"), _stream(stream, u.device))
+        int(bool(softplus)))
+    if fn is _lib.mamba_scan_fwd_state:
+        args = args + (_ptr(h0, (bsz, dim, N), torch.float32, "h0"),)
+    args = args + (_ptr(y, (bsz, dim, L), dt, "y"), _ptr(last_state, (bsz, dim, N), torch.float32, "last_state"),
+                   _stream(stream, u.device))
     return args, shape, y, last_state
 
 
-def _scan(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream):
+def _scan(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream, h0=None):
     args, _shape, y, last_state = _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
-                                             want_state, stream)
+                                             want_state, stream, h0)
     _check(fn(*args))
     return y, last_state
 

@@ -75,6 +75,8 @@ static int env_int(const char* name, int dflt) {
     return (v && *v) ? atoi(v) : dflt;
 }
 
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb);
+
 // ---------------------------------------------------------------------------- forward plan
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -261,16 +263,31 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
 
     bool owned = false;
     if (p.nseg > 1) {
-        const size_t bytes = (size_t)(p.nseg - 1) * s->batch * s->dim * s->dstate * sizeof(float2);
+        const size_t nstate = (size_t)s->batch * s->dim * s->dstate;
+        const size_t bytes = (size_t)(p.nseg - 1) * nstate * sizeof(float2);
+        // An initial state that shares memory with last_state is copied first: the last segment
+        // writes last_state while CTAs of earlier segments may still be reading the initial state.
+        const bool copy_h0 = a.h0 != nullptr && overlaps(a.h0, nstate * 4, a.last_state, nstate * 4);
+        const size_t total = bytes + (copy_h0 ? nstate * sizeof(float) : 0);
+        if (copy_h0 && scratch != nullptr) return fail(MAMBA_ERR_ARG, "internal: initial state with fixed scratch");
         if (scratch != nullptr) {
             if (bytes > scratch_cap)
                 return fail(MAMBA_ERR_ARG, "this shape splits the sequence into %d segments whose carries need %zu bytes "
                             "of scratch; the fixed scratch holds %zu bytes", p.nseg, bytes, scratch_cap);
             a.agg = scratch;
         } else {
-            cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&a.agg), bytes, st);
+            cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&a.agg), total, st);
             if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync (segment carries)");
             owned = true;
+            if (copy_h0) {
+                float* hcopy = reinterpret_cast<float*>(reinterpret_cast<char*>(a.agg) + bytes);
+                e = cudaMemcpyAsync(hcopy, a.h0, nstate * sizeof(float), cudaMemcpyDeviceToDevice, st);
+                if (e != cudaSuccess) {
+                    cudaFreeAsync(a.agg, st);
+                    return cuda_fail(e, "cudaMemcpyAsync (initial state)");
+                }
+                a.h0 = hcopy;
+            }
         }
         const unsigned g1 = (unsigned)((long long)s->batch * (p.nseg - 1) * p.kcta);
         rc = launch_fwd<TIn, NP, true, TM>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
@@ -338,7 +355,8 @@ using namespace mscan;
 
 static int scan_fwd_impl(const mamba_scan_shape* s, const void* u, const void* delta, const float* A, const void* B,
                          const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
-                         void* y, float* last_state, float2* scratch, size_t scratch_cap, void* stream) {
+                         const float* h0, void* y, float* last_state, float2* scratch, size_t scratch_cap,
+                         void* stream) {
     t_err.clear();
     int rc = check_shape(s, true);
     if (rc) return rc;
@@ -346,8 +364,11 @@ static int scan_fwd_impl(const mamba_scan_shape* s, const void* u, const void* d
     const long long chans = (long long)s->batch * s->dim;
     if (s->seqlen == 0) {
         if (last_state) {
-            cudaError_t e = cudaMemsetAsync(last_state, 0, (size_t)chans * s->dstate * sizeof(float), st);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(last_state)");
+            const size_t nb = (size_t)chans * s->dstate * sizeof(float);
+            cudaError_t e = h0 ? (h0 == last_state ? cudaSuccess
+                                                   : cudaMemcpyAsync(last_state, h0, nb, cudaMemcpyDeviceToDevice, st))
+                               : cudaMemsetAsync(last_state, 0, nb, st);
+            if (e != cudaSuccess) return cuda_fail(e, "last_state for an empty sequence");
         }
         return MAMBA_OK;
     }
@@ -357,12 +378,16 @@ static int scan_fwd_impl(const mamba_scan_shape* s, const void* u, const void* d
     const size_t nx = (size_t)chans * s->seqlen * es;
     const size_t nbc = (size_t)s->batch * s->dstate * s->seqlen * es;
     if (overlaps(y, nx, u, nx) || overlaps(y, nx, delta, nx) || overlaps(y, nx, z, nx) || overlaps(y, nx, B, nbc) ||
-        overlaps(y, nx, C, nbc) || overlaps(y, nx, last_state, (size_t)chans * s->dstate * 4))
+        overlaps(y, nx, C, nbc) || overlaps(y, nx, last_state, (size_t)chans * s->dstate * 4) ||
+        overlaps(y, nx, h0, (size_t)chans * s->dstate * 4))
         return fail(MAMBA_ERR_ARG, "y overlaps an input or last_state");
+    if (h0 && last_state && h0 != last_state &&
+        overlaps(h0, (size_t)chans * s->dstate * 4, last_state, (size_t)chans * s->dstate * 4))
+        return fail(MAMBA_ERR_ARG, "h0 and last_state must be the same buffer or not overlap");
     FwdArgs a{};
     a.u = u; a.delta = delta; a.z = z; a.B = B; a.C = C;
     a.A = A; a.D = D; a.bias = delta_bias;
-    a.y = y; a.last_state = last_state;
+    a.y = y; a.last_state = last_state; a.h0 = h0;
     a.batch = s->batch; a.dim = s->dim; a.dstate = s->dstate;
     a.L = s->seqlen;
     const bool sp = softplus_flag != 0, gate = z != nullptr;
@@ -378,7 +403,16 @@ extern "C" int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const vo
                               const void* B, const void* C, const float* D, const void* z,
                               const float* delta_bias, int softplus_flag, void* y, float* last_state,
                               void* stream) {
-    return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, nullptr, 0, stream);
+    return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr, y, last_state, nullptr, 0,
+                         stream);
+}
+
+extern "C" int mamba_scan_fwd_state(const mamba_scan_shape* s, const void* u, const void* delta, const float* A,
+                                    const void* B, const void* C, const float* D, const void* z,
+                                    const float* delta_bias, int softplus_flag, const float* h0, void* y,
+                                    float* last_state, void* stream) {
+    return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, h0, y, last_state, nullptr, 0,
+                         stream);
 }
 
 // ---------------------------------------------------------------------------- allocation-free variant
@@ -417,7 +451,7 @@ extern "C" int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, 
     float2* scratch = nullptr;
     rc = noalloc_scratch(&scratch);
     if (rc) return rc;
-    return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, scratch,
+    return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr, y, last_state, scratch,
                          (size_t)MAMBA_NOALLOC_SCRATCH_BYTES, stream);
 }
 

@@ -62,6 +62,7 @@ struct FwdArgs {
     const float* bias;
     void* y;
     float* last_state;
+    const float* h0;  // [batch][dim][dstate] state before the first position, or NULL (zero)
     float2* agg;  // [nseg-1][batch][dim][dstate]: (prod Abar, h_end) of each segment
     int batch, dim, dstate;
     long long L;
@@ -260,12 +261,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
     float2 A2[G / 2];
     float2 h[G / 2];
+    const float* h0 = (!AGG && cvalid && a.h0 != nullptr) ? a.h0 + row * N : nullptr;
 #pragma unroll
     for (int p = 0; p < G / 2; ++p) {
         const int n0 = g * G + 2 * p, n1 = n0 + 1;
         A2[p].x = (cvalid && n0 < N) ? a.A[(long long)dch * N + n0] * kLog2e : 0.f;
         A2[p].y = (cvalid && n1 < N) ? a.A[(long long)dch * N + n1] * kLog2e : 0.f;
-        h[p] = make_float2(0.f, 0.f);
+        h[p] = make_float2((h0 && n0 < N) ? h0[n0] : 0.f, (h0 && n1 < N) ? h0[n1] : 0.f);
     }
     if (!AGG && seg > 0 && cvalid) {
         // fold the carries of segments 0 .. seg-1 in order: h <- prod Abar * h + h_end

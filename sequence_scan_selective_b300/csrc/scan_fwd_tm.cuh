@@ -227,10 +227,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
         f2p A2[G / 2];  // A * log2(e) of the lane's state pairs
         f2p h[G / 2];   // the lane's states, as packed pairs
+        const float* hin = (!AGG && cvalid && a.h0 != nullptr) ? a.h0 + row * N : nullptr;
 #pragma unroll
         for (int p = 0; p < G / 2; ++p) {
             const int n0 = g * G + 2 * p, n1 = n0 + 1;
-            float h0 = 0.f, h1 = 0.f;
+            float h0 = (hin && n0 < N) ? hin[n0] : 0.f, h1 = (hin && n1 < N) ? hin[n1] : 0.f;
             if (!AGG && seg > 0 && cvalid) {
                 // fold the carries of segments 0 .. seg-1 in order: h <- prod Abar * h + h_end
                 for (int q = 0; q < seg; ++q) {

@@ -230,3 +230,66 @@ def test_tensor_memory_variant(ms, dtype, case):
         cfg = synth.CONFIGS["m130"].replace(batch=2, dim=33, dstate=5, seqlen=301, dtype=dtype, seed=18)
         env = {"MAMBA_SCAN_TMEM": "1"}
     _check_full(ms, cfg, env=env)
+
+
+# ------------------------------------------------------------------------------ initial state
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_initial_state_matches_oracle(ms, dtype):
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=70, seqlen=300, dtype=dtype, seed=40)
+    inp = synth.scan_inputs(cfg)
+    h0 = np.random.default_rng(40).standard_normal((cfg.batch, cfg.dim, cfg.dstate)).astype(np.float32)
+    d = dev_inputs(inp, dtype)
+    y, st = ms.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], True,
+                              h0=torch.from_numpy(h0).cuda())
+    torch.cuda.synchronize()
+    y_ref, st_ref = oracle.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                inp["delta_bias"], True, dtype, h0=h0.astype(np.float64))
+    assert rel_err(from_dev(y), y_ref) <= TOL[dtype]
+    assert rel_err(from_dev(st), st_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", ["wide", "split"])
+def test_chunked_prefill_in_place(ms, dtype, shape):
+    """A sequence scanned in pieces, each piece continuing from the state the previous one left in
+    the same buffer (h0 is last_state), gives the scan of the whole sequence (the recurrence only
+    carries h across positions, visual guide section 2.4)."""
+    if shape == "wide":
+        cfg = synth.CONFIGS["m130"].replace(batch=2, dim=64, seqlen=960, dtype=dtype, seed=41)
+        cuts = [0, 320, 653, 960]          # the middle piece has a ragged length
+    else:                                   # few channels: every piece is split along L internally
+        cfg = synth.CONFIGS["long"].replace(batch=1, dim=32, seqlen=12000, dtype=dtype, seed=42)
+        cuts = [0, 4000, 8001, 12000]
+    inp = synth.scan_inputs(cfg)
+    d = dev_inputs(inp, dtype)
+    state = torch.zeros((cfg.batch, cfg.dim, cfg.dstate), device="cuda")
+    ys = []
+    for a_, b_ in zip(cuts[:-1], cuts[1:]):
+        piece = lambda k: d[k][:, :, a_:b_].contiguous()
+        y, _ = ms.mamba_scan_fwd(piece("u"), piece("delta"), d["A"], piece("B"), piece("C"), d["D"], piece("z"),
+                                 d["delta_bias"], True, h0=state, last_state=state)
+        ys.append(y)
+    torch.cuda.synchronize()
+    ms.device_status()
+    y_ref, st_ref = oracle_scan_full(inp, dtype)
+    assert rel_err(from_dev(torch.cat(ys, dim=2)), y_ref) <= TOL[dtype]
+    assert rel_err(from_dev(state), st_ref) <= TOL[dtype]
+
+
+def test_initial_state_empty_sequence(ms):
+    h0 = torch.randn((2, 8, 4), device="cuda")
+    st = torch.full((2, 8, 4), 7.0, device="cuda")
+    z = torch.zeros((2, 8, 0), device="cuda")
+    ms.mamba_scan_fwd(z, z.clone(), -torch.ones((8, 4), device="cuda"), torch.zeros((2, 4, 0), device="cuda"),
+                      torch.zeros((2, 4, 0), device="cuda"), h0=h0, last_state=st)
+    torch.cuda.synchronize()
+    assert torch.equal(st, h0)
+
+
+def test_initial_state_partial_overlap_rejected(ms):
+    buf = torch.zeros((2 * 8 * 4 + 4,), device="cuda")
+    h0, st = buf[:64].view(2, 8, 4), buf[4:68].view(2, 8, 4)
+    x = torch.zeros((2, 8, 16), device="cuda")
+    with pytest.raises(ms.MambaScanError, match="same buffer"):
+        ms.mamba_scan_fwd(x, x.clone(), -torch.ones((8, 4), device="cuda"), torch.zeros((2, 4, 16), device="cuda"),
+                          torch.zeros((2, 4, 16), device="cuda"), h0=h0, last_state=st)

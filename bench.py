@@ -452,7 +452,8 @@ def _sample_rows(cfg, budget_rows):
 def _oracle_rate(cfg, inp, dec, nthreads):
     """Channels per second of the oracle on all host threads, from a probe of several channels per
     thread (so the probe itself runs in parallel like the timed sample)."""
-    probe = _sample_rows(cfg, max(4 * nthreads, 16))
+    _oracle_step(cfg, inp, dec, _sample_rows(cfg, nthreads), nthreads)  # warm-up: library load, threads
+    probe = _sample_rows(cfg, max(16 * nthreads, 64))
     t = time.perf_counter()
     _oracle_step(cfg, inp, dec, probe, nthreads)
     return len(probe) / max(time.perf_counter() - t, 1e-4)

@@ -21,12 +21,16 @@
 //    (B_n, B_n+1, C_n, C_n+1) fp32 quads per step so that consumers read one quad per state pair.
 //  * Consumers walk each chunk in slots of 16 steps, in three phases per slot:
 //      A  lane (c, g) forms Delta = softplus(delta + bias), Delta*u, D*u and silu(z) for its 4
-//         owned steps (16-byte tile reads), and publishes (Delta, Delta, Delta*u, Delta*u)
-//         quads in the warp's scratch;
-//      B  all lanes advance their G states through the 16 steps (one quad of Delta per step, one
-//         B/C quad per state pair), leaving per-step partial sums of C.h;
+//         owned steps (16-byte tile reads), and publishes (Delta_t, Delta*u_t) pairs in the
+//         warp's scratch (two steps per 16 bytes);
+//      B  all lanes advance their G states through the 16 steps (one 16-byte read of Delta pairs
+//         per two steps, one B/C quad per state pair per step), leaving per-step partial sums
+//         of C.h;
 //      C  lane (c, g) sums the 4 partials of its owned steps, adds D*u, applies the gate and
 //         stores y with one 128-bit (fp32) or 64-bit (bf16) store.
+//    The phases of a slot run back to back (a software pipeline across slots was measured
+//    slower: it needs more registers and instructions).  The operand reads of phase B go through
+//    the SM's shared-memory pipe, which bounds the loop; the pair layout halves the Delta bytes.
 //  * Few channels (long sequences): the time axis is split into segments.  An aggregate launch
 //    computes each segment's carry (prod Abar = 2^(A log2e sum Delta), h_end from zero); the full
 //    launch folds the carries of the preceding segments into its initial state.  This regroups
@@ -44,10 +48,10 @@ constexpr int kUnitCh = 8;      // channels per work unit (one warp)
 constexpr int kLanesPerCh = 4;  // lanes sharing one channel's states
 constexpr int kSlot = 16;       // steps per slot
 constexpr int kOwned = kSlot / kLanesPerCh;  // steps whose per-element work a lane does
-constexpr int kQPitch = kSlot * 16 + 16;     // bytes per channel row of Delta quads (padded)
+constexpr int kQPitch = 9 * 16;              // bytes per channel row of (Delta, Delta*u) pairs (padded)
 constexpr int kYPitch = kSlot * 4 + 16;      // bytes per (lane group, channel) row of partials
-constexpr int kQBuf = kUnitCh * kQPitch;       // one buffer of Delta quads (8 channels)
-constexpr int kWarpScratch = 2 * kQBuf + kLanesPerCh * kUnitCh * kYPitch;  // 6912 bytes
+constexpr int kQBuf = kUnitCh * kQPitch;       // one buffer of Delta pairs (8 channels)
+constexpr int kWarpScratch = 2 * kQBuf + kLanesPerCh * kUnitCh * kYPitch;  // 4864 bytes
 constexpr int kMaxConsumerWarps = 15;
 constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
 
@@ -282,7 +286,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
     }
 
-    // warp scratch: two buffers of Delta quads (slot parity) and one of partial sums
+    // warp scratch: two buffers of Delta pairs (slot parity) and one of partial sums
     unsigned char* wsq = smem + a.scratch_off + wid * kWarpScratch;
     unsigned char* wsy = wsq + 2 * kQBuf;
     const int nslots = (int)((t_end - t_begin + kSlot - 1) / kSlot);
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         return __all_sync(0xffffffffu, mbar_wait_bounded(&qready[k % NS], (uint32_t)((k / NS) & 1), kWaitLimitNs));
     };
 
-    // Phase A of slot i: Delta, Delta*u of the 4 owned steps -> quads in wsq[i & 1]; returns
+    // Phase A of slot i: Delta, Delta*u of the 4 owned steps -> pairs in wsq[i & 1]; returns
     // D*u and the gate of the owned steps for phase C.
     auto phase_a = [&](int i, float2& skip01, float2& skip23, float2& gate01, float2& gate23) {
         const int k = i / SPC, sl = i % SPC;
@@ -336,11 +340,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
         const float2 du01 = fmul2(dt01, make_float2(uv[0], uv[1]));
         const float2 du23 = fmul2(dt23, make_float2(uv[2], uv[3]));
-        float4* qw = reinterpret_cast<float4*>(wsq + (i & 1) * kQBuf + c * kQPitch + g * kOwned * 16);
-        qw[0] = make_float4(dt01.x, dt01.x, du01.x, du01.x);
-        qw[1] = make_float4(dt01.y, dt01.y, du01.y, du01.y);
-        qw[2] = make_float4(dt23.x, dt23.x, du23.x, du23.x);
-        qw[3] = make_float4(dt23.y, dt23.y, du23.y, du23.y);
+        float4* qw = reinterpret_cast<float4*>(wsq + (i & 1) * kQBuf + c * kQPitch);
+        qw[2 * g] = make_float4(dt01.x, du01.x, dt01.y, du01.y);
+        qw[2 * g + 1] = make_float4(dt23.x, du23.x, dt23.y, du23.y);
         if (!AGG) {
             skip01 = fmul2(make_float2(Dd, Dd), make_float2(uv[0], uv[1]));
             skip23 = fmul2(make_float2(Dd, Dd), make_float2(uv[2], uv[3]));
@@ -362,7 +364,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                            sl * kSlot * NPAIR + g * (G / 2);
 #pragma unroll
         for (int t = 0; t < kSlot; ++t) {
-            const float4 q = qrow[t];  // (Delta, Delta, Delta*u, Delta*u)
+            const float4 q2 = qrow[t >> 1];  // (Delta_t, Delta*u_t, Delta_t+1, Delta*u_t+1)
+            const float dq = (t & 1) ? q2.z : q2.x, duq = (t & 1) ? q2.w : q2.y;
+            const float4 q = make_float4(dq, dq, duq, duq);
             if (AGG) sumdt += q.x;
             float2 ya;
 #pragma unroll
@@ -402,26 +406,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
     };
 
-    // Software pipeline over slots: phase A of slot i+1 and phase B of slot i share one region
-    // without warp barriers (so their instructions interleave), as does phase C of slot i with
-    // the next region.
     float2 sk01 = make_float2(0.f, 0.f), sk23 = sk01, gt01 = sk01, gt23 = sk01;
-    ok = wait_tiles(0);
-    if (ok) phase_a(0, sk01, sk23, gt01, gt23);
-    __syncwarp();
 #pragma unroll 1
     for (int i = 0; i < nslots && ok; ++i) {
         const int k = i / SPC, sl = i % SPC;
-        const bool next = i + 1 < nslots;
-        if (sl == 0) ok = wait_quads(k);
-        if (ok && next && sl == SPC - 1) ok = wait_tiles(k + 1);
+        if (sl == 0) {
+            ok = wait_tiles(k);
+            if (ok) ok = wait_quads(k);
+        }
         if (!ok) break;
-        float2 nk01 = make_float2(0.f, 0.f), nk23 = nk01, nt01 = nk01, nt23 = nk01;
-        if (next) phase_a(i + 1, nk01, nk23, nt01, nt23);
+        phase_a(i, sk01, sk23, gt01, gt23);
+        __syncwarp();
         float yp[kSlot];
         phase_b(i, yp);
         __syncwarp();
-        if (sl == SPC - 1 || !next) mbar_arrive(&empty[k % NS]);  // this lane is done with chunk k's stage
+        if (sl == SPC - 1 || i + 1 == nslots) mbar_arrive(&empty[k % NS]);
         if (!AGG) {
             float4* yw = reinterpret_cast<float4*>(wsy + (g * kUnitCh + c) * kYPitch);
 #pragma unroll
@@ -429,7 +428,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
         __syncwarp();
         if (!AGG) phase_c(i, sk01, sk23, gt01, gt23);
-        sk01 = nk01; sk23 = nk23; gt01 = nt01; gt23 = nt23;
+        __syncwarp();
     }
     if (!ok) {
         if (lane == 0) atomicExch(&g_status, 1);

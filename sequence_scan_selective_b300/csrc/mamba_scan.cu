@@ -92,11 +92,13 @@ struct FwdPlan {
 // (a split costs one extra pass over delta, u and B for all but the last segment).  Each
 // (segment, batch row) gets kcta CTAs with an even share of its units, so that the grid is about
 // one CTA per SM and the per-SM work differs by at most one unit.
-template <typename TIn, int NP, bool TM>
+template <typename TIn, int NP, bool TM, int LPC>
 static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     constexpr int TC = Chunk<TIn>::TC;
+    constexpr int CPW = TM ? kUnitCh : Layout<LPC>::CPW;  // channels per work unit
+    constexpr int UB = CPW * 128;                          // u/delta/z tile bytes per unit and chunk
     const long long L = s->seqlen;
-    p.upr = (s->dim + kUnitCh - 1) / kUnitCh;
+    p.upr = (s->dim + CPW - 1) / CPW;
     const long long units = (long long)s->batch * p.upr;
     long long want = env_int("MAMBA_SCAN_NSEG", 0);
     if (want <= 0) {
@@ -122,9 +124,9 @@ static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     // stages fit.
     // (tensor-memory variant: no quads in the stages; two 8 KB copy sources; 4 more mbarriers)
     const int bc_bytes = 2 * NP * 128, quad_bytes = TM ? 0 : TC * (NP / 2) * 16;
-    const int wscratch = TM ? kWarpScratchT : kWarpScratch;
+    const int wscratch = TM ? kWarpScratchT : Layout<LPC>::SCRATCH;
     const int extra = TM ? 2 * kSrcBytes + 4 * 8 + 16 : 0;
-    auto stage_of = [&](int w) { return (3 * w * 1024 + bc_bytes + quad_bytes + 1023) / 1024 * 1024; };
+    auto stage_of = [&](int w) { return (3 * w * UB + bc_bytes + quad_bytes + 1023) / 1024 * 1024; };
     auto smem_of = [&](int w, int ns) { return ns * stage_of(w) + w * wscratch + extra + 3 * ns * 8 + 1024; };
     int wcap = kMaxConsumerWarps;
     while (wcap > 1 && smem_of(wcap, 2) > kSmemLimit) --wcap;
@@ -144,7 +146,7 @@ static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     p.wlo = p.upr / p.kcta;
     if (rows * k > 0x7fffffffLL) return fail(MAMBA_ERR_ARG, "grid too large");
 
-    p.bc_off = 3 * p.wmax * 1024;
+    p.bc_off = 3 * p.wmax * UB;
     p.quad_off = p.bc_off + bc_bytes;
     p.stage_bytes = stage_of(p.wmax);
     int ns = env_int("MAMBA_SCAN_STAGES", 4);
@@ -173,10 +175,10 @@ static int allow_smem(K kern, std::atomic<unsigned long long>& done_mask) {
     return MAMBA_OK;
 }
 
-template <typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE, bool TM>
+template <typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE, bool TM, int LPC>
 static int launch_fwd_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
     static std::atomic<unsigned long long> attr_done{0};
-    auto kern = TM ? scan_fwd_tm_kernel<TIn, TMA, AGG, SP, GATE> : scan_fwd_kernel<TIn, NP, TMA, AGG, SP, GATE>;
+    auto kern = TM ? scan_fwd_tm_kernel<TIn, TMA, AGG, SP, GATE> : scan_fwd_kernel<TIn, NP, LPC, TMA, AGG, SP, GATE>;
     int rc = allow_smem(kern, attr_done);
     if (rc) return rc;
     kern<<<grid, 32 * (a.wmax + 1), smem_bytes, st>>>(a, maps);
@@ -187,31 +189,31 @@ static int launch_fwd_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, 
 }
 
 // Selects the instantiation for the runtime flags (data path, softplus, gate).
-template <typename TIn, int NP, bool AGG, bool TM>
+template <typename TIn, int NP, bool AGG, bool TM, int LPC>
 static int launch_fwd(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, bool tma, bool sp,
                       bool gate, cudaStream_t st) {
     if constexpr (AGG) {  // the aggregate pass reads no z
-        if (tma) return sp ? launch_fwd_one<TIn, NP, true, true, true, false, TM>(a, maps, grid, smem_bytes, st)
-                           : launch_fwd_one<TIn, NP, true, true, false, false, TM>(a, maps, grid, smem_bytes, st);
-        return sp ? launch_fwd_one<TIn, NP, false, true, true, false, TM>(a, maps, grid, smem_bytes, st)
-                  : launch_fwd_one<TIn, NP, false, true, false, false, TM>(a, maps, grid, smem_bytes, st);
+        if (tma) return sp ? launch_fwd_one<TIn, NP, true, true, true, false, TM, LPC>(a, maps, grid, smem_bytes, st)
+                           : launch_fwd_one<TIn, NP, true, true, false, false, TM, LPC>(a, maps, grid, smem_bytes, st);
+        return sp ? launch_fwd_one<TIn, NP, false, true, true, false, TM, LPC>(a, maps, grid, smem_bytes, st)
+                  : launch_fwd_one<TIn, NP, false, true, false, false, TM, LPC>(a, maps, grid, smem_bytes, st);
     } else {
         if (tma) {
-            if (sp) return gate ? launch_fwd_one<TIn, NP, true, false, true, true, TM>(a, maps, grid, smem_bytes, st)
-                                : launch_fwd_one<TIn, NP, true, false, true, false, TM>(a, maps, grid, smem_bytes, st);
-            return gate ? launch_fwd_one<TIn, NP, true, false, false, true, TM>(a, maps, grid, smem_bytes, st)
-                        : launch_fwd_one<TIn, NP, true, false, false, false, TM>(a, maps, grid, smem_bytes, st);
+            if (sp) return gate ? launch_fwd_one<TIn, NP, true, false, true, true, TM, LPC>(a, maps, grid, smem_bytes, st)
+                                : launch_fwd_one<TIn, NP, true, false, true, false, TM, LPC>(a, maps, grid, smem_bytes, st);
+            return gate ? launch_fwd_one<TIn, NP, true, false, false, true, TM, LPC>(a, maps, grid, smem_bytes, st)
+                        : launch_fwd_one<TIn, NP, true, false, false, false, TM, LPC>(a, maps, grid, smem_bytes, st);
         }
-        if (sp) return gate ? launch_fwd_one<TIn, NP, false, false, true, true, TM>(a, maps, grid, smem_bytes, st)
-                            : launch_fwd_one<TIn, NP, false, false, true, false, TM>(a, maps, grid, smem_bytes, st);
-        return gate ? launch_fwd_one<TIn, NP, false, false, false, true, TM>(a, maps, grid, smem_bytes, st)
-                    : launch_fwd_one<TIn, NP, false, false, false, false, TM>(a, maps, grid, smem_bytes, st);
+        if (sp) return gate ? launch_fwd_one<TIn, NP, false, false, true, true, TM, LPC>(a, maps, grid, smem_bytes, st)
+                            : launch_fwd_one<TIn, NP, false, false, true, false, TM, LPC>(a, maps, grid, smem_bytes, st);
+        return gate ? launch_fwd_one<TIn, NP, false, false, false, true, TM, LPC>(a, maps, grid, smem_bytes, st)
+                    : launch_fwd_one<TIn, NP, false, false, false, false, TM, LPC>(a, maps, grid, smem_bytes, st);
     }
 }
 
 // `scratch`/`scratch_cap`: when scratch is non-NULL the segment carries live there (no allocation);
 // otherwise they come from cudaMallocAsync on `st`.
-template <typename TIn, int NP, bool TM>
+template <typename TIn, int NP, bool TM, int LPC>
 static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gate, float2* scratch,
                    size_t scratch_cap, cudaStream_t st) {
     constexpr int TC = Chunk<TIn>::TC;
@@ -223,7 +225,7 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
 
     FwdPlan p;
-    int rc = plan_fwd<TIn, NP, TM>(s, nsm, p);
+    int rc = plan_fwd<TIn, NP, TM, LPC>(s, nsm, p);
     if (rc) return rc;
 
     const bool tma_ok = encode_fn() != nullptr && (L * esize) % 16 == 0 && aligned16(a.u) && aligned16(a.delta) &&
@@ -238,7 +240,8 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
         bool ok = true;
         for (int m = 0; m < 3 && ok; ++m)
             for (int w = 0; w < 2 && ok; ++w) {
-                const int rowsbox = kUnitCh * (w == 0 ? (p.wlo > 0 ? p.wlo : 1) : p.wlo + 1);
+                constexpr int CPW = TM ? kUnitCh : Layout<LPC>::CPW;
+                const int rowsbox = CPW * (w == 0 ? (p.wlo > 0 ? p.wlo : 1) : p.wlo + 1);
                 ok = encode_3d(&dst[m][w], src[m], esize, L, s->dim, s->batch, TC, rowsbox > 256 ? 256 : rowsbox);
             }
         ok = ok && encode_3d(&maps.B, a.B, esize, L, s->dstate, s->batch, TC, s->dstate) &&
@@ -290,11 +293,11 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
             }
         }
         const unsigned g1 = (unsigned)((long long)s->batch * (p.nseg - 1) * p.kcta);
-        rc = launch_fwd<TIn, NP, true, TM>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
+        rc = launch_fwd<TIn, NP, true, TM, LPC>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
     }
     if (rc == MAMBA_OK) {
         const unsigned g2 = (unsigned)((long long)s->batch * p.nseg * p.kcta);
-        rc = launch_fwd<TIn, NP, false, TM>(a, maps, g2, p.smem_bytes, tma_ok, softplus, gate, st);
+        rc = launch_fwd<TIn, NP, false, TM, LPC>(a, maps, g2, p.smem_bytes, tma_ok, softplus, gate, st);
     }
     if (owned) {
         cudaError_t e = cudaFreeAsync(a.agg, st);
@@ -308,9 +311,14 @@ static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, bool softpl
                         size_t scratch_cap, cudaStream_t st) {
     // N <= 16 with MAMBA_SCAN_TMEM=1: the variant that feeds B/C through tensor memory (not the
     // default: slower on the measured workloads)
-    if constexpr (NP == 16)
-        if (getenv("MAMBA_SCAN_TMEM") != nullptr) return fwd_run<TIn, NP, true>(s, a, softplus, gate, scratch, scratch_cap, st);
-    return fwd_run<TIn, NP, false>(s, a, softplus, gate, scratch, scratch_cap, st);
+    if constexpr (NP == 16) {
+        if (getenv("MAMBA_SCAN_TMEM") != nullptr)
+            return fwd_run<TIn, NP, true, 4>(s, a, softplus, gate, scratch, scratch_cap, st);
+        // lanes per channel: 2 (8 states per lane, 16 channels per warp) or 4
+        if (env_int("MAMBA_SCAN_LPC", 4) == 2)
+            return fwd_run<TIn, NP, false, 2>(s, a, softplus, gate, scratch, scratch_cap, st);
+    }
+    return fwd_run<TIn, NP, false, 4>(s, a, softplus, gate, scratch, scratch_cap, st);
 }
 
 // ---------------------------------------------------------------------------- checks

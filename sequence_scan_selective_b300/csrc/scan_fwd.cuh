@@ -53,6 +53,17 @@ constexpr int kYPitch = kSlot * 4 + 16;      // bytes per (lane group, channel) 
 constexpr int kQBuf = kUnitCh * kQPitch;       // one buffer of Delta pairs (8 channels)
 constexpr int kWarpScratch = 2 * kQBuf + kLanesPerCh * kUnitCh * kYPitch;  // 4864 bytes
 constexpr int kMaxConsumerWarps = 15;
+
+// Lane layout of scan_fwd_kernel: LPC lanes share one channel's states (LPC = 4: 8 channels per
+// warp, G = N/4 states per lane; LPC = 2: 16 channels per warp, G = N/2 states per lane).
+template <int LPC>
+struct Layout {
+    static constexpr int CPW = 32 / LPC;                  // channels per warp (work unit)
+    static constexpr int OWN = kSlot / LPC;               // steps of per-element work per lane per slot
+    static constexpr int UNIT_BYTES = CPW * 128;          // one unit's u/delta/z tile per chunk
+    static constexpr int QBUF = CPW * kQPitch;            // one buffer of Delta pairs
+    static constexpr int SCRATCH = 2 * QBUF + 32 * kYPitch;  // per-warp scratch bytes
+};
 constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
 
 struct FwdArgs {
@@ -72,7 +83,7 @@ struct FwdArgs {
     long long L;
     long long seg_len;  // multiple of the chunk length
     int nseg;
-    int upr;     // work units per batch row = ceil(dim / 8)
+    int upr;     // work units per batch row = ceil(dim / channels per unit)
     int kcta;    // CTAs per (segment, batch row)
     int wmax;    // consumer warps per CTA; warp wmax is the producer
     int wlo;     // CTAs with this many units use the narrow u/delta/z maps (index 0)
@@ -80,7 +91,7 @@ struct FwdArgs {
     int stage_bytes, bc_off, quad_off, scratch_off, src_off, bar_off;
 };
 
-// u, delta, z maps: [0] box of 8*wlo rows, [1] box of 8*(wlo+1) rows; B, C: box [N, TC].
+// u, delta, z maps: [0] box of wlo units' rows, [1] of (wlo+1) units' rows; B, C: box [N, TC].
 struct FwdMaps {
     CUtensorMap u[2], d[2], z[2], B, C;
 };
@@ -119,10 +130,14 @@ __device__ __forceinline__ void store4<uint16_t>(uint16_t* p, const float* v) {
     *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
 }
 
-template <typename TIn, int NP, bool TMA, bool AGG, bool SOFTPLUS, bool GATE>
+template <typename TIn, int NP, int LPC, bool TMA, bool AGG, bool SOFTPLUS, bool GATE>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     scan_fwd_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps) {
-    constexpr int G = NP / kLanesPerCh;  // states per lane
+    using LY = Layout<LPC>;
+    constexpr int CPW = LY::CPW;
+    constexpr int OWN = LY::OWN;
+    constexpr int UB = LY::UNIT_BYTES;
+    constexpr int G = NP / LPC;  // states per lane
     constexpr int NPAIR = NP / 2;
     constexpr int TC = Chunk<TIn>::TC;
     constexpr int SPC = Chunk<TIn>::SPC;
@@ -166,16 +181,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (wid == W) {
         // ================================================================== producer warp
         const int mi = nunits == a.wlo ? 0 : 1;
-        const uint32_t tx = (uint32_t)(nunits * kUnitCh * 128 * (has_z ? 3 : 2) + (AGG ? 1 : 2) * N * 128);
+        const uint32_t tx = (uint32_t)(nunits * UB * (has_z ? 3 : 2) + (AGG ? 1 : 2) * N * 128);
         auto issue = [&](int k) {  // lane 0: TMA loads of chunk k into stage k % NS
             const int s = k % NS;
             unsigned char* st = smem + s * a.stage_bytes;
             const int t0 = (int)(t_begin + (long long)k * TC);
             mbar_arrive_expect_tx(&full[s], tx);
-            const int r0 = u0 * kUnitCh;
+            const int r0 = u0 * CPW;
             tma_load_3d(st, &maps.u[mi], &full[s], t0, r0, b);
-            tma_load_3d(st + W * 1024, &maps.d[mi], &full[s], t0, r0, b);
-            if (has_z) tma_load_3d(st + 2 * W * 1024, &maps.z[mi], &full[s], t0, r0, b);
+            tma_load_3d(st + W * UB, &maps.d[mi], &full[s], t0, r0, b);
+            if (has_z) tma_load_3d(st + 2 * W * UB, &maps.z[mi], &full[s], t0, r0, b);
             tma_load_3d(st + a.bc_off, &maps.B, &full[s], t0, 0, b);
             if (!AGG) tma_load_3d(st + a.bc_off + NP * 128, &maps.C, &full[s], t0, 0, b);
         };
@@ -255,9 +270,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (wid >= nunits) return;
 
     // ====================================================================== consumer warps
-    const int c = lane & 7;
-    const int g = lane >> 3;
-    const int dch = (u0 + wid) * kUnitCh + c;
+    const int c = lane % CPW;  // channel within the unit
+    const int g = lane / CPW;  // state group: states g*G .. g*G+G-1
+    const int dch = (u0 + wid) * CPW + c;
     const bool cvalid = dch < a.dim;
     const long long row = (long long)b * a.dim + (cvalid ? dch : 0);
     const float bias = (cvalid && a.bias != nullptr) ? a.bias[dch] : 0.f;
@@ -287,8 +302,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
 
     // warp scratch: two buffers of Delta pairs (slot parity) and one of partial sums
-    unsigned char* wsq = smem + a.scratch_off + wid * kWarpScratch;
-    unsigned char* wsy = wsq + 2 * kQBuf;
+    unsigned char* wsq = smem + a.scratch_off + wid * LY::SCRATCH;
+    unsigned char* wsy = wsq + 2 * LY::QBUF;
     const int nslots = (int)((t_end - t_begin + kSlot - 1) / kSlot);
     float sumdt = 0.f;
     bool ok = true;
@@ -301,56 +316,60 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         return __all_sync(0xffffffffu, mbar_wait_bounded(&qready[k % NS], (uint32_t)((k / NS) & 1), kWaitLimitNs));
     };
 
-    // Phase A of slot i: Delta, Delta*u of the 4 owned steps -> pairs in wsq[i & 1]; returns
-    // D*u and the gate of the owned steps for phase C.
-    auto phase_a = [&](int i, float2& skip01, float2& skip23, float2& gate01, float2& gate23) {
+    // Phase A of slot i: Delta, Delta*u of the OWN owned steps -> pairs in wsq[i & 1]; returns
+    // D*u and the gate of the owned steps (skip[j], gate[j] cover steps 2j, 2j+1) for phase C.
+    auto phase_a = [&](int i, float2* skip, float2* gate) {
         const int k = i / SPC, sl = i % SPC;
-        const long long to = t_begin + (long long)i * kSlot + g * kOwned;  // first owned step
         const unsigned char* st = smem + (k % NS) * a.stage_bytes;
-        float dv[4], uv[4], zv[4];
-        if (TMA) {
-            const int byte = (sl * kSlot + g * kOwned) * ES;
-            tile_load4<TIn>(st + (W + wid) * 1024, c, byte, dv);
-            tile_load4<TIn>(st + wid * 1024, c, byte, uv);
-            if (has_z) tile_load4<TIn>(st + (2 * W + wid) * 1024, c, byte, zv);
-        } else {
-            const TIn* gd = static_cast<const TIn*>(a.delta) + row * a.L;
-            const TIn* gu = static_cast<const TIn*>(a.u) + row * a.L;
-            const TIn* gz = static_cast<const TIn*>(a.z) + row * a.L;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool in = cvalid && to + j < t_end;
-                dv[j] = in ? In<TIn>::to_f32(gd[to + j]) : 0.f;
-                uv[j] = in ? In<TIn>::to_f32(gu[to + j]) : 0.f;
-                zv[j] = (in && has_z) ? In<TIn>::to_f32(gz[to + j]) : 0.f;
-            }
-        }
-        float2 dt01 = make_float2(dv[0] + bias, dv[1] + bias);
-        float2 dt23 = make_float2(dv[2] + bias, dv[3] + bias);
-        if (SOFTPLUS) {
-            dt01 = softplus2(dt01);
-            dt23 = softplus2(dt23);
-        }
-        if (to + 4 > t_end) {  // steps past the end (or past this segment) leave h unchanged
-            const long long nv = t_end - to;
-            if (nv < 1) dt01.x = 0.f;
-            if (nv < 2) dt01.y = 0.f;
-            if (nv < 3) dt23.x = 0.f;
-            dt23.y = 0.f;
-        }
-        const float2 du01 = fmul2(dt01, make_float2(uv[0], uv[1]));
-        const float2 du23 = fmul2(dt23, make_float2(uv[2], uv[3]));
-        float4* qw = reinterpret_cast<float4*>(wsq + (i & 1) * kQBuf + c * kQPitch);
-        qw[2 * g] = make_float4(dt01.x, du01.x, dt01.y, du01.y);
-        qw[2 * g + 1] = make_float4(dt23.x, du23.x, dt23.y, du23.y);
-        if (!AGG) {
-            skip01 = fmul2(make_float2(Dd, Dd), make_float2(uv[0], uv[1]));
-            skip23 = fmul2(make_float2(Dd, Dd), make_float2(uv[2], uv[3]));
-            if (has_z) {
-                gate01 = silu2(make_float2(zv[0], zv[1]));
-                gate23 = silu2(make_float2(zv[2], zv[3]));
+        for (int j4 = 0; j4 < OWN / 4; ++j4) {
+            const int tl = g * OWN + 4 * j4;                          // first step of this group in the slot
+            const long long to = t_begin + (long long)i * kSlot + tl;
+            float dv[4], uv[4], zv[4];
+            if (TMA) {
+                const int byte = (sl * kSlot + tl) * ES;
+                tile_load4<TIn>(st + (W + wid) * UB, c, byte, dv);
+                tile_load4<TIn>(st + wid * UB, c, byte, uv);
+                if (has_z) tile_load4<TIn>(st + (2 * W + wid) * UB, c, byte, zv);
             } else {
-                gate01 = gate23 = make_float2(1.f, 1.f);
+                const TIn* gd = static_cast<const TIn*>(a.delta) + row * a.L;
+                const TIn* gu = static_cast<const TIn*>(a.u) + row * a.L;
+                const TIn* gz = static_cast<const TIn*>(a.z) + row * a.L;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = cvalid && to + j < t_end;
+                    dv[j] = in ? In<TIn>::to_f32(gd[to + j]) : 0.f;
+                    uv[j] = in ? In<TIn>::to_f32(gu[to + j]) : 0.f;
+                    zv[j] = (in && has_z) ? In<TIn>::to_f32(gz[to + j]) : 0.f;
+                }
+            }
+            float2 dt01 = make_float2(dv[0] + bias, dv[1] + bias);
+            float2 dt23 = make_float2(dv[2] + bias, dv[3] + bias);
+            if (SOFTPLUS) {
+                dt01 = softplus2(dt01);
+                dt23 = softplus2(dt23);
+            }
+            if (to + 4 > t_end) {  // steps past the end (or past this segment) leave h unchanged
+                const long long nv = t_end - to;
+                if (nv < 1) dt01.x = 0.f;
+                if (nv < 2) dt01.y = 0.f;
+                if (nv < 3) dt23.x = 0.f;
+                dt23.y = 0.f;
+            }
+            const float2 du01 = fmul2(dt01, make_float2(uv[0], uv[1]));
+            const float2 du23 = fmul2(dt23, make_float2(uv[2], uv[3]));
+            float4* qw = reinterpret_cast<float4*>(wsq + (i & 1) * LY::QBUF + c * kQPitch);
+            qw[tl / 2] = make_float4(dt01.x, du01.x, dt01.y, du01.y);
+            qw[tl / 2 + 1] = make_float4(dt23.x, du23.x, dt23.y, du23.y);
+            if (!AGG) {
+                skip[2 * j4] = fmul2(make_float2(Dd, Dd), make_float2(uv[0], uv[1]));
+                skip[2 * j4 + 1] = fmul2(make_float2(Dd, Dd), make_float2(uv[2], uv[3]));
+                if (has_z) {
+                    gate[2 * j4] = silu2(make_float2(zv[0], zv[1]));
+                    gate[2 * j4 + 1] = silu2(make_float2(zv[2], zv[3]));
+                } else {
+                    gate[2 * j4] = gate[2 * j4 + 1] = make_float2(1.f, 1.f);
+                }
             }
         }
     };
@@ -359,7 +378,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     // lane's share of C.h at step t.
     auto phase_b = [&](int i, float* yp) {
         const int k = i / SPC, sl = i % SPC;
-        const float4* qrow = reinterpret_cast<const float4*>(wsq + (i & 1) * kQBuf + c * kQPitch);
+        const float4* qrow = reinterpret_cast<const float4*>(wsq + (i & 1) * LY::QBUF + c * kQPitch);
         const float4* bc = reinterpret_cast<const float4*>(smem + (k % NS) * a.stage_bytes + a.quad_off) +
                            sl * kSlot * NPAIR + g * (G / 2);
 #pragma unroll
@@ -382,31 +401,35 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
     };
 
-    // Phase C of slot i: sum the 4 lanes' partials of the owned steps, skip term, gate, store.
-    auto phase_c = [&](int i, float2 skip01, float2 skip23, float2 gate01, float2 gate23) {
-        const long long to = t_begin + (long long)i * kSlot + g * kOwned;
-        float4 acc = *reinterpret_cast<const float4*>(wsy + c * kYPitch + g * 16);
+    // Phase C of slot i: sum the LPC lanes' partials of the owned steps, skip term, gate, store.
+    auto phase_c = [&](int i, const float2* skip, const float2* gate) {
 #pragma unroll
-        for (int gg = 1; gg < kLanesPerCh; ++gg) {
-            const float4 v = *reinterpret_cast<const float4*>(wsy + (gg * kUnitCh + c) * kYPitch + g * 16);
-            const float2 lo = fadd2(make_float2(acc.x, acc.y), make_float2(v.x, v.y));
-            const float2 hi = fadd2(make_float2(acc.z, acc.w), make_float2(v.z, v.w));
-            acc = make_float4(lo.x, lo.y, hi.x, hi.y);
-        }
-        const float2 y01 = fmul2(fadd2(make_float2(acc.x, acc.y), skip01), gate01);
-        const float2 y23 = fmul2(fadd2(make_float2(acc.z, acc.w), skip23), gate23);
-        const float yv[4] = {y01.x, y01.y, y23.x, y23.y};
-        TIn* gy = static_cast<TIn*>(a.y) + row * a.L + to;
-        if (TMA && to + 4 <= t_end) {
-            if (cvalid) store4<TIn>(gy, yv);
-        } else if (cvalid) {
+        for (int j4 = 0; j4 < OWN / 4; ++j4) {
+            const int tl = g * OWN + 4 * j4;
+            const long long to = t_begin + (long long)i * kSlot + tl;
+            float4 acc = *reinterpret_cast<const float4*>(wsy + c * kYPitch + tl * 4);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (to + j < t_end) store_out<TIn>(gy + j, yv[j]);
+            for (int gg = 1; gg < LPC; ++gg) {
+                const float4 v = *reinterpret_cast<const float4*>(wsy + (gg * CPW + c) * kYPitch + tl * 4);
+                const float2 lo = fadd2(make_float2(acc.x, acc.y), make_float2(v.x, v.y));
+                const float2 hi = fadd2(make_float2(acc.z, acc.w), make_float2(v.z, v.w));
+                acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+            }
+            const float2 y01 = fmul2(fadd2(make_float2(acc.x, acc.y), skip[2 * j4]), gate[2 * j4]);
+            const float2 y23 = fmul2(fadd2(make_float2(acc.z, acc.w), skip[2 * j4 + 1]), gate[2 * j4 + 1]);
+            const float yv[4] = {y01.x, y01.y, y23.x, y23.y};
+            TIn* gy = static_cast<TIn*>(a.y) + row * a.L + to;
+            if (TMA && to + 4 <= t_end) {
+                if (cvalid) store4<TIn>(gy, yv);
+            } else if (cvalid) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (to + j < t_end) store_out<TIn>(gy + j, yv[j]);
+            }
         }
     };
 
-    float2 sk01 = make_float2(0.f, 0.f), sk23 = sk01, gt01 = sk01, gt23 = sk01;
+    float2 skip[OWN / 2], gate[OWN / 2];
 #pragma unroll 1
     for (int i = 0; i < nslots && ok; ++i) {
         const int k = i / SPC, sl = i % SPC;
@@ -415,19 +438,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             if (ok) ok = wait_quads(k);
         }
         if (!ok) break;
-        phase_a(i, sk01, sk23, gt01, gt23);
+        phase_a(i, skip, gate);
         __syncwarp();
         float yp[kSlot];
         phase_b(i, yp);
         __syncwarp();
         if (sl == SPC - 1 || i + 1 == nslots) mbar_arrive(&empty[k % NS]);
         if (!AGG) {
-            float4* yw = reinterpret_cast<float4*>(wsy + (g * kUnitCh + c) * kYPitch);
+            float4* yw = reinterpret_cast<float4*>(wsy + (g * CPW + c) * kYPitch);
 #pragma unroll
             for (int j = 0; j < kSlot / 4; ++j) yw[j] = make_float4(yp[4 * j], yp[4 * j + 1], yp[4 * j + 2], yp[4 * j + 3]);
         }
         __syncwarp();
-        if (!AGG) phase_c(i, sk01, sk23, gt01, gt23);
+        if (!AGG) phase_c(i, skip, gate);
         __syncwarp();
     }
     if (!ok) {

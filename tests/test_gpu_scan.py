@@ -77,12 +77,27 @@ def test_state_sizes(ms, N):
     _check_full(ms, cfg)
 
 
-@pytest.mark.parametrize("wmax,stages", [("1", "2"), ("3", "3"), ("15", "4"), ("0", "2")])
+@pytest.mark.parametrize("wmax,stages,lpc", [("1", "2", "4"), ("3", "3", "4"), ("15", "4", "4"), ("0", "2", "4"),
+                                             ("1", "2", "2"), ("4", "3", "2"), ("0", "4", "2")])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_tiling_variants(ms, wmax, stages, dtype):
-    """Consumer warps per CTA (work units per CTA) and ring depth change only the schedule."""
+def test_tiling_variants(ms, wmax, stages, lpc, dtype):
+    """Consumer warps per CTA (work units per CTA), ring depth and lanes per channel (2: 8 states
+    per lane, 16 channels per warp; 4: 4 states per lane, 8 channels per warp) change only the
+    schedule."""
     cfg = synth.CONFIGS["m130"].replace(batch=2, dim=130, seqlen=333, dtype=dtype, seed=21)
-    _check_full(ms, cfg, env={"MAMBA_SCAN_WMAX": wmax, "MAMBA_SCAN_STAGES": stages})
+    _check_full(ms, cfg, env={"MAMBA_SCAN_WMAX": wmax, "MAMBA_SCAN_STAGES": stages, "MAMBA_SCAN_LPC": lpc})
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", ["split", "ragged_n"])
+def test_two_lanes_per_channel(ms, dtype, case):
+    if case == "split":
+        cfg = synth.CONFIGS["long"].replace(batch=1, dim=40, seqlen=6000, dtype=dtype, seed=23)
+        env = {"MAMBA_SCAN_LPC": "2", "MAMBA_SCAN_NSEG": "3"}
+    else:
+        cfg = synth.CONFIGS["m130"].replace(batch=3, dim=37, dstate=11, seqlen=301, dtype=dtype, seed=24)
+        env = {"MAMBA_SCAN_LPC": "2"}
+    _check_full(ms, cfg, env=env)
 
 
 @pytest.mark.parametrize("drop", [("z",), ("D",), ("delta_bias",), ("z", "D", "delta_bias")])

@@ -6,10 +6,13 @@ package.  The product package never imports it, and it imports nothing from the 
 The arithmetic lives in ``oracle.c`` (plain C, double precision, sequential in time); this module
 only compiles it with gcc on first use and marshals numpy arrays into it.
 
-Parity status: every function here is pinned by the ``-m "not gpu"`` tests in
-``tests/test_oracle_pins.py`` (LTI convolution by brute force, the scalar-state closed form, the
-one-step formula, the Delta -> 0 and Delta -> infinity limits, linearity in the input, and the
-decode step against the scan).
+Parity status: every function here is pinned by the ``-m "not gpu"`` tests.
+``tests/test_oracle_pins.py`` pins the forward scan and the decode step (LTI convolution by brute
+force, the scalar-state closed form, the one-step formula, the Delta -> 0 and Delta -> infinity
+limits, linearity in the input, the decode step against the scan).
+``tests/test_oracle_grad_pins.py`` pins the exact zero-order hold (against a numerical solution of
+the held-input ODE by scipy) and the gradients (against Richardson-extrapolated central
+differences of the forward, input by input).
 """
 from __future__ import annotations
 
@@ -31,6 +34,23 @@ F32, BF16 = 0, 1
 _DT = {"f32": F32, "bf16": BF16}
 
 
+_P, _I, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
+SIGNATURES = {
+    "oracle_version": [],
+    "oracle_scan_rows": [_LL, _P, _P, _I, _I, _LL, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P,
+                         _P, _I],
+    "oracle_scan_rows_ex": [_LL, _P, _P, _I, _I, _LL, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _P,
+                            _P, _P, _I],
+    "oracle_state_step_rows": [_LL, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P,
+                               _I],
+    "oracle_state_step_rows_ex": [_LL, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I,
+                                  _P, _I],
+    "oracle_scan_bwd_rows": [_LL, _P, _P, _I, _I, _I, _LL, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I,
+                             _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I],
+}
+DISC = {"euler": 0, "zoh": 1}
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so (gcc, -O2, OpenMP, strict IEEE double arithmetic)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
@@ -48,11 +68,9 @@ def lib() -> ctypes.CDLL:
             build()
             L = ctypes.CDLL(_LIB)
             P, I, LL, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_double
-            L.oracle_scan_rows.restype = I
-            L.oracle_scan_rows.argtypes = [LL, P, P, I, I, LL, I, P, P, P, P, P, P, P, P, I, P, P, P, I]
-            L.oracle_state_step_rows.restype = I
-            L.oracle_state_step_rows.argtypes = [LL, P, P, I, I, I, P, P, P, P, P, P, P, P, P, I, P, I]
-            L.oracle_version.restype = I
+            for name, argtypes in SIGNATURES.items():
+                getattr(L, name).restype = I
+                getattr(L, name).argtypes = argtypes
             _lib = L
     return _lib
 
@@ -70,9 +88,10 @@ def _storage(a, dt):
 
 
 def scan_rows(rows, dim, u_rows, delta_rows, z_rows, A, D, delta_bias, B, C, softplus=True,
-              dtype="f32", h0_rows=None, nthreads=0):
+              dtype="f32", h0_rows=None, nthreads=0, disc="euler"):
     """Scan for the channels ``rows`` (flat b*dim + d).  u/delta/z_rows [nrows, L] in storage
-    dtype; B, C [batch, N, L].  Returns (y [nrows, L], state [nrows, N]) in float64."""
+    dtype; B, C [batch, N, L].  ``disc`` is "euler" (Bbar = Delta B) or "zoh" (exact zero-order
+    hold).  Returns (y [nrows, L], state [nrows, N]) in float64."""
     dt = _DT[dtype]
     rows = np.asarray(rows, dtype=np.int64)
     nrows = len(rows)
@@ -87,17 +106,23 @@ def scan_rows(rows, dim, u_rows, delta_rows, z_rows, A, D, delta_bias, B, C, sof
     h0 = _c(h0_rows, np.float64)
     y = np.empty((nrows, L), dtype=np.float64)
     st = np.empty((nrows, N), dtype=np.float64)
-    rc = lib().oracle_scan_rows(nrows, _ptr(rb), _ptr(rd), dim, N, L, dt, _ptr(u_rows),
-                                _ptr(delta_rows), _ptr(z_rows), _ptr(A), _ptr(D), _ptr(delta_bias),
-                                _ptr(B), _ptr(C), int(bool(softplus)), _ptr(h0), _ptr(y), _ptr(st),
-                                int(nthreads))
+    if disc == "euler":  # the plain entry point, so a planted mistake in it is seen by every pin
+        rc = lib().oracle_scan_rows(nrows, _ptr(rb), _ptr(rd), dim, N, L, dt, _ptr(u_rows),
+                                    _ptr(delta_rows), _ptr(z_rows), _ptr(A), _ptr(D),
+                                    _ptr(delta_bias), _ptr(B), _ptr(C), int(bool(softplus)),
+                                    _ptr(h0), _ptr(y), _ptr(st), int(nthreads))
+    else:
+        rc = lib().oracle_scan_rows_ex(nrows, _ptr(rb), _ptr(rd), dim, N, L, dt, _ptr(u_rows),
+                                       _ptr(delta_rows), _ptr(z_rows), _ptr(A), _ptr(D),
+                                       _ptr(delta_bias), _ptr(B), _ptr(C), int(bool(softplus)),
+                                       DISC[disc], _ptr(h0), _ptr(y), _ptr(st), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_scan_rows rejected its arguments (rc={rc})")
     return y, st
 
 
 def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, dtype="f32", h0=None,
-         nthreads=0):
+         nthreads=0, disc="euler"):
     """Full scan.  u, delta, z [batch, dim, L]; returns y [batch, dim, L], last_state [batch, dim, N]
     (float64)."""
     bsz, dim, L = np.asarray(u).shape
@@ -106,12 +131,12 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, dtyp
     r = lambda x: None if x is None else np.asarray(x).reshape(bsz * dim, L)
     y, st = scan_rows(rows, dim, r(u), r(delta), r(z), A, D, delta_bias, B, C, softplus, dtype,
                       None if h0 is None else np.asarray(h0, dtype=np.float64).reshape(bsz * dim, N),
-                      nthreads)
+                      nthreads, disc)
     return y.reshape(bsz, dim, L), st.reshape(bsz, dim, N)
 
 
 def state_step_rows(rows, dim, state_rows, x_rows, delta_rows, z_rows, A, D, delta_bias, B, C,
-                    softplus=True, dtype="f32", nthreads=0):
+                    softplus=True, dtype="f32", nthreads=0, disc="euler"):
     """One decode step for channels ``rows``.  state_rows [nrows, N] float64 is updated IN PLACE;
     x/delta/z_rows [nrows]; B, C [batch, N].  Returns y [nrows] float64."""
     dt = _DT[dtype]
@@ -128,17 +153,24 @@ def state_step_rows(rows, dim, state_rows, x_rows, delta_rows, z_rows, A, D, del
     B, C = _storage(B, dt), _storage(C, dt)
     D, delta_bias = _c(D, np.float32), _c(delta_bias, np.float32)
     y = np.empty(nrows, dtype=np.float64)
-    rc = lib().oracle_state_step_rows(nrows, _ptr(rb), _ptr(rd), dim, N, dt, _ptr(state_rows),
-                                      _ptr(x_rows), _ptr(delta_rows), _ptr(z_rows), _ptr(A), _ptr(D),
-                                      _ptr(delta_bias), _ptr(B), _ptr(C), int(bool(softplus)),
-                                      _ptr(y), int(nthreads))
+    if disc == "euler":
+        rc = lib().oracle_state_step_rows(nrows, _ptr(rb), _ptr(rd), dim, N, dt, _ptr(state_rows),
+                                          _ptr(x_rows), _ptr(delta_rows), _ptr(z_rows), _ptr(A),
+                                          _ptr(D), _ptr(delta_bias), _ptr(B), _ptr(C),
+                                          int(bool(softplus)), _ptr(y), int(nthreads))
+    else:
+        rc = lib().oracle_state_step_rows_ex(nrows, _ptr(rb), _ptr(rd), dim, N, dt,
+                                             _ptr(state_rows), _ptr(x_rows), _ptr(delta_rows),
+                                             _ptr(z_rows), _ptr(A), _ptr(D), _ptr(delta_bias),
+                                             _ptr(B), _ptr(C), int(bool(softplus)), DISC[disc],
+                                             _ptr(y), int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_state_step_rows rejected its arguments (rc={rc})")
     return y
 
 
 def state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
-               dtype="f32", nthreads=0):
+               dtype="f32", nthreads=0, disc="euler"):
     """Full decode step.  state [batch, dim, N] float64 updated in place; x/delta/z [batch, dim];
     B, C [batch, N].  Returns y [batch, dim] float64."""
     bsz, dim, N = state.shape
@@ -146,5 +178,59 @@ def state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softpl
     st = state.reshape(bsz * dim, N)
     r = lambda a: None if a is None else np.asarray(a).reshape(bsz * dim)
     y = state_step_rows(rows, dim, st, r(x), r(delta), r(z), A, D, delta_bias, B, C, softplus,
-                        dtype, nthreads)
+                        dtype, nthreads, disc)
     return y.reshape(bsz, dim)
+
+
+def scan_bwd_rows(rows, batch, dim, u_rows, delta_rows, z_rows, A, D, delta_bias, B, C, dy_rows,
+                  softplus=True, dtype="f32", h0_rows=None, dstate_rows=None, disc="euler",
+                  nthreads=0):
+    """Gradients of the scan for the channels ``rows``: the loss is sum(dy * y) +
+    sum(dstate * last_state) over those channels.  Returns a dict of float64 arrays: per channel
+    du, ddelta, dz (None without z), dh0 [nrows, N]; summed over the given channels dA [dim, N],
+    dD [dim], ddelta_bias [dim], dB, dC [batch, N, L]."""
+    dt = _DT[dtype]
+    rows = np.asarray(rows, dtype=np.int64)
+    nrows = len(rows)
+    A = _c(A, np.float32)
+    N = A.shape[1]
+    L = np.asarray(u_rows).shape[-1]
+    rb = np.ascontiguousarray(rows // dim, dtype=np.int32)
+    rd = np.ascontiguousarray(rows % dim, dtype=np.int32)
+    has_z = z_rows is not None
+    u_rows, delta_rows, z_rows = (_storage(x, dt) for x in (u_rows, delta_rows, z_rows))
+    B, C = _storage(B, dt), _storage(C, dt)
+    D, delta_bias = _c(D, np.float32), _c(delta_bias, np.float32)
+    h0, dyr, dst = _c(h0_rows, np.float64), _c(dy_rows, np.float64), _c(dstate_rows, np.float64)
+    out = {"du": np.empty((nrows, L)), "ddelta": np.empty((nrows, L)),
+           "dz": np.empty((nrows, L)) if has_z else None, "dh0": np.empty((nrows, N)),
+           "dA": np.zeros((A.shape[0], N)), "dD": np.zeros(A.shape[0]),
+           "ddelta_bias": np.zeros(A.shape[0]), "dB": np.zeros((batch, N, L)),
+           "dC": np.zeros((batch, N, L))}
+    rc = lib().oracle_scan_bwd_rows(
+        nrows, _ptr(rb), _ptr(rd), batch, dim, N, L, dt, _ptr(u_rows), _ptr(delta_rows),
+        _ptr(z_rows), _ptr(A), _ptr(D), _ptr(delta_bias), _ptr(B), _ptr(C), int(bool(softplus)),
+        DISC[disc], _ptr(h0), _ptr(dyr), _ptr(dst), _ptr(out["du"]), _ptr(out["ddelta"]),
+        _ptr(out["dz"]), _ptr(out["dh0"]), _ptr(out["dA"]), _ptr(out["dD"]),
+        _ptr(out["ddelta_bias"]), _ptr(out["dB"]), _ptr(out["dC"]), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_scan_bwd_rows rejected its arguments (rc={rc})")
+    return out
+
+
+def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True, dtype="f32",
+             h0=None, dlast_state=None, disc="euler", nthreads=0):
+    """Gradients of the full scan.  u, delta, z, dy [batch, dim, L]; dlast_state [batch, dim, N]
+    (None = 0).  Returns a dict: du, ddelta, dz [batch, dim, L], dh0 [batch, dim, N], dA [dim, N],
+    dD, ddelta_bias [dim], dB, dC [batch, N, L] (float64)."""
+    bsz, dim, L = np.asarray(u).shape
+    N = np.asarray(A).shape[1]
+    r = lambda x, w: None if x is None else np.asarray(x).reshape(bsz * dim, w)
+    out = scan_bwd_rows(np.arange(bsz * dim), bsz, dim, r(u, L), r(delta, L), r(z, L), A, D,
+                        delta_bias, B, C, r(np.asarray(dy, np.float64), L), softplus, dtype,
+                        r(h0, N), r(dlast_state, N), disc, nthreads)
+    for k in ("du", "ddelta", "dz"):
+        if out[k] is not None:
+            out[k] = out[k].reshape(bsz, dim, L)
+    out["dh0"] = out["dh0"].reshape(bsz, dim, N)
+    return out

@@ -1,0 +1,199 @@
+"""Pins of the oracle's exact zero-order hold and of its gradients.
+
+Neither check re-types the oracle's arithmetic:
+
+* zero-order hold (visual guide to Mamba and SSMs, section 2.3: the input is held over each step of
+  length Delta): the held-input ODE h' = A h + B x is integrated numerically over every step by
+  scipy's DOP853 at tight tolerances and compared with the oracle's closed-form update;
+* gradients (same guide, section 3.4: the backward pass recomputes the states): every gradient of
+  ``oracle.scan_bwd`` is compared, input element by input element, with a Richardson-extrapolated
+  central difference of the forward oracle.  The base point is dyadic (multiples of 2^-8) and the
+  steps are 2^-10 and 2^-11, so every perturbed input is exact in fp32 and the difference quotient
+  sees exactly the step it divides by.
+"""
+import numpy as np
+import pytest
+from scipy.integrate import solve_ivp
+from scipy.special import expit
+
+import oracle
+
+FD_RTOL = 1e-8
+
+
+def _rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+
+
+def _dyadic(rng, shape, lo, hi):
+    return (np.round(rng.uniform(lo, hi, size=shape) * 256.0) / 256.0).astype(np.float32)
+
+
+def _case(seed, bsz=2, dim=3, N=3, L=7, softplus=True, gate=True, skip=True, bias=True, h0=True,
+          dstate=True, zero_A=False):
+    rng = np.random.default_rng(seed)
+    A = _dyadic(rng, (dim, N), -2.0, -0.25)
+    if zero_A:
+        A[0, 1] = 0.0
+    c = dict(
+        u=_dyadic(rng, (bsz, dim, L), -2, 2),
+        delta=_dyadic(rng, (bsz, dim, L), -2.0, 0.5) if softplus else _dyadic(rng, (bsz, dim, L), 0.05, 0.6),
+        A=A, B=_dyadic(rng, (bsz, N, L), -2, 2), C=_dyadic(rng, (bsz, N, L), -2, 2),
+        D=_dyadic(rng, dim, 0.5, 1.5) if skip else None,
+        z=_dyadic(rng, (bsz, dim, L), -2, 2) if gate else None,
+        delta_bias=_dyadic(rng, dim, -0.25, 0.25) if bias else None,
+        h0=rng.normal(size=(bsz, dim, N)) if h0 else None)
+    dy = rng.normal(size=(bsz, dim, L))
+    ds = rng.normal(size=(bsz, dim, N)) if dstate else None
+    return c, dy, ds, softplus
+
+
+def _loss(c, dy, ds, softplus, disc):
+    y, st = oracle.scan(c["u"], c["delta"], c["A"], c["B"], c["C"], c["D"], c["z"], c["delta_bias"],
+                        softplus, "f32", h0=c["h0"], disc=disc)
+    out = float(np.sum(dy * y))
+    if ds is not None:
+        out += float(np.sum(ds * st))
+    return out
+
+
+def _fd(c, dy, ds, softplus, disc, name):
+    """Richardson-extrapolated central differences of the loss with respect to c[name]."""
+    base = c[name]
+    g = np.zeros(base.shape, np.float64)
+    for idx in np.ndindex(base.shape):
+        quot = []
+        for eps in (2.0 ** -10, 2.0 ** -11):
+            vals = []
+            for sgn in (1.0, -1.0):
+                p = base.copy()
+                p[idx] = p[idx] + sgn * eps
+                assert float(p[idx]) == float(base[idx]) + sgn * eps  # exact perturbation
+                vals.append(_loss({**c, name: p}, dy, ds, softplus, disc))
+            quot.append((vals[0] - vals[1]) / (2.0 * eps))
+        g[idx] = (4.0 * quot[1] - quot[0]) / 3.0
+    return g
+
+
+CONFIGS = {
+    "all_inputs": dict(),
+    "bare": dict(softplus=False, gate=False, skip=False, bias=False, h0=False, dstate=False),
+    "no_gate_with_state": dict(gate=False, h0=False),
+    "no_softplus_gate": dict(softplus=False, skip=False),
+}
+
+
+@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("cfg", sorted(CONFIGS))
+def test_gradients_match_finite_differences(cfg, disc):
+    c, dy, ds, softplus = _case(11 + len(cfg), **CONFIGS[cfg])
+    g = oracle.scan_bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], dy, c["D"], c["z"],
+                        c["delta_bias"], softplus, "f32", h0=c["h0"], dlast_state=ds, disc=disc)
+    pairs = [("u", "du"), ("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC")]
+    pairs += [(k, gk) for k, gk in (("z", "dz"), ("D", "dD"), ("delta_bias", "ddelta_bias"),
+                                    ("h0", "dh0")) if c[k] is not None]
+    for name, gname in pairs:
+        want = _fd(c, dy, ds, softplus, disc, name)
+        assert _rel(g[gname], want) < FD_RTOL, (cfg, disc, gname, _rel(g[gname], want))
+
+
+def test_zoh_gradients_at_zero_A():
+    """A = 0 in one state: the hold factor is Delta there and its A-derivative Delta^2 / 2."""
+    c, dy, ds, softplus = _case(5, zero_A=True)
+    g = oracle.scan_bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], dy, c["D"], c["z"],
+                        c["delta_bias"], softplus, "f32", h0=c["h0"], dlast_state=ds, disc="zoh")
+    for name, gname in (("A", "dA"), ("delta", "ddelta"), ("u", "du")):
+        want = _fd(c, dy, ds, softplus, "zoh", name)
+        assert _rel(g[gname], want) < FD_RTOL, (gname, _rel(g[gname], want))
+
+
+def test_gradient_rows_sum_to_full():
+    """Gradients for a subset of channels: per-channel outputs equal the full run's rows, and the
+    shared gradients (dB, dC) add up over a partition of the channels."""
+    c, dy, ds, softplus = _case(3, bsz=2, dim=4, N=3, L=9)
+    full = oracle.scan_bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], dy, c["D"], c["z"],
+                           c["delta_bias"], softplus, "f32", h0=c["h0"], dlast_state=ds)
+    bsz, dim, L = c["u"].shape
+    N = c["A"].shape[1]
+    r = lambda x, w: x.reshape(bsz * dim, w)
+    parts = [np.array([0, 3, 5]), np.array([1, 2, 4, 6, 7])]
+    acc_dB = np.zeros_like(full["dB"])
+    for rows in parts:
+        p = oracle.scan_bwd_rows(rows, bsz, dim, r(c["u"], L)[rows], r(c["delta"], L)[rows],
+                                 r(c["z"], L)[rows], c["A"], c["D"], c["delta_bias"], c["B"],
+                                 c["C"], r(dy, L)[rows], softplus, "f32",
+                                 r(c["h0"], N)[rows], r(ds, N)[rows])
+        np.testing.assert_array_equal(p["du"], r(full["du"], L)[rows])
+        np.testing.assert_array_equal(p["dh0"], r(full["dh0"], N)[rows])
+        acc_dB += p["dB"]
+    assert _rel(acc_dB, full["dB"]) < 1e-14
+
+
+def _ode_scan(c, softplus):
+    """The held-input ODE h' = a h + B_t x_t, solved numerically over each step [0, Delta_t]."""
+    bsz, dim, L = c["u"].shape
+    N = c["A"].shape[1]
+    y = np.zeros((bsz, dim, L))
+    for b in range(bsz):
+        for d in range(dim):
+            a = c["A"][d].astype(np.float64)
+            h = np.zeros(N)
+            for t in range(L):
+                x = float(c["u"][b, d, t])
+                s = float(c["delta"][b, d, t]) + float(c["delta_bias"][d])
+                dt = np.logaddexp(0.0, s) if softplus else s
+                Bt = c["B"][b, :, t].astype(np.float64)
+                sol = solve_ivp(lambda _t, hh: a * hh + Bt * x, (0.0, dt), h, method="DOP853",
+                                rtol=1e-13, atol=1e-15)
+                h = sol.y[:, -1]
+                zz = float(c["z"][b, d, t])
+                y[b, d, t] = (float(c["C"][b, :, t] @ h) + float(c["D"][d]) * x) * zz * expit(zz)
+    return y
+
+
+def test_zoh_matches_numerical_ode():
+    c, _, _, softplus = _case(21, bsz=1, dim=2, N=3, L=6, h0=False)
+    y, _ = oracle.scan(c["u"], c["delta"], c["A"], c["B"], c["C"], c["D"], c["z"], c["delta_bias"],
+                       softplus, "f32", disc="zoh")
+    assert _rel(y, _ode_scan(c, softplus)) < 1e-9
+
+
+def test_zoh_and_euler_differ_at_second_order():
+    """The simplified Bbar = Delta B agrees with the hold to first order in Delta: halving every
+    step size quarters the gap in the first state update."""
+    c, _, _, _ = _case(8, bsz=1, dim=2, N=3, L=1, softplus=False, gate=False, h0=False)
+    gaps = []
+    for scale in (1.0, 0.5, 0.25):
+        cc = {**c, "delta": (c["delta"] * np.float32(scale)).astype(np.float32)}
+        ye, _ = oracle.scan(cc["u"], cc["delta"], cc["A"], cc["B"], cc["C"], None, None, None,
+                            False, "f32", disc="euler")
+        yz, _ = oracle.scan(cc["u"], cc["delta"], cc["A"], cc["B"], cc["C"], None, None, None,
+                            False, "f32", disc="zoh")
+        gaps.append(np.max(np.abs(ye - yz)))
+    assert 3.6 < gaps[0] / gaps[1] < 4.4 and 3.8 < gaps[1] / gaps[2] < 4.2, gaps
+
+
+def test_zoh_equals_euler_where_A_is_zero():
+    c, _, _, softplus = _case(9, zero_A=True)
+    c["A"][:] = 0.0
+    ye, se = oracle.scan(c["u"], c["delta"], c["A"], c["B"], c["C"], c["D"], c["z"],
+                         c["delta_bias"], softplus, "f32", h0=c["h0"])
+    yz, sz = oracle.scan(c["u"], c["delta"], c["A"], c["B"], c["C"], c["D"], c["z"],
+                         c["delta_bias"], softplus, "f32", h0=c["h0"], disc="zoh")
+    np.testing.assert_array_equal(ye, yz)
+    np.testing.assert_array_equal(se, sz)
+
+
+def test_zoh_decode_steps_equal_scan():
+    c, _, _, softplus = _case(4, L=5)
+    y, st = oracle.scan(c["u"], c["delta"], c["A"], c["B"], c["C"], c["D"], c["z"], c["delta_bias"],
+                        softplus, "f32", h0=c["h0"], disc="zoh")
+    state = np.array(c["h0"], np.float64, order="C")
+    for t in range(c["u"].shape[2]):
+        yt = oracle.state_step(state, c["u"][:, :, t], c["delta"][:, :, t], c["A"],
+                               np.ascontiguousarray(c["B"][:, :, t]),
+                               np.ascontiguousarray(c["C"][:, :, t]), c["D"], c["z"][:, :, t],
+                               c["delta_bias"], softplus, "f32", disc="zoh")
+        assert _rel(yt, y[:, :, t]) < 1e-13
+    assert _rel(state, st) < 1e-13

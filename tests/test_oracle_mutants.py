@@ -2,8 +2,9 @@
 
 Each mutant is a one-line textual change of ``oracle/oracle.c`` (a dropped term, a wrong sign or
 index, a transposed operand, a misplaced bias), compiled to a temporary library that replaces the
-oracle's for the duration of one check.  A mutant passes the check only if at least one pin in
-``test_oracle_pins.py`` fails on it.
+oracle's for the duration of one check.  A mutant passes the check only if at least one pin fails
+on it: a pin of ``test_oracle_pins.py`` for the forward scan and the decode step, a pin of
+``test_oracle_grad_pins.py`` for the exact zero-order hold and the gradients.
 """
 import ctypes
 import os
@@ -13,6 +14,7 @@ import tempfile
 import pytest
 
 import oracle
+import test_oracle_grad_pins as gpins
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -22,7 +24,7 @@ MUTANTS = {
     "skip_term_dropped": ("double y = acc + Dd * x;", "double y = acc;"),
     "A_sign_flipped": ("const double Abar = exp(dt * a_n[n]);", "const double Abar = exp(-dt * a_n[n]);"),
     "euler_A": ("const double Abar = exp(dt * a_n[n]);", "const double Abar = 1.0 + dt * a_n[n];"),
-    "Bbar_missing_delta": ("const double Bbar_x = dt * widen(B, bc, in_dtype) * x;",
+    "Bbar_missing_delta": ("const double Bbar_x = bbar_factor(dt, a_n[n], zoh) * widen(B, bc, in_dtype) * x;",
                            "const double Bbar_x = widen(B, bc, in_dtype) * x;"),
     "BC_transposed": ("const long long bc = ((long long)b * dstate + n) * seqlen + t;",
                       "const long long bc = ((long long)b * seqlen + t) * dstate + n;"),
@@ -36,10 +38,41 @@ MUTANTS = {
     "gate_is_sigmoid": ("return z / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(-z));"),
     "softplus_overflows": ("if (x > 0.0) return x + log1p(exp(-x));", "if (x > 1e300) return x;"),
     "step_skip_dropped": ("double y = acc + (D ? (double)D[d] : 0.0) * x;", "double y = acc;"),
-    "step_A_sign": ("const double Abar = exp(dt * (double)A[(long long)d * dstate + n]);",
-                    "const double Abar = exp(-dt * (double)A[(long long)d * dstate + n]);"),
+    "step_A_sign": ("const double Abar = exp(dt * a);", "const double Abar = exp(-dt * a);"),
     "bf16_widen_wrong_shift": ("((const uint16_t*)p)[i]) << 16;", "((const uint16_t*)p)[i]) << 15;"),
 }
+
+# Mistakes in the exact zero-order hold and in the reverse-mode gradients, caught by the pins of
+# tests/test_oracle_grad_pins.py.
+GRAD_MUTANTS = {
+    "zoh_missing_division": ("return expm1(dt * a) / a;", "return expm1(dt * a);"),
+    "zoh_exp_not_expm1": ("return expm1(dt * a) / a;", "return exp(dt * a) / a;"),
+    "grad_C_uses_adjoint": ("gC[n * L + t] += e * h_t[n];", "gC[n * L + t] += lam * h_t[n];"),
+    "grad_B_missing_x": ("gB[n * L + t] += lam * k * x;", "gB[n * L + t] += lam * k;"),
+    "grad_dt_drops_decay_term": ("gdt += lam * (a_n[n] * decay * h_prev[n] + dk_ddt * Bv * x);",
+                                 "gdt += lam * (dk_ddt * Bv * x);"),
+    "grad_A_uses_new_state": ("gA[n] += lam * (dt * decay * h_prev[n] + dk_da * Bv * x);",
+                              "gA[n] += lam * (dt * decay * h_t[n] + dk_da * Bv * x);"),
+    "adjoint_not_decayed": ("mu[n] = lam * decay;", "mu[n] = lam;"),
+    "gate_grad_is_sigmoid": ("return sg * (1.0 + z * (1.0 - sg));", "return sg;"),
+    "softplus_grad_dropped": ("const double gs = softplus_flag ? gdt * softplus_grad(s) : gdt;",
+                              "const double gs = gdt;"),
+    "skip_grad_dropped": ("double gx = e * Dd, gdt = 0.0;", "double gx = 0.0, gdt = 0.0;"),
+    "gate_not_in_adjoint": ("const double e = dy_rows[i * L + t] * gate;",
+                            "const double e = dy_rows[i * L + t];"),
+    "zoh_dk_da_sign": ("dk_da = (dt * a_n[n] * decay - expm1(dt * a_n[n])) / (a_n[n] * a_n[n]);",
+                       "dk_da = (expm1(dt * a_n[n]) - dt * a_n[n] * decay) / (a_n[n] * a_n[n]);"),
+    "zoh_dk_ddt_euler": ("dk_ddt = decay;", "dk_ddt = 1.0;"),
+    "zoh_zero_A_dk_da": ("dk_da = 0.5 * dt * dt;", "dk_da = dt * dt;"),
+}
+
+GRAD_PINS = [
+    lambda: gpins.test_gradients_match_finite_differences("all_inputs", "euler"),
+    lambda: gpins.test_gradients_match_finite_differences("all_inputs", "zoh"),
+    lambda: gpins.test_gradients_match_finite_differences("bare", "zoh"),
+    gpins.test_zoh_gradients_at_zero_A,
+    gpins.test_zoh_matches_numerical_ode,
+]
 
 PINS = [
     lambda: pins.test_lti_equals_convolution(1, 16, 4, 64),
@@ -69,24 +102,34 @@ def _compile(src_text, out_dir):
     return so
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_catch_mutant(name, monkeypatch):
-    old, new = MUTANTS[name]
+def _caught(old, new, pins_to_run, monkeypatch):
     src = open(SRC).read()
     assert src.count(old) >= 1, f"mutant anchor not found: {old!r}"
     mutated = src.replace(old, new)
-    real = oracle.lib()
     with tempfile.TemporaryDirectory() as td:
         so = _compile(mutated, td)
         mut = ctypes.CDLL(so)
-        for fn in ("oracle_scan_rows", "oracle_state_step_rows"):
-            getattr(mut, fn).restype = getattr(real, fn).restype
-            getattr(mut, fn).argtypes = getattr(real, fn).argtypes
+        for fn, argtypes in oracle.SIGNATURES.items():
+            getattr(mut, fn).restype = ctypes.c_int
+            getattr(mut, fn).argtypes = argtypes
         monkeypatch.setattr(oracle, "_lib", mut)
         caught = []
-        for pin in PINS:
+        for pin in pins_to_run:
             try:
                 pin()
             except (AssertionError, ValueError, FloatingPointError):
                 caught.append(pin)
-        assert caught, f"no pin caught mutant {name}"
+                break
+        return caught
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, monkeypatch):
+    old, new = MUTANTS[name]
+    assert _caught(old, new, PINS, monkeypatch), f"no pin caught mutant {name}"
+
+
+@pytest.mark.parametrize("name", sorted(GRAD_MUTANTS))
+def test_grad_pins_catch_mutant(name, monkeypatch):
+    old, new = GRAD_MUTANTS[name]
+    assert _caught(old, new, GRAD_PINS, monkeypatch), f"no pin caught mutant {name}"

@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
+                    help="fwd: forward scan + decode step (default); bwd: the backward pass alone")
     return ap.parse_args()
 
 
@@ -75,6 +77,16 @@ def step_bytes(cfg) -> int:
     s = esize(cfg.dtype)
     b, d, n = cfg.batch, cfg.dim, cfg.dstate
     return 2 * b * d * n * 4 + b * d * 4 * s + 2 * b * n * s + d * (n + 2) * 4
+
+
+def bwd_bytes(cfg) -> int:
+    """Algorithmic bytes of one backward pass: u, delta, z, dy read and du, ddelta, dz written per
+    element; B, C read and dB, dC (fp32) written per batch row; A, D, bias read and their
+    gradients written; h0 and the last-state gradient read, dh0 written.  The state checkpoints of
+    the recomputation are not counted."""
+    s = esize(cfg.dtype)
+    b, d, n, L = cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen
+    return b * d * L * 7 * s + b * n * L * (2 * s + 2 * 4) + 2 * d * (n + 2) * 4 + 3 * b * d * n * 4
 
 
 def measured_peaks():
@@ -509,13 +521,95 @@ def run_reference(args, cfg, rank):
     }
 
 
+def run_bwd(args, cfg, rank, world, local_rank):
+    """The backward pass alone (mamba_scan_bwd: recompute + reverse sweep), device-timed."""
+    import torch
+    import sequence_scan_selective_b300 as ms
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    inp = synth.scan_inputs(cfg)
+    g = synth.grad_inputs(cfg)
+    params = {k: to_torch(inp[k], "f32", dev) for k in ("A", "D", "delta_bias")}
+    sets = []
+    for _ in range(2):  # two input sets used alternately (inputs larger than L2)
+        st = {k: to_torch(inp[k], cfg.dtype, dev) for k in SCAN_KEYS}
+        st["dy"] = to_torch(g["dy"], cfg.dtype, dev)
+        st["h0"] = to_torch(g["h0"], "f32", dev)
+        st["dlast"] = to_torch(g["dlast"], "f32", dev)
+        sets.append(st)
+    out = None
+    calls = []
+    for st in sets:
+        c, out = ms.prepare_scan_bwd(st["u"], st["delta"], params["A"], st["B"], st["C"], st["dy"],
+                                     params["D"], st["z"], params["delta_bias"], True, h0=st["h0"],
+                                     dlast_state=st["dlast"], out=out)
+        calls.append(c)
+    stream = torch.cuda.current_stream()
+    W = max(args.warmup, 3)
+    for i in range(W):
+        calls[i % 2]()
+    torch.cuda.synchronize()
+    K = args.steps
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n0 = ms.launch_count()
+    with ClockSampler(local_rank) as clk:
+        clk.mark(True)
+        t_start.record(stream)
+        for i in range(K):
+            calls[i % 2]()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        clk.mark(False)
+    launches = ms.launch_count() - n0
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms, avg_ms, launches = aggregate_ranks(dist, dev, total_ms, total_ms / K, launches)
+    elems_step = cfg.batch * cfg.dim * cfg.seqlen
+    peaks, kind = measured_peaks()
+    bb = bwd_bytes(cfg)
+    achieved = bb / (avg_ms * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    line = {
+        "metric": METRIC, "value": whole_job_rate(elems_step, K, world, total_ms), "unit": "elements/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, recipe of the workload)",
+        "config": {"workload": WORKLOADS[args.workload].replace("scan+decode", "backward pass"),
+                   "batch": cfg.batch, "d_inner": cfg.dim, "d_state": cfg.dstate, "seq_len": cfg.seqlen,
+                   "storage": cfg.dtype, "step": "backward pass: gradients of u, delta, z, A, B, C, D, bias, h0",
+                   "elements_per_step": elems_step, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2; two input sets alternate"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": f"{kind} hbm_gbs",
+                     "kernel": "scan_bwd_kernel", "algorithmic_bytes_per_launch": bb,
+                     "kernel_avg_us": round(avg_ms * 1e3, 2)},
+        "clocks": clk.summary(),
+        "gpu_launches": launches,
+        "e2e": None,
+    }
+    if dist:
+        dist.destroy_process_group()
+    return line
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = synth.CONFIGS[args.workload]
-    line = run_reference(args, cfg, rank) if args.impl == "reference" else run_ours(args, cfg, rank, world, local_rank)
+    if args.impl == "reference":
+        line = run_reference(args, cfg, rank)
+    elif args.which == "bwd":
+        line = run_bwd(args, cfg, rank, world, local_rank)
+    else:
+        line = run_ours(args, cfg, rank, world, local_rank)
     if rank == 0 and line is not None:
         print(json.dumps(line), flush=True)
 

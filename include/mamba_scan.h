@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define MAMBA_SCAN_VERSION 1
+#define MAMBA_SCAN_VERSION 2
 
 /* storage type of u / delta / z / B / C / y (A, D, delta_bias and all states are always fp32) */
 #define MAMBA_F32 0
@@ -44,6 +44,12 @@ extern "C" {
 #define MAMBA_ERR_TIMEOUT (-3) /* a kernel gave up a bounded wait (see mamba_scan_device_status) */
 
 #define MAMBA_MAX_DSTATE 64
+
+/* How B is discretised (Abar = exp(Delta A) in both; visual guide section 2.3, zero-order hold):
+ * MAMBA_DISC_SIMPLE: Bbar = Delta * B.  MAMBA_DISC_ZOH: Bbar = (exp(Delta A) - 1) / A * B, the
+ * exact solution of h' = A h + B x with x held over the step (Delta * B where A == 0). */
+#define MAMBA_DISC_SIMPLE 0
+#define MAMBA_DISC_ZOH 1
 
 typedef struct {
     int batch;          /* b  >= 1 */
@@ -134,6 +140,39 @@ int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, const void*
                            const void* B, const void* C, const float* D, const void* z,
                            const float* delta_bias, int softplus_flag, void* y, float* last_state,
                            void* stream);
+
+/*
+ * Gradients of the forward scan (mamba_scan_fwd_state) for the loss
+ *   sum(dy * y) + sum(dlast_state * last_state),
+ * i.e. the backward pass of training.  The expanded states are not stored by the forward pass;
+ * this call recomputes them (visual guide section 3.4, "recomputation"): a forward sweep keeps
+ * one state checkpoint per 16 positions (stream-ordered scratch, cudaMallocAsync on `stream`,
+ * b * ceil(L/16) * d * 64 bytes, freed on the same stream), and a reverse sweep recomputes each
+ * 16-position slot from its checkpoint and walks it backwards.
+ *
+ *   discretization  MAMBA_DISC_SIMPLE (MAMBA_DISC_ZOH is rejected with MAMBA_ERR_ARG for now).
+ *   u .. h0         the forward inputs, as for mamba_scan_fwd_state (z, D, delta_bias, h0 may be
+ *                   NULL with the same meaning).  dstate must be <= 16.
+ *   dy              [b, d, L]  in_dtype: gradient of the loss with respect to y.
+ *   dlast_state     [b, d, N]  fp32 or NULL (= 0): gradient with respect to last_state.
+ * Outputs (written; none may overlap an input or another output):
+ *   du, ddelta      [b, d, L]  in_dtype (ddelta is the gradient with respect to the raw delta,
+ *                              before bias and softplus).
+ *   dz              [b, d, L]  in_dtype, or NULL (not computed; must be NULL when z is NULL).
+ *   dA              [d, N]     fp32, summed over batch and positions.
+ *   dB, dC          [b, N, L]  fp32, summed over channels.
+ *   dD, ddelta_bias [d]        fp32 or NULL (not computed), summed over batch and positions.
+ *   dh0             [b, d, N]  fp32 or NULL: gradient with respect to h0.
+ * With L == 0 only dA, dD, ddelta_bias (zeros) and dh0 (= dlast_state, or zeros) are written and
+ * the per-position pointers may be NULL.  The sums over channels and batch rows are accumulated
+ * with atomics, so their rounding (not their value) can differ between runs.
+ * Errors: MAMBA_ERR_ARG, MAMBA_ERR_CUDA.
+ */
+int mamba_scan_bwd(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
+                   const float* A, const void* B, const void* C, const float* D, const void* z,
+                   const float* delta_bias, int softplus_flag, const float* h0, const void* dy,
+                   const float* dlast_state, void* du, void* ddelta, void* dz, float* dA, float* dB,
+                   float* dC, float* dD, float* ddelta_bias, float* dh0, void* stream);
 
 /* Message describing the calling thread's most recent failure ("" if none). */
 const char* mamba_scan_last_error(void);

@@ -9,6 +9,7 @@ Entry points (names as in include/mamba_scan.h):
   mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, y=None, last_state=None)
   mamba_scan_fwd_noalloc(...)   same arguments; the library allocates no device memory
   mamba_state_step(state, x, delta, A, B, C, D, z, delta_bias, softplus, y=None)
+  mamba_scan_bwd(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0=None, dlast_state=None)
 """
 from __future__ import annotations
 
@@ -51,6 +52,8 @@ def _load() -> ctypes.CDLL:
     lib.mamba_scan_fwd_state.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, I, P, P, P, P]
     lib.mamba_state_step.restype = I
     lib.mamba_state_step.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, I, P, P]
+    lib.mamba_scan_bwd.restype = I
+    lib.mamba_scan_bwd.argtypes = [ctypes.POINTER(Shape), I] + [P] * 8 + [I] + [P] * 13
     lib.mamba_scan_last_error.restype = ctypes.c_char_p
     lib.mamba_scan_last_error.argtypes = []
     lib.mamba_scan_version.restype = I
@@ -65,8 +68,11 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 
 # symbols the header declares; the tests check that every one of them is exported
-EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_state", "mamba_state_step", "mamba_scan_last_error", "mamba_scan_version",
-            "mamba_scan_device_status", "mamba_scan_launch_count")
+EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_state", "mamba_state_step",
+            "mamba_scan_bwd", "mamba_scan_last_error", "mamba_scan_version", "mamba_scan_device_status",
+            "mamba_scan_launch_count")
+MAMBA_DISC_SIMPLE, MAMBA_DISC_ZOH = 0, 1
+_DISC = {"simple": MAMBA_DISC_SIMPLE, "zoh": MAMBA_DISC_ZOH}
 
 
 def lib() -> ctypes.CDLL:
@@ -221,6 +227,60 @@ def prepare_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None
     args, shape, y = _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream)
     keep = (shape, state, x, delta, A, B, C, D, z, delta_bias, y)
     return PreparedCall(_lib.mamba_state_step, args, keep), y
+
+
+def _bwd_args(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0, dlast_state, disc, stream, out):
+    bsz, dim, L = u.shape
+    N = A.shape[1]
+    dt = u.dtype
+    code = _dtype_code(u)
+    f32 = dict(device=u.device, dtype=torch.float32)
+    if out is None:
+        out = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+               "dz": torch.empty_like(u) if z is not None else None,
+               "dA": torch.empty((dim, N), **f32), "dB": torch.empty((bsz, N, L), **f32),
+               "dC": torch.empty((bsz, N, L), **f32),
+               "dD": torch.empty((dim,), **f32) if D is not None else None,
+               "ddelta_bias": torch.empty((dim,), **f32) if delta_bias is not None else None,
+               "dh0": torch.empty((bsz, dim, N), **f32) if h0 is not None else None}
+    shape = Shape(bsz, dim, N, L, code)
+    args = (
+        ctypes.byref(shape), _DISC[disc], _ptr(u, (bsz, dim, L), dt, "u"),
+        _ptr(delta, (bsz, dim, L), dt, "delta"), _ptr(A, (dim, N), torch.float32, "A"),
+        _ptr(B, (bsz, N, L), dt, "B"), _ptr(C, (bsz, N, L), dt, "C"),
+        _ptr(D, (dim,), torch.float32, "D"), _ptr(z, (bsz, dim, L), dt, "z"),
+        _ptr(delta_bias, (dim,), torch.float32, "delta_bias"), int(bool(softplus)),
+        _ptr(h0, (bsz, dim, N), torch.float32, "h0"), _ptr(dy, (bsz, dim, L), dt, "dy"),
+        _ptr(dlast_state, (bsz, dim, N), torch.float32, "dlast_state"),
+        _ptr(out["du"], (bsz, dim, L), dt, "du"), _ptr(out["ddelta"], (bsz, dim, L), dt, "ddelta"),
+        _ptr(out["dz"], (bsz, dim, L), dt, "dz"), _ptr(out["dA"], (dim, N), torch.float32, "dA"),
+        _ptr(out["dB"], (bsz, N, L), torch.float32, "dB"), _ptr(out["dC"], (bsz, N, L), torch.float32, "dC"),
+        _ptr(out["dD"], (dim,), torch.float32, "dD"),
+        _ptr(out["ddelta_bias"], (dim,), torch.float32, "ddelta_bias"),
+        _ptr(out["dh0"], (bsz, dim, N), torch.float32, "dh0"), _stream(stream, u.device))
+    return args, shape, out
+
+
+def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True, h0=None,
+                   dlast_state=None, disc="simple", stream=None, out=None):
+    """Gradients of mamba_scan_fwd for the loss sum(dy * y) + sum(dlast_state * last_state).
+    Inputs as for mamba_scan_fwd plus dy [b, d, L] (input dtype) and dlast_state [b, d, N] float32.
+    Returns a dict: du, ddelta, dz [b, d, L] (input dtype; dz None without z), dA [d, N],
+    dB, dC [b, N, L], dD, ddelta_bias [d] (None when D / delta_bias is None), dh0 [b, d, N]
+    (None without h0), all float32 except du, ddelta, dz.  ``out`` may supply that dict."""
+    args, _shape, out = _bwd_args(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0, dlast_state, disc,
+                                  stream, out)
+    _check(_lib.mamba_scan_bwd(*args))
+    return out
+
+
+def prepare_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True, h0=None,
+                     dlast_state=None, disc="simple", stream=None, out=None):
+    """mamba_scan_bwd with its arguments checked once.  Returns (call, out)."""
+    args, shape, out = _bwd_args(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0, dlast_state, disc,
+                                 stream, out)
+    keep = (shape, u, delta, A, B, C, dy, D, z, delta_bias, h0, dlast_state, out)
+    return PreparedCall(_lib.mamba_scan_bwd, args, keep), out
 
 
 def device_status(stream=None) -> None:

@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "scan_fwd.cuh"
 #include "scan_fwd_tm.cuh"
+#include "scan_bwd.cuh"
 #include "state_step.cuh"
 
 namespace mscan {
@@ -357,6 +358,20 @@ static int step_dispatch(const StepArgs& a, cudaStream_t st) {
     return MAMBA_OK;
 }
 
+template <typename TIn>
+static int bwd_launch(const BwdArgs& a, bool vec, cudaStream_t st) {
+    static std::atomic<unsigned long long> attr_vec{0}, attr_scalar{0};
+    auto kern = vec ? scan_bwd_kernel<TIn, true> : scan_bwd_kernel<TIn, false>;
+    int rc = allow_smem(kern, vec ? attr_vec : attr_scalar);
+    if (rc) return rc;
+    const dim3 grid((unsigned)((a.dim + bwd::kCh - 1) / bwd::kCh), (unsigned)a.batch);
+    kern<<<grid, bwd::kThreads, bwd::Layout<TIn>::BYTES, st>>>(a);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "scan_bwd_kernel launch");
+    return MAMBA_OK;
+}
+
 }  // namespace mscan
 
 using namespace mscan;
@@ -488,6 +503,82 @@ extern "C" int mamba_state_step(const mamba_scan_shape* s, float* state, const v
     if (s->dstate <= 16) return bf ? step_dispatch<uint16_t, 16>(a, st) : step_dispatch<float, 16>(a, st);
     if (s->dstate <= 32) return bf ? step_dispatch<uint16_t, 32>(a, st) : step_dispatch<float, 32>(a, st);
     return bf ? step_dispatch<uint16_t, 64>(a, st) : step_dispatch<float, 64>(a, st);
+}
+
+extern "C" int mamba_scan_bwd(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
+                              const float* A, const void* B, const void* C, const float* D, const void* z,
+                              const float* delta_bias, int softplus_flag, const float* h0, const void* dy,
+                              const float* dlast_state, void* du, void* ddelta, void* dz, float* dA, float* dB,
+                              float* dC, float* dD, float* ddelta_bias, float* dh0, void* stream) {
+    t_err.clear();
+    int rc = check_shape(s, true);
+    if (rc) return rc;
+    if (discretization != MAMBA_DISC_SIMPLE && discretization != MAMBA_DISC_ZOH)
+        return fail(MAMBA_ERR_ARG, "unknown discretization %d", discretization);
+    if (discretization == MAMBA_DISC_ZOH) return fail(MAMBA_ERR_ARG, "the backward pass takes the simplified discretization only");
+    if (s->dstate > 16) return fail(MAMBA_ERR_ARG, "the backward pass supports dstate <= 16");
+    if (s->batch > 65535) return fail(MAMBA_ERR_ARG, "the backward pass supports batch <= 65535");
+    if (s->seqlen > (1LL << 34)) return fail(MAMBA_ERR_ARG, "seqlen too large");
+    if (!A || !dA) return fail(MAMBA_ERR_ARG, "A and dA are required");
+    if (dz && !z) return fail(MAMBA_ERR_ARG, "dz given without z");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const long long chans = (long long)s->batch * s->dim;
+    const long long L = s->seqlen;
+    const int N = s->dstate;
+    const size_t es = s->in_dtype == MAMBA_F32 ? 4 : 2;
+    const size_t nx = (size_t)chans * L * es, nbc4 = (size_t)s->batch * N * L * 4, ns = (size_t)chans * N * 4;
+    cudaError_t e = cudaMemsetAsync(dA, 0, (size_t)s->dim * N * 4, st);
+    if (e == cudaSuccess && dD) e = cudaMemsetAsync(dD, 0, (size_t)s->dim * 4, st);
+    if (e == cudaSuccess && ddelta_bias) e = cudaMemsetAsync(ddelta_bias, 0, (size_t)s->dim * 4, st);
+    if (e != cudaSuccess) return cuda_fail(e, "zeroing parameter gradients");
+    if (L == 0) {  // nothing reaches the inputs; the state's gradient passes straight through
+        if (dh0) {
+            e = dlast_state ? (dlast_state == dh0 ? cudaSuccess
+                                                  : cudaMemcpyAsync(dh0, dlast_state, ns, cudaMemcpyDeviceToDevice, st))
+                            : cudaMemsetAsync(dh0, 0, ns, st);
+            if (e != cudaSuccess) return cuda_fail(e, "dh0 for an empty sequence");
+        }
+        return MAMBA_OK;
+    }
+    if (!u || !delta || !B || !C || !dy || !du || !ddelta || !dB || !dC)
+        return fail(MAMBA_ERR_ARG, "u, delta, B, C, dy, du, ddelta, dB and dC are required");
+    const void* ins[] = {u, delta, z, dy};
+    const void* outs[] = {du, ddelta, dz};
+    for (const void* o : outs)
+        for (const void* i : ins)
+            if (overlaps(o, nx, i, nx)) return fail(MAMBA_ERR_ARG, "a gradient output overlaps an input");
+    if (overlaps(du, nx, ddelta, nx) || overlaps(du, nx, dz, nx) || overlaps(ddelta, nx, dz, nx) ||
+        overlaps(dB, nbc4, dC, nbc4) || overlaps(dB, nbc4, B, nbc4 * es / 4) || overlaps(dC, nbc4, C, nbc4 * es / 4))
+        return fail(MAMBA_ERR_ARG, "gradient outputs overlap");
+    e = cudaMemsetAsync(dB, 0, nbc4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dC, 0, nbc4, st);
+    if (e != cudaSuccess) return cuda_fail(e, "zeroing dB/dC");
+
+    BwdArgs a{};
+    a.u = u; a.delta = delta; a.z = z; a.dy = dy; a.B = B; a.C = C;
+    a.A = A; a.D = D; a.bias = delta_bias; a.h0 = h0; a.dlast = dlast_state;
+    a.du = du; a.ddelta = ddelta; a.dz = dz;
+    a.dA = dA; a.dB = dB; a.dC = dC; a.dD = dD; a.dbias = ddelta_bias; a.dh0 = dh0;
+    a.batch = s->batch; a.dim = s->dim; a.dstate = N; a.L = L;
+    a.ntile = (int)((L + bwd::kT - 1) / bwd::kT);
+    a.nslot = (int)((L + bwd::kSlot - 1) / bwd::kSlot);
+    a.softplus = softplus_flag != 0;
+    const bool vec = (L * (long long)es) % 16 == 0 && aligned16(u) && aligned16(delta) && aligned16(dy) &&
+                     aligned16(B) && aligned16(C) && aligned16(du) && aligned16(ddelta) && aligned16(dB) &&
+                     aligned16(dC) && (!z || aligned16(z)) && (!dz || aligned16(dz));
+    float* ckpt = nullptr;
+    if (a.nslot > 1) {
+        const size_t nck = (size_t)s->batch * a.nslot * s->dim * bwd::kNS * sizeof(float);
+        e = cudaMallocAsync(reinterpret_cast<void**>(&ckpt), nck, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(state checkpoints)");
+    }
+    a.ckpt = ckpt;
+    rc = s->in_dtype == MAMBA_BF16 ? bwd_launch<uint16_t>(a, vec, st) : bwd_launch<float>(a, vec, st);
+    if (ckpt) {
+        e = cudaFreeAsync(ckpt, st);
+        if (rc == MAMBA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(state checkpoints)");
+    }
+    return rc;
 }
 
 extern "C" const char* mamba_scan_last_error(void) { return t_err.c_str(); }

@@ -1,0 +1,536 @@
+// Backward pass of the selective scan, with the states recomputed instead of stored.
+//
+// The forward pass keeps the expanded state h[b, d, n, t] in registers and never writes it (visual
+// guide to Mamba and SSMs, section 3.4, kernel fusion); the backward pass needs it, and the guide's
+// answer (same section, "recomputation") is to recompute it from what is cheap to keep.  Here that
+// is one checkpoint of the state per 16 steps (written by a forward sweep, 1/4 of the size of u in
+// fp32 at N = 16), from which each 16-step slot is recomputed into registers and then walked in
+// reverse.
+//
+// With a_t = exp(Delta_t A), h_t = a_t h_{t-1} + Delta_t B_t x_t, ypre_t = C_t h_t + D x_t and
+// y_t = ypre_t silu(z_t), the reverse walk carries mu_t = dL/dh_t from the later steps:
+//   e_t      = dy_t silu(z_t)                        gradient reaching ypre_t
+//   lam_t    = mu_t + e_t C_t                         total gradient reaching h_t
+//   dC_t    += e_t h_t,  dB_t += lam_t Delta_t x_t    (summed over the channels of a batch row)
+//   dDelta_t = sum_n lam_t (A a_t h_{t-1} + B_t x_t)  (a_t h_{t-1} = h_t - Delta_t B_t x_t)
+//   dx_t     = Delta_t sum_n lam_t B_t + D e_t,   dA += lam_t a_t h_{t-1} Delta_t
+//   mu_{t-1} = a_t lam_t
+// then ddelta = dDelta * sigmoid(delta + bias) (softplus) and dz = dy ypre silu'(z).
+//
+// Work layout: a CTA of 4 warps owns 32 channels of one batch row for the whole sequence; a warp
+// owns 8 channels, lane (c = lane % 8, g = lane / 8) holds states 4g..4g+3 of channel c (N <= 16).
+// Tiles of 32 steps of u, delta, z, dy (per channel) and B, C (per batch row) are staged in shared
+// memory by cp.async, double-buffered.  The sums over channels (dB, dC) are reduced across the 8
+// channel lanes of a warp by a shuffle reduce-scatter, across the 4 warps in shared memory, and
+// across CTAs of the same batch row with vector atomics; the sums over states (dDelta, dx, ypre)
+// across the 4 state lanes of a channel by a second reduce-scatter.
+#pragma once
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "common.cuh"
+
+namespace mscan {
+
+struct BwdArgs {
+    const void* u;      // [b, d, L] TIn
+    const void* delta;  // [b, d, L] TIn
+    const void* z;      // [b, d, L] TIn or null (no gate)
+    const void* dy;     // [b, d, L] TIn
+    const void* B;      // [b, N, L] TIn
+    const void* C;      // [b, N, L] TIn
+    const float* A;     // [d, N]
+    const float* D;     // [d] or null
+    const float* bias;  // [d] or null
+    const float* h0;    // [b, d, N] or null (zero initial state)
+    const float* dlast; // [b, d, N] or null (no gradient at last_state)
+    void* du;           // [b, d, L] TIn
+    void* ddelta;       // [b, d, L] TIn
+    void* dz;           // [b, d, L] TIn or null
+    float* dA;          // [d, N], accumulated (zeroed by the host)
+    float* dB;          // [b, N, L], accumulated (zeroed by the host)
+    float* dC;          // [b, N, L], accumulated (zeroed by the host)
+    float* dD;          // [d] or null, accumulated
+    float* dbias;       // [d] or null, accumulated
+    float* dh0;         // [b, d, N] or null
+    float* ckpt;        // [b, nslot, d, 16] state before each 16-step slot (slot 0 unused)
+    int batch, dim, dstate;
+    long long L;
+    int ntile, nslot;
+    int softplus;
+};
+
+namespace bwd {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kCh = kWarps * 8;  // channels per CTA
+constexpr int kT = 32;           // steps per tile
+constexpr int kSlot = 16;        // steps per recomputed slot
+constexpr int kNS = 16;          // state capacity (lanes per channel x 4)
+constexpr int kPad = kT + 1;     // padded row (floats) of the per-channel and per-state sums
+constexpr int kBcqPitch = 36;    // floats per step in the B/C step buffer (padded)
+
+template <typename TIn>
+struct Layout {
+    static constexpr int ROW = kT * (int)sizeof(TIn) + 16;  // bytes per staged row (padded)
+    static constexpr int CHUNKS = kT * (int)sizeof(TIn) / 16;  // 16-byte pieces per row
+    // one stage: u, delta, z, dy rows of the CTA's channels, then B and C rows
+    static constexpr int OFF_U = 0;
+    static constexpr int OFF_DL = OFF_U + kCh * ROW;
+    static constexpr int OFF_Z = OFF_DL + kCh * ROW;
+    static constexpr int OFF_DY = OFF_Z + kCh * ROW;
+    static constexpr int OFF_B = OFF_DY + kCh * ROW;
+    static constexpr int OFF_C = OFF_B + kNS * ROW;
+    static constexpr int STAGE = OFF_C + kNS * ROW;
+    // after the two stages: B/C per step (bcq[t][0..15] = B, [16..31] = C), per-warp step data
+    // q[t][c] = (Delta, Delta x, e, x), per-warp per-channel sums r[k][c][t] (k: dDelta, sum of
+    // lam B, sum of C h), per-warp dB/dC partials part[t][kind * 16 + n] (kind 0: dC, 1: dB)
+    static constexpr int OFF_BCQ = 2 * STAGE;
+    static constexpr int OFF_Q = OFF_BCQ + kT * kBcqPitch * 4;
+    static constexpr int OFF_R = OFF_Q + kWarps * kT * 8 * 16;
+    static constexpr int OFF_PART = OFF_R + kWarps * 3 * 8 * kPad * 4;
+    static constexpr int BYTES = OFF_PART + kWarps * kT * kPad * 4;
+};
+
+// v[0..7] held by every lane; returns, in the lane with (lane & 7) == k, the sum of v[k] over the
+// 8 lanes that differ from it in bits 0-2.  Seven shuffles instead of 24 for a plain butterfly.
+__device__ __forceinline__ float reduce_scatter8(const float (&v)[8], int lane) {
+    const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+    float w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float send = b2 ? v[j] : v[j + 4];
+        const float keep = b2 ? v[j + 4] : v[j];
+        w[j] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+    float x[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float send = b1 ? w[j] : w[j + 2];
+        const float keep = b1 ? w[j + 2] : w[j];
+        x[j] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    const float send = b0 ? x[0] : x[1];
+    const float keep = b0 ? x[1] : x[0];
+    return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+}
+
+// (v0, v1, v2) held by every lane; returns, in the lane with ((lane >> 3) & 3) == k < 3, the sum
+// of v_k over the 4 lanes that differ from it in bits 3-4 (the state lanes of one channel).
+__device__ __forceinline__ float reduce_scatter3(float v0, float v1, float v2, int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8;
+    const float s0 = b4 ? v0 : v2, k0 = b4 ? v2 : v0;
+    const float s1 = b4 ? v1 : 0.f, k1 = b4 ? 0.f : v1;
+    const float w0 = k0 + __shfl_xor_sync(0xffffffffu, s0, 16);
+    const float w1 = k1 + __shfl_xor_sync(0xffffffffu, s1, 16);
+    const float send = b3 ? w0 : w1;
+    const float keep = b3 ? w1 : w0;
+    return keep + __shfl_xor_sync(0xffffffffu, send, 8);
+}
+
+__device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + ex2_approx(-x * kLog2e)); }
+
+// Stage tile k (steps 32k .. 32k+31) of the CTA's channel rows (u, delta; z and dy when `full`) and
+// of B (and C when `full`) rows n < N.  Positions past L or past the last channel read as zero.
+// VEC: 16-byte cp.async pieces (rows 16-byte aligned, L * sizeof(TIn) a multiple of 16), left in
+// flight; otherwise plain element loads, complete on return.
+template <typename TIn, bool VEC>
+__device__ __forceinline__ void load_tile(uint8_t* st, const BwdArgs& a, int b, int d0, int k, bool full) {
+    using Lt = Layout<TIn>;
+    constexpr int EPC = 16 / (int)sizeof(TIn);  // elements per 16-byte piece
+    const long long t0 = (long long)k * kT;
+    const int tid = threadIdx.x;
+    const int nch_t = full ? 4 : 2;
+    const int nbc_t = full ? 2 : 1;
+    // the four channel tensors sit back to back in a stage: u, delta, z, dy
+    auto chsrc = [&](int tens) -> const void* { return tens == 0 ? a.u : tens == 1 ? a.delta : tens == 2 ? a.z : a.dy; };
+    auto choff = [](int tens) { return Lt::OFF_U + tens * kCh * Lt::ROW; };
+    if (VEC) {
+        constexpr int per = kCh * Lt::CHUNKS;
+        for (int i = tid; i < nch_t * per; i += kThreads) {
+            const int tens = i / per, rem = i - tens * per;
+            const int row = rem / Lt::CHUNKS, piece = rem - row * Lt::CHUNKS;
+            if (!chsrc(tens)) continue;
+            const int d = d0 + row;
+            const long long e0 = t0 + piece * EPC;
+            const bool ok = d < a.dim && e0 < a.L;
+            const TIn* p = static_cast<const TIn*>(chsrc(tens)) +
+                           (ok ? ((long long)b * a.dim + d) * a.L + e0 : 0);
+            cp_async16(st + choff(tens) + row * Lt::ROW + piece * 16, p, ok ? 16u : 0u);
+        }
+        const int perb = a.dstate * Lt::CHUNKS;
+        for (int i = tid; i < nbc_t * perb; i += kThreads) {
+            const int tens = i / perb, rem = i - tens * perb;
+            const int n = rem / Lt::CHUNKS, piece = rem - n * Lt::CHUNKS;
+            const long long e0 = t0 + piece * EPC;
+            const bool ok = e0 < a.L;
+            const TIn* p = static_cast<const TIn*>(tens ? a.C : a.B) +
+                           (ok ? ((long long)b * a.dstate + n) * a.L + e0 : 0);
+            cp_async16(st + (tens ? Lt::OFF_C : Lt::OFF_B) + n * Lt::ROW + piece * 16, p, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+    } else {
+        constexpr int per = kCh * kT;
+        for (int i = tid; i < nch_t * per; i += kThreads) {
+            const int tens = i / per, rem = i - tens * per;
+            const int row = rem / kT, t = rem - row * kT;
+            if (!chsrc(tens)) continue;
+            const int d = d0 + row;
+            const long long e = t0 + t;
+            TIn v{};
+            if (d < a.dim && e < a.L) v = static_cast<const TIn*>(chsrc(tens))[((long long)b * a.dim + d) * a.L + e];
+            reinterpret_cast<TIn*>(st + choff(tens) + row * Lt::ROW)[t] = v;
+        }
+        const int perb = a.dstate * kT;
+        for (int i = tid; i < nbc_t * perb; i += kThreads) {
+            const int tens = i / perb, rem = i - tens * perb;
+            const int n = rem / kT, t = rem - n * kT;
+            const long long e = t0 + t;
+            TIn v{};
+            if (e < a.L) v = static_cast<const TIn*>(tens ? a.C : a.B)[((long long)b * a.dstate + n) * a.L + e];
+            reinterpret_cast<TIn*>(st + (tens ? Lt::OFF_C : Lt::OFF_B) + n * Lt::ROW)[t] = v;
+        }
+    }
+}
+
+// 8 consecutive staged elements (steps 8g .. 8g+7) of one row, widened to fp32.
+template <typename TIn>
+__device__ __forceinline__ void row8(const uint8_t* row, int g, float (&v)[8]) {
+    if constexpr (sizeof(TIn) == 4) {
+        const float4 p0 = reinterpret_cast<const float4*>(row)[2 * g];
+        const float4 p1 = reinterpret_cast<const float4*>(row)[2 * g + 1];
+        v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
+        v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
+    } else {
+        const uint4 p = reinterpret_cast<const uint4*>(row)[g];
+        const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
+// Store 8 consecutive outputs of one row at steps tg0 .. tg0+7 (those below L).
+template <typename TIn, bool VEC>
+__device__ __forceinline__ void store8(TIn* p, long long tg0, long long L, const float (&v)[8]) {
+    if (VEC && tg0 + 8 <= L) {
+        if constexpr (sizeof(TIn) == 4) {
+            reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+            reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        } else {
+            reinterpret_cast<uint4*>(p)[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                        pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (tg0 + j < L) store_out<TIn>(p + j, v[j]);
+    }
+}
+
+}  // namespace bwd
+
+template <typename TIn, bool VEC>
+__global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArgs a) {
+    using namespace bwd;
+    using Lt = bwd::Layout<TIn>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = lane & 7, g = lane >> 3;  // channel lane and state group (also step group)
+    const int b = blockIdx.y;
+    const int d0 = blockIdx.x * kCh;
+    const int row = warp * 8 + c;  // the lane's channel within the CTA
+    const int d = d0 + row;
+    const bool dvalid = d < a.dim;
+    const int N = a.dstate;
+    const bool gate = a.z != nullptr;
+
+    float* bcq = reinterpret_cast<float*>(smem + Lt::OFF_BCQ);
+    float4* q = reinterpret_cast<float4*>(smem + Lt::OFF_Q) + warp * kT * 8;        // [t][c]
+    float* R = reinterpret_cast<float*>(smem + Lt::OFF_R) + warp * 3 * 8 * kPad;     // [k][c][t]
+    float* part = reinterpret_cast<float*>(smem + Lt::OFF_PART) + warp * kT * kPad;  // [t][col]
+
+    // B/C rows of states n >= N stay zero in both stages: their states never move
+    for (int i = tid; i < 2 * 2 * kNS * Lt::ROW / 16; i += kThreads) {
+        const int stg = i / (2 * kNS * Lt::ROW / 16), rem = i - stg * (2 * kNS * Lt::ROW / 16);
+        reinterpret_cast<uint4*>(smem + stg * Lt::STAGE + Lt::OFF_B)[rem] = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
+
+    float Aj[4], A2[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int n = 4 * g + j;
+        Aj[j] = (dvalid && n < N) ? a.A[(long long)d * N + n] : 0.f;
+        A2[j] = Aj[j] * kLog2e;
+    }
+    const float bias_c = (dvalid && a.bias) ? a.bias[d] : 0.f;
+    const float D_c = (dvalid && a.D) ? a.D[d] : 0.f;
+    const long long chrow = ((long long)b * a.dim + d) * a.L;  // start of the channel's rows
+
+    float h0v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int n = 4 * g + j;
+        h0v[j] = (a.h0 && dvalid && n < N) ? a.h0[((long long)b * a.dim + d) * N + n] : 0.f;
+    }
+    float* ck = a.ckpt ? a.ckpt + (((long long)b * a.nslot) * a.dim + d) * kNS + 4 * g : nullptr;
+    const long long ckstride = (long long)a.dim * kNS;  // floats between consecutive slots
+
+    // Phase A: per (channel, step) quantities of tile k for this lane's channel c, steps 8g..8g+7.
+    auto phase_a = [&](const uint8_t* st, int k, bool full) {
+        const long long t0 = (long long)k * kT;
+        float dl[8], uu[8], zz[8], dyv[8];
+        row8<TIn>(st + Lt::OFF_DL + row * Lt::ROW, g, dl);
+        row8<TIn>(st + Lt::OFF_U + row * Lt::ROW, g, uu);
+        if (full) {
+            row8<TIn>(st + Lt::OFF_DY + row * Lt::ROW, g, dyv);
+            if (gate) row8<TIn>(st + Lt::OFF_Z + row * Lt::ROW, g, zz);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+            float2 s2 = make_float2(dl[j] + bias_c, dl[j + 1] + bias_c);
+            if (a.softplus) s2 = softplus2(s2);
+            const float sv[2] = {s2.x, s2.y};
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int t = 8 * g + j + i;
+                const bool ok = dvalid && t0 + t < a.L;
+                const float dt = ok ? sv[i] : 0.f;
+                const float x = ok ? uu[j + i] : 0.f;
+                float e = 0.f;
+                if (full && ok) e = gate ? dyv[j + i] * silu_f(zz[j + i]) : dyv[j + i];
+                q[t * 8 + c] = make_float4(dt, dt * x, e, x);
+            }
+        }
+    };
+
+    // B (and C) of the tile, one step per row of bcq: thread (t = lane, warp) moves states 4w..4w+3.
+    auto transpose_bc = [&](const uint8_t* st, bool withC) {
+        const TIn* Bs = reinterpret_cast<const TIn*>(st + Lt::OFF_B);
+        const TIn* Cs = reinterpret_cast<const TIn*>(st + Lt::OFF_C);
+        constexpr int RW = Lt::ROW / (int)sizeof(TIn);
+        const int t = lane, n0 = 4 * warp;
+        float4 bq = make_float4(In<TIn>::to_f32(Bs[(n0 + 0) * RW + t]), In<TIn>::to_f32(Bs[(n0 + 1) * RW + t]),
+                                In<TIn>::to_f32(Bs[(n0 + 2) * RW + t]), In<TIn>::to_f32(Bs[(n0 + 3) * RW + t]));
+        *reinterpret_cast<float4*>(bcq + t * kBcqPitch + n0) = bq;
+        if (withC) {
+            float4 cq = make_float4(In<TIn>::to_f32(Cs[(n0 + 0) * RW + t]), In<TIn>::to_f32(Cs[(n0 + 1) * RW + t]),
+                                    In<TIn>::to_f32(Cs[(n0 + 2) * RW + t]), In<TIn>::to_f32(Cs[(n0 + 3) * RW + t]));
+            *reinterpret_cast<float4*>(bcq + t * kBcqPitch + 16 + n0) = cq;
+        }
+    };
+
+    // ---------------------------------------------------------------- forward sweep: checkpoints
+    if (a.nslot > 1) {
+        float h[4] = {h0v[0], h0v[1], h0v[2], h0v[3]};
+        if (VEC) load_tile<TIn, VEC>(smem, a, b, d0, 0, false);
+        for (int k = 0; k < a.ntile; ++k) {
+            uint8_t* st = smem + (k & 1) * Lt::STAGE;
+            if (VEC) {
+                if (k + 1 < a.ntile) {
+                    load_tile<TIn, VEC>(smem + ((k + 1) & 1) * Lt::STAGE, a, b, d0, k + 1, false);
+                    cp_async_wait<1>();
+                } else {
+                    cp_async_wait<0>();
+                }
+            } else {
+                load_tile<TIn, VEC>(st, a, b, d0, k, false);
+            }
+            __syncthreads();
+            transpose_bc(st, false);
+            phase_a(st, k, false);
+            __syncthreads();
+#pragma unroll 1
+            for (int s = 0; s < 2; ++s) {
+                const int gs = 2 * k + s;
+                if (gs >= a.nslot) break;
+                if (gs >= 1 && dvalid) *reinterpret_cast<float4*>(ck + gs * ckstride) = make_float4(h[0], h[1], h[2], h[3]);
+#pragma unroll
+                for (int i = 0; i < bwd::kSlot; ++i) {
+                    const int t = s * bwd::kSlot + i;
+                    const float4 qq = q[t * 8 + c];
+                    const float4 bq = *reinterpret_cast<const float4*>(bcq + t * kBcqPitch + 4 * g);
+                    const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) h[j] = fmaf(ex2_approx(qq.x * A2[j]), h[j], qq.y * bv[j]);
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // ---------------------------------------------------------------- reverse sweep
+    float mu[4], dAacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int n = 4 * g + j;
+        mu[j] = (a.dlast && dvalid && n < N) ? a.dlast[((long long)b * a.dim + d) * N + n] : 0.f;
+    }
+    float dD_acc = 0.f, dbias_acc = 0.f;
+    const int col = (c >> 2) * 16 + 4 * g + (c & 3);  // this lane's dC/dB column after the scatter
+    if (VEC) load_tile<TIn, VEC>(smem + ((a.ntile - 1) & 1) * Lt::STAGE, a, b, d0, a.ntile - 1, true);
+#pragma unroll 1
+    for (int k = a.ntile - 1; k >= 0; --k) {
+        uint8_t* st = smem + (k & 1) * Lt::STAGE;
+        const long long t0 = (long long)k * kT;
+        if (VEC) {
+            if (k > 0) {
+                load_tile<TIn, VEC>(smem + ((k - 1) & 1) * Lt::STAGE, a, b, d0, k - 1, true);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
+            }
+        } else {
+            load_tile<TIn, VEC>(st, a, b, d0, k, true);
+        }
+        __syncthreads();
+        transpose_bc(st, true);
+        phase_a(st, k, true);
+        __syncthreads();
+
+#pragma unroll 1
+        for (int s = 1; s >= 0; --s) {
+            const int gs = 2 * k + s;
+            if (gs >= a.nslot) continue;  // wholly past L: nothing moves there
+            float h[4];
+            if (gs == 0) {
+                h[0] = h0v[0]; h[1] = h0v[1]; h[2] = h0v[2]; h[3] = h0v[3];
+            } else {
+                const float4 v = dvalid ? *reinterpret_cast<const float4*>(ck + gs * ckstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+                h[0] = v.x; h[1] = v.y; h[2] = v.z; h[3] = v.w;
+            }
+            // recompute the slot's states
+            float hist[bwd::kSlot][4];
+#pragma unroll
+            for (int i = 0; i < bwd::kSlot; ++i) {
+                const int t = s * bwd::kSlot + i;
+                const float4 qq = q[t * 8 + c];
+                const float4 bq = *reinterpret_cast<const float4*>(bcq + t * kBcqPitch + 4 * g);
+                const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    h[j] = fmaf(ex2_approx(qq.x * A2[j]), h[j], qq.y * bv[j]);
+                    hist[i][j] = h[j];
+                }
+            }
+            // walk the slot in reverse
+#pragma unroll
+            for (int i = bwd::kSlot - 1; i >= 0; --i) {
+                const int t = s * bwd::kSlot + i;
+                const float4 qq = q[t * 8 + c];  // (Delta, Delta x, e, x)
+                const float4 bq = *reinterpret_cast<const float4*>(bcq + t * kBcqPitch + 4 * g);
+                const float4 cq = *reinterpret_cast<const float4*>(bcq + t * kBcqPitch + 16 + 4 * g);
+                const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
+                const float cv[4] = {cq.x, cq.y, cq.z, cq.w};
+                float v[8];
+                float sdt = 0.f, sub = 0.f, sch = 0.f;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float ht = hist[i][j];
+                    const float bx = qq.y * bv[j];
+                    const float ah = ht - bx;  // a_t h_{t-1}
+                    const float lam = fmaf(qq.z, cv[j], mu[j]);
+                    sch = fmaf(cv[j], ht, sch);
+                    v[j] = qq.z * ht;
+                    v[4 + j] = lam * qq.y;
+                    sub = fmaf(lam, bv[j], sub);
+                    sdt = fmaf(lam, fmaf(Aj[j], ah, bv[j] * qq.w), sdt);
+                    dAacc[j] = fmaf(lam * ah, qq.x, dAacc[j]);
+                    mu[j] = ex2_approx(qq.x * A2[j]) * lam;
+                }
+                part[t * kPad + col] = reduce_scatter8(v, lane);
+                const float r3 = reduce_scatter3(sdt, sub, sch, lane);
+                if (g < 3) R[(g * 8 + c) * kPad + t] = r3;
+            }
+        }
+        __syncwarp();
+
+        // Phase C: per (channel, step) gradients for channel c, steps 8g .. 8g+7 of the tile
+        {
+            float dl[8], zz[8], dyv[8], o_du[8], o_dd[8], o_dz[8];
+            row8<TIn>(st + Lt::OFF_DL + row * Lt::ROW, g, dl);
+            row8<TIn>(st + Lt::OFF_DY + row * Lt::ROW, g, dyv);
+            if (gate) row8<TIn>(st + Lt::OFF_Z + row * Lt::ROW, g, zz);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int t = 8 * g + j;
+                const bool ok = dvalid && t0 + t < a.L;
+                const float4 qq = q[t * 8 + c];
+                const float sdt = R[(0 * 8 + c) * kPad + t];
+                const float sub = R[(1 * 8 + c) * kPad + t];
+                const float sch = R[(2 * 8 + c) * kPad + t];
+                const float sarg = dl[j] + bias_c;
+                const float gdt = a.softplus ? sdt * sigmoid_f(sarg) : sdt;
+                o_dd[j] = gdt;
+                o_du[j] = fmaf(sub, qq.x, qq.z * D_c);
+                if (gate) {
+                    const float sg = sigmoid_f(zz[j]);
+                    const float ypre = fmaf(D_c, qq.w, sch);
+                    o_dz[j] = dyv[j] * ypre * sg * fmaf(zz[j], 1.f - sg, 1.f);
+                }
+                if (ok) {
+                    dD_acc = fmaf(qq.z, qq.w, dD_acc);
+                    dbias_acc += gdt;
+                }
+            }
+            if (dvalid) {
+                const long long off = chrow + t0 + 8 * g;
+                store8<TIn, VEC>(static_cast<TIn*>(a.du) + off, t0 + 8 * g, a.L, o_du);
+                store8<TIn, VEC>(static_cast<TIn*>(a.ddelta) + off, t0 + 8 * g, a.L, o_dd);
+                if (gate && a.dz) store8<TIn, VEC>(static_cast<TIn*>(a.dz) + off, t0 + 8 * g, a.L, o_dz);
+            }
+        }
+        __syncthreads();
+
+        // dB, dC of the tile: sum the 4 warps' partials, one atomic per 4 steps per CTA
+        {
+            const float* P = reinterpret_cast<const float*>(smem + Lt::OFF_PART);
+#pragma unroll
+            for (int rep = 0; rep < 2; ++rep) {
+                const int gi = tid + rep * kThreads;  // 256 groups: (column, 4 steps)
+                const int colr = gi >> 3, tq = gi & 7;
+                const int kind = colr >> 4, n = colr & 15;
+                if (n < N) {
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w)
+#pragma unroll
+                        for (int tt = 0; tt < 4; ++tt) acc[tt] += P[w * kT * kPad + (tq * 4 + tt) * kPad + colr];
+                    const long long tg = t0 + tq * 4;
+                    float* dst = (kind ? a.dB : a.dC) + ((long long)b * N + n) * a.L + tg;
+                    if (VEC) {
+                        if (tg < a.L) red_add_v4(dst, make_float4(acc[0], acc[1], acc[2], acc[3]));
+                    } else {
+#pragma unroll
+                        for (int tt = 0; tt < 4; ++tt)
+                            if (tg + tt < a.L) atomicAdd(dst + tt, acc[tt]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---------------------------------------------------------------- per-channel results
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int n = 4 * g + j;
+        if (dvalid && n < N) {
+            atomicAdd(a.dA + (long long)d * N + n, dAacc[j]);
+            if (a.dh0) a.dh0[((long long)b * a.dim + d) * N + n] = mu[j];
+        }
+    }
+    dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 8);
+    dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 16);
+    dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, 8);
+    dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, 16);
+    if (dvalid && g == 0) {
+        if (a.dD) atomicAdd(a.dD + d, dD_acc);
+        if (a.dbias) atomicAdd(a.dbias + d, dbias_acc);
+    }
+}
+
+}  // namespace mscan

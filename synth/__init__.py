@@ -39,6 +39,8 @@ DELTA_MAX = 1e-1
 _T_U, _T_DELTA, _T_Z, _T_B, _T_C, _T_D, _T_BIAS, _T_H0 = range(1, 9)
 # decode tensors use separate ids so they never share a stream with the scan tensors
 _T_DX, _T_DDELTA, _T_DZ, _T_DB, _T_DC = range(11, 16)
+# backward-pass inputs: gradient at y, gradient at last_state, initial state of a scan
+_T_DY, _T_DLAST, _T_SH0 = range(21, 24)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -211,6 +213,38 @@ def scan_inputs(cfg: ScanConfig, seqlen: Optional[int] = None) -> dict:
         out[k] = rows[k].reshape(cfg.batch, cfg.dim, L)
     out.update(scan_bc(cfg, L))
     return out
+
+
+# ----------------------------------------------------------------------------------------- backward
+def grad_rows(cfg: ScanConfig, rows: Iterable[int], seqlen: Optional[int] = None) -> np.ndarray:
+    """Gradient arriving at y for the given flat channel rows: N(0, 1), [len(rows), L] in the
+    storage dtype."""
+    rows = np.asarray(list(rows), dtype=np.int64)
+    L = seqlen or cfg.seqlen
+    arr = np.empty((len(rows), L), dtype=_storage_dtype(cfg.dtype))
+    _fill_rows(arr, rows, lambda r: _rng(cfg.seed, _T_DY, r).standard_normal(L, dtype=np.float32), cfg.dtype)
+    return arr
+
+
+def state_rows(cfg: ScanConfig, rows: Iterable[int], which: str) -> np.ndarray:
+    """Per-channel fp32 state-shaped inputs, N(0, 1), [len(rows), N]: ``which`` = "h0" (initial
+    state of a scan) or "dlast" (gradient arriving at last_state)."""
+    rows = np.asarray(list(rows), dtype=np.int64)
+    tid = {"h0": _T_SH0, "dlast": _T_DLAST}[which]
+    arr = np.empty((len(rows), cfg.dstate), dtype=np.float32)
+    _fill_rows(arr, rows, lambda r: _rng(cfg.seed, tid, r).standard_normal(cfg.dstate, dtype=np.float32),
+               "f32")
+    return arr
+
+
+def grad_inputs(cfg: ScanConfig, seqlen: Optional[int] = None) -> dict:
+    """Backward-pass inputs for the whole workload: dy [batch, dim, L] (storage dtype),
+    dlast_state and h0 [batch, dim, N] (fp32)."""
+    L = seqlen or cfg.seqlen
+    rows = range(cfg.batch * cfg.dim)
+    return {"dy": grad_rows(cfg, rows, L).reshape(cfg.batch, cfg.dim, L),
+            "dlast": state_rows(cfg, rows, "dlast").reshape(cfg.batch, cfg.dim, cfg.dstate),
+            "h0": state_rows(cfg, rows, "h0").reshape(cfg.batch, cfg.dim, cfg.dstate)}
 
 
 # ----------------------------------------------------------------------------------------- decode

@@ -96,3 +96,39 @@ def test_product_package_does_not_reach_the_oracle():
         if os.path.isfile(path) and path.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
             text = open(path, errors="replace").read()
             assert "oracle" not in text.lower(), path
+
+
+def _prototypes():
+    """name -> number of parameters, from the comment-stripped header."""
+    out = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"(mamba_\w+)\s*\(([^)]*)\)\s*;", text):
+            params = m.group(2).strip()
+            out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_header(ms):
+    lib = ms.lib()
+    protos = _prototypes()
+    assert protos
+    for name, n in protos.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+
+
+def test_bwd_host_argument_checks(ms):
+    lib = ms.lib()
+    P = ctypes.c_void_p
+    d = P(256)  # never dereferenced: every case below fails validation first
+    args = lambda s, disc=0, z=None, dz=None, A=d: (ctypes.byref(s), disc, d, d, A, d, d, None, z, None, 1, None, d,
+                                                   None, d, d, dz, d, d, d, None, None, None, None)
+    assert lib.mamba_scan_bwd(*args(_shape(ms, dstate=17))) == -1
+    assert b"dstate" in lib.mamba_scan_last_error()
+    assert lib.mamba_scan_bwd(*args(_shape(ms), disc=7)) == -1
+    assert lib.mamba_scan_bwd(*args(_shape(ms), dz=d)) == -1
+    assert b"dz" in lib.mamba_scan_last_error()
+    assert lib.mamba_scan_bwd(*args(_shape(ms), A=None)) == -1
+    assert lib.mamba_scan_bwd(*args(_shape(ms, seqlen=-3))) == -1

@@ -45,10 +45,11 @@ SIGNATURES = {
                                _I],
     "oracle_state_step_rows_ex": [_LL, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I,
                                   _P, _I],
+    "oracle_causal_conv_rows": [_LL, _P, _I, _I, _LL, _I, _P, _P, _P, _I, _P, _P],
     "oracle_scan_bwd_rows": [_LL, _P, _P, _I, _I, _I, _LL, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I,
                              _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I],
 }
-DISC = {"euler": 0, "zoh": 1}
+DISC = {"simple": 0, "zoh": 1}
 
 
 def build(force: bool = False) -> str:
@@ -88,9 +89,9 @@ def _storage(a, dt):
 
 
 def scan_rows(rows, dim, u_rows, delta_rows, z_rows, A, D, delta_bias, B, C, softplus=True,
-              dtype="f32", h0_rows=None, nthreads=0, disc="euler"):
+              dtype="f32", h0_rows=None, nthreads=0, disc="simple"):
     """Scan for the channels ``rows`` (flat b*dim + d).  u/delta/z_rows [nrows, L] in storage
-    dtype; B, C [batch, N, L].  ``disc`` is "euler" (Bbar = Delta B) or "zoh" (exact zero-order
+    dtype; B, C [batch, N, L].  ``disc`` is "simple" (Bbar = Delta B) or "zoh" (exact zero-order
     hold).  Returns (y [nrows, L], state [nrows, N]) in float64."""
     dt = _DT[dtype]
     rows = np.asarray(rows, dtype=np.int64)
@@ -106,7 +107,7 @@ def scan_rows(rows, dim, u_rows, delta_rows, z_rows, A, D, delta_bias, B, C, sof
     h0 = _c(h0_rows, np.float64)
     y = np.empty((nrows, L), dtype=np.float64)
     st = np.empty((nrows, N), dtype=np.float64)
-    if disc == "euler":  # the plain entry point, so a planted mistake in it is seen by every pin
+    if disc == "simple":  # the plain entry point, so a planted mistake in it is seen by every pin
         rc = lib().oracle_scan_rows(nrows, _ptr(rb), _ptr(rd), dim, N, L, dt, _ptr(u_rows),
                                     _ptr(delta_rows), _ptr(z_rows), _ptr(A), _ptr(D),
                                     _ptr(delta_bias), _ptr(B), _ptr(C), int(bool(softplus)),
@@ -122,7 +123,7 @@ def scan_rows(rows, dim, u_rows, delta_rows, z_rows, A, D, delta_bias, B, C, sof
 
 
 def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, dtype="f32", h0=None,
-         nthreads=0, disc="euler"):
+         nthreads=0, disc="simple"):
     """Full scan.  u, delta, z [batch, dim, L]; returns y [batch, dim, L], last_state [batch, dim, N]
     (float64)."""
     bsz, dim, L = np.asarray(u).shape
@@ -136,7 +137,7 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, dtyp
 
 
 def state_step_rows(rows, dim, state_rows, x_rows, delta_rows, z_rows, A, D, delta_bias, B, C,
-                    softplus=True, dtype="f32", nthreads=0, disc="euler"):
+                    softplus=True, dtype="f32", nthreads=0, disc="simple"):
     """One decode step for channels ``rows``.  state_rows [nrows, N] float64 is updated IN PLACE;
     x/delta/z_rows [nrows]; B, C [batch, N].  Returns y [nrows] float64."""
     dt = _DT[dtype]
@@ -153,7 +154,7 @@ def state_step_rows(rows, dim, state_rows, x_rows, delta_rows, z_rows, A, D, del
     B, C = _storage(B, dt), _storage(C, dt)
     D, delta_bias = _c(D, np.float32), _c(delta_bias, np.float32)
     y = np.empty(nrows, dtype=np.float64)
-    if disc == "euler":
+    if disc == "simple":
         rc = lib().oracle_state_step_rows(nrows, _ptr(rb), _ptr(rd), dim, N, dt, _ptr(state_rows),
                                           _ptr(x_rows), _ptr(delta_rows), _ptr(z_rows), _ptr(A),
                                           _ptr(D), _ptr(delta_bias), _ptr(B), _ptr(C),
@@ -170,7 +171,7 @@ def state_step_rows(rows, dim, state_rows, x_rows, delta_rows, z_rows, A, D, del
 
 
 def state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
-               dtype="f32", nthreads=0, disc="euler"):
+               dtype="f32", nthreads=0, disc="simple"):
     """Full decode step.  state [batch, dim, N] float64 updated in place; x/delta/z [batch, dim];
     B, C [batch, N].  Returns y [batch, dim] float64."""
     bsz, dim, N = state.shape
@@ -183,7 +184,7 @@ def state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softpl
 
 
 def scan_bwd_rows(rows, batch, dim, u_rows, delta_rows, z_rows, A, D, delta_bias, B, C, dy_rows,
-                  softplus=True, dtype="f32", h0_rows=None, dstate_rows=None, disc="euler",
+                  softplus=True, dtype="f32", h0_rows=None, dstate_rows=None, disc="simple",
                   nthreads=0):
     """Gradients of the scan for the channels ``rows``: the loss is sum(dy * y) +
     sum(dstate * last_state) over those channels.  Returns a dict of float64 arrays: per channel
@@ -219,7 +220,7 @@ def scan_bwd_rows(rows, batch, dim, u_rows, delta_rows, z_rows, A, D, delta_bias
 
 
 def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True, dtype="f32",
-             h0=None, dlast_state=None, disc="euler", nthreads=0):
+             h0=None, dlast_state=None, disc="simple", nthreads=0):
     """Gradients of the full scan.  u, delta, z, dy [batch, dim, L]; dlast_state [batch, dim, N]
     (None = 0).  Returns a dict: du, ddelta, dz [batch, dim, L], dh0 [batch, dim, N], dA [dim, N],
     dD, ddelta_bias [dim], dB, dC [batch, N, L] (float64)."""
@@ -234,3 +235,34 @@ def scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=Tr
             out[k] = out[k].reshape(bsz, dim, L)
     out["dh0"] = out["dh0"].reshape(bsz, dim, N)
     return out
+
+
+def causal_conv_rows(rows, dim, x_rows, w, conv_bias=None, silu=True, dtype="f32", x_prev_rows=None):
+    """Causal depthwise convolution of the channels ``rows`` (flat b*dim + d): x_rows [nrows, L]
+    in storage dtype, w [dim, K], conv_bias [dim]; x_prev_rows [nrows, K-1] (the inputs before
+    position 0, oldest first; None = zeros).  Returns u [nrows, L] float64."""
+    dt = _DT[dtype]
+    rows = np.asarray(rows, dtype=np.int64)
+    w = _c(w, np.float32)
+    K = w.shape[1]
+    L = np.asarray(x_rows).shape[-1]
+    rd = np.ascontiguousarray(rows % dim, dtype=np.int32)
+    x_rows = _storage(x_rows, dt)
+    prev = _c(x_prev_rows, np.float64)
+    u = np.empty((len(rows), L), dtype=np.float64)
+    rc = lib().oracle_causal_conv_rows(len(rows), _ptr(rd), dim, K, L, dt, _ptr(x_rows), _ptr(w),
+                                       _ptr(_c(conv_bias, np.float32)), int(bool(silu)), _ptr(prev), _ptr(u))
+    if rc != 0:
+        raise ValueError(f"oracle_causal_conv_rows rejected its arguments (rc={rc})")
+    return u
+
+
+def causal_conv(x, w, conv_bias=None, silu=True, dtype="f32", x_prev=None):
+    """Full causal depthwise convolution: x [batch, dim, L] -> u [batch, dim, L] float64;
+    x_prev [batch, dim, K-1] or None."""
+    bsz, dim, L = np.asarray(x).shape
+    K = np.asarray(w).shape[1]
+    prev = None if x_prev is None else np.asarray(x_prev, np.float64).reshape(bsz * dim, K - 1)
+    u = causal_conv_rows(np.arange(bsz * dim), dim, np.asarray(x).reshape(bsz * dim, L), w, conv_bias, silu,
+                         dtype, prev)
+    return u.reshape(bsz, dim, L)

@@ -334,3 +334,40 @@ int oracle_scan_bwd_rows(long long nrows, const int* row_b, const int* row_d, in
     }
     return failed ? -2 : 0;
 }
+
+/*
+ * Causal depthwise convolution over time, the step the Mamba block applies to the expanded input
+ * before the selective SSM (visual guide, section 3.5: a convolution in front of the SSM so that
+ * tokens are not processed independently).  Per channel d, with kernel width K:
+ *   u[t] = act(conv_bias[d] + sum_{k=0}^{K-1} w[d, k] * x[t - (K-1) + k])
+ * where x at positions before 0 comes from x_prev (the K-1 inputs preceding the sequence, oldest
+ * first) or is zero, and act is silu when act_silu is set, else the identity.  The width, the
+ * "previous inputs" convention and the activation are readings: the pages do not give them.
+ *
+ * x_rows [nrows, seqlen] in in_dtype; w [dim, K], conv_bias [dim] (may be NULL) fp32;
+ * x_prev_rows [nrows, K-1] fp64 or NULL; u_rows [nrows, seqlen] fp64 (output).
+ */
+int oracle_causal_conv_rows(long long nrows, const int* row_d, int dim, int K, long long seqlen, int in_dtype,
+                            const void* x_rows, const float* w, const float* conv_bias, int act_silu,
+                            const double* x_prev_rows, double* u_rows) {
+    if (nrows < 0 || dim <= 0 || K <= 0 || K > 64 || seqlen < 0) return -1;
+    if (nrows > 0 && (!row_d || !x_rows || !w || !u_rows)) return -1;
+    if (in_dtype != ORACLE_F32 && in_dtype != ORACLE_BF16) return -1;
+    for (long long i = 0; i < nrows; ++i) {
+        const int d = row_d[i];
+        for (long long t = 0; t < seqlen; ++t) {
+            double acc = conv_bias ? (double)conv_bias[d] : 0.0;
+            for (int k = 0; k < K; ++k) {
+                const long long s = t - (K - 1) + k;  /* input position this tap reads */
+                double xv = 0.0;
+                if (s >= 0)
+                    xv = widen(x_rows, i * seqlen + s, in_dtype);
+                else if (x_prev_rows)
+                    xv = x_prev_rows[i * (K - 1) + (K - 1) + s];
+                acc += (double)w[(long long)d * K + k] * xv;
+            }
+            u_rows[i * seqlen + t] = act_silu ? silu(acc) : acc;
+        }
+    }
+    return 0;
+}

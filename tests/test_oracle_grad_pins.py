@@ -84,7 +84,7 @@ CONFIGS = {
 }
 
 
-@pytest.mark.parametrize("disc", ["euler", "zoh"])
+@pytest.mark.parametrize("disc", ["simple", "zoh"])
 @pytest.mark.parametrize("cfg", sorted(CONFIGS))
 def test_gradients_match_finite_differences(cfg, disc):
     c, dy, ds, softplus = _case(11 + len(cfg), **CONFIGS[cfg])
@@ -159,7 +159,7 @@ def test_zoh_matches_numerical_ode():
     assert _rel(y, _ode_scan(c, softplus)) < 1e-9
 
 
-def test_zoh_and_euler_differ_at_second_order():
+def test_zoh_and_simple_differ_at_second_order():
     """The simplified Bbar = Delta B agrees with the hold to first order in Delta: halving every
     step size quarters the gap in the first state update."""
     c, _, _, _ = _case(8, bsz=1, dim=2, N=3, L=1, softplus=False, gate=False, h0=False)
@@ -167,14 +167,14 @@ def test_zoh_and_euler_differ_at_second_order():
     for scale in (1.0, 0.5, 0.25):
         cc = {**c, "delta": (c["delta"] * np.float32(scale)).astype(np.float32)}
         ye, _ = oracle.scan(cc["u"], cc["delta"], cc["A"], cc["B"], cc["C"], None, None, None,
-                            False, "f32", disc="euler")
+                            False, "f32", disc="simple")
         yz, _ = oracle.scan(cc["u"], cc["delta"], cc["A"], cc["B"], cc["C"], None, None, None,
                             False, "f32", disc="zoh")
         gaps.append(np.max(np.abs(ye - yz)))
     assert 3.6 < gaps[0] / gaps[1] < 4.4 and 3.8 < gaps[1] / gaps[2] < 4.2, gaps
 
 
-def test_zoh_equals_euler_where_A_is_zero():
+def test_zoh_equals_simple_where_A_is_zero():
     c, _, _, softplus = _case(9, zero_A=True)
     c["A"][:] = 0.0
     ye, se = oracle.scan(c["u"], c["delta"], c["A"], c["B"], c["C"], c["D"], c["z"],

@@ -14,6 +14,7 @@ import tempfile
 import pytest
 
 import oracle
+import test_oracle_conv_pins as cpins
 import test_oracle_grad_pins as gpins
 import test_oracle_pins as pins
 
@@ -66,8 +67,23 @@ GRAD_MUTANTS = {
     "zoh_zero_A_dk_da": ("dk_da = 0.5 * dt * dt;", "dk_da = dt * dt;"),
 }
 
+# Mistakes in the causal convolution, caught by the pins of tests/test_oracle_conv_pins.py.
+CONV_MUTANTS = {
+    "conv_taps_reversed": ("const long long s = t - (K - 1) + k;", "const long long s = t - k;"),
+    "conv_previous_inputs_ignored": ("else if (x_prev_rows)", "else if (0)"),
+    "conv_bias_dropped": ("double acc = conv_bias ? (double)conv_bias[d] : 0.0;", "double acc = 0.0;"),
+    "conv_activation_dropped": ("u_rows[i * seqlen + t] = act_silu ? silu(acc) : acc;",
+                                "u_rows[i * seqlen + t] = acc;"),
+}
+
+CONV_PINS = [
+    lambda: cpins.test_conv_matches_numpy_convolve(4),
+    cpins.test_conv_activation_is_silu,
+    lambda: cpins.test_split_sequence_with_previous_inputs(3),
+]
+
 GRAD_PINS = [
-    lambda: gpins.test_gradients_match_finite_differences("all_inputs", "euler"),
+    lambda: gpins.test_gradients_match_finite_differences("all_inputs", "simple"),
     lambda: gpins.test_gradients_match_finite_differences("all_inputs", "zoh"),
     lambda: gpins.test_gradients_match_finite_differences("bare", "zoh"),
     gpins.test_zoh_gradients_at_zero_A,
@@ -133,3 +149,9 @@ def test_pins_catch_mutant(name, monkeypatch):
 def test_grad_pins_catch_mutant(name, monkeypatch):
     old, new = GRAD_MUTANTS[name]
     assert _caught(old, new, GRAD_PINS, monkeypatch), f"no pin caught mutant {name}"
+
+
+@pytest.mark.parametrize("name", sorted(CONV_MUTANTS))
+def test_conv_pins_catch_mutant(name, monkeypatch):
+    old, new = CONV_MUTANTS[name]
+    assert _caught(old, new, CONV_PINS, monkeypatch), f"no pin caught mutant {name}"

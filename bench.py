@@ -56,6 +56,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
                     help="fwd: forward scan + decode step (default); bwd: the backward pass alone")
+    ap.add_argument("--conv", type=int, default=0,
+                    help="fwd pass: fuse a causal depthwise convolution of this width (1-4) in front of the scan")
+    ap.add_argument("--disc", choices=["simple", "zoh"], default="simple",
+                    help="discretisation of B in the forward scan and decode step")
     return ap.parse_args()
 
 
@@ -295,10 +299,20 @@ def run_ours(args, cfg, rank, world, local_rank):
     ydec = torch.empty((cfg.batch, cfg.dim), device=dev, dtype=sets[0]["u"].dtype)
     stream = torch.cuda.current_stream()
     # the public API's prepared form: arguments are checked once, each launch is one C call
-    scans = [ms.prepare_scan_fwd(s["u"], s["delta"], params["A"], s["B"], s["C"], params["D"], s["z"],
-                                 params["delta_bias"], True, y=y, last_state=state)[0] for s in sets]
+    if args.conv:
+        cp = {k: to_torch(v, "f32", dev) for k, v in synth.conv_params(cfg, args.conv).items()}
+        scans = [ms.prepare_scan_fwd_conv(s["u"], cp["conv_w"], cp["conv_bias"], s["delta"], params["A"], s["B"],
+                                          s["C"], params["D"], s["z"], params["delta_bias"], True, disc=args.disc,
+                                          y=y, last_state=state)[0] for s in sets]
+    elif args.disc != "simple":
+        scans = [ms.prepare_scan_fwd(s["u"], s["delta"], params["A"], s["B"], s["C"], params["D"], s["z"],
+                                     params["delta_bias"], True, y=y, last_state=state, disc=args.disc)[0]
+                 for s in sets]
+    else:
+        scans = [ms.prepare_scan_fwd(s["u"], s["delta"], params["A"], s["B"], s["C"], params["D"], s["z"],
+                                     params["delta_bias"], True, y=y, last_state=state)[0] for s in sets]
     decode = ms.prepare_state_step(state, dsets["x"], dsets["delta"], params["A"], dsets["B"], dsets["C"],
-                                   params["D"], dsets["z"], params["delta_bias"], True, y=ydec)[0]
+                                   params["D"], dsets["z"], params["delta_bias"], True, y=ydec, disc=args.disc)[0]
 
     def step(i, ev=None):
         if ev is not None:
@@ -339,7 +353,8 @@ def run_ours(args, cfg, rank, world, local_rank):
 
     elems_step = cfg.batch * cfg.dim * (cfg.seqlen + 1)
     value = whole_job_rate(elems_step, K, world, total_ms)
-    e2e = None if args.no_e2e else run_e2e(args, cfg, inp, dec, params, dev, world, dist)
+    e2e = None if (args.no_e2e or args.conv or args.disc != "simple") else run_e2e(args, cfg, inp, dec, params, dev,
+                                                                                  world, dist)
 
     peaks, kind = measured_peaks()
     sb = scan_bytes(cfg)
@@ -355,7 +370,9 @@ def run_ours(args, cfg, rank, world, local_rank):
         "dtype": "f32", "data": "synthetic (seeded, recipe of the workload)",
         "config": {"workload": WORKLOADS[args.workload], "batch": cfg.batch, "d_inner": cfg.dim,
                    "d_state": cfg.dstate, "seq_len": cfg.seqlen, "storage": cfg.dtype,
-                   "step": "fwd scan (last_state) + 1 decode step from it",
+                   "step": "fwd scan (last_state) + 1 decode step from it"
+                           + (f"; causal conv (width {args.conv}) fused in front of the scan" if args.conv else "")
+                           + ("; exact zero-order hold" if args.disc == "zoh" else ""),
                    "elements_per_step": elems_step, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2; two input sets alternate"},
         "roofline": roofline,
@@ -363,7 +380,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "gpu_launches": launches,
         "e2e": e2e,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.conv and args.disc == "simple":
         line["cpu_baseline"] = cpu_baseline(cfg, inp, dec)
     if dist:
         dist.destroy_process_group()

@@ -100,6 +100,39 @@ int mamba_scan_fwd_state(const mamba_scan_shape* s, const void* u, const void* d
                          float* last_state, void* stream);
 
 /*
+ * mamba_scan_fwd_state with a choice of discretisation: MAMBA_DISC_SIMPLE (identical to
+ * mamba_scan_fwd_state) or MAMBA_DISC_ZOH, the exact zero-order hold
+ *   Bbar_t x_t = (exp(Delta_t A) - 1) / A * B_t x_t     (Delta_t B_t x_t where A == 0),
+ * the discretisation the visual guide names in section 2.3 (the input held constant over each step
+ * of length Delta).  Any other value is MAMBA_ERR_ARG.  Everything else as for mamba_scan_fwd_state.
+ */
+int mamba_scan_fwd_ex(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
+                      const float* A, const void* B, const void* C, const float* D, const void* z,
+                      const float* delta_bias, int softplus_flag, const float* h0, void* y,
+                      float* last_state, void* stream);
+
+/*
+ * The block's causal depthwise convolution fused in front of the scan (visual guide section 3.5:
+ * the Mamba block convolves the expanded input before the selective SSM).  Instead of u the call
+ * takes the convolution's input x and computes, inside the scan kernel, per channel d
+ *   u[t] = act(conv_bias[d] + sum_{k=0}^{conv_k-1} conv_w[d, k] * x[t - conv_k + 1 + k]),
+ * act = silu when conv_silu is nonzero, else the identity; u is never written to memory.  It feeds
+ * both the recurrence (Bbar u) and the skip term (D u).
+ *
+ *   x             [b, d, L]  in_dtype (takes the place of u).
+ *   conv_w        [d, conv_k] fp32, 1 <= conv_k <= 4.   conv_bias [d] fp32 or NULL (= 0).
+ *   conv_prev     [b, d, conv_k - 1] fp32 or NULL (= 0): the inputs x before position 0, oldest
+ *                 first, for a sequence scanned in pieces (pass the previous piece's last
+ *                 conv_k - 1 inputs, together with its last_state as h0).
+ * Everything else as for mamba_scan_fwd_ex.
+ */
+int mamba_scan_fwd_conv(const mamba_scan_shape* s, int discretization, const void* x, const float* conv_w,
+                        const float* conv_bias, int conv_k, int conv_silu, const float* conv_prev,
+                        const void* delta, const float* A, const void* B, const void* C, const float* D,
+                        const void* z, const float* delta_bias, int softplus_flag, const float* h0, void* y,
+                        float* last_state, void* stream);
+
+/*
  * One recurrent decoding step for every (batch, channel): constant work per token, no cache of
  * past tokens (news write-up, "architecture" section; visual guide section 1.4).
  *
@@ -113,6 +146,12 @@ int mamba_scan_fwd_state(const mamba_scan_shape* s, const void* u, const void* d
 int mamba_state_step(const mamba_scan_shape* s, float* state, const void* x, const void* delta,
                      const float* A, const void* B, const void* C, const float* D, const void* z,
                      const float* delta_bias, int softplus_flag, void* y, void* stream);
+
+/* mamba_state_step with a choice of discretisation (MAMBA_DISC_SIMPLE or MAMBA_DISC_ZOH, as for
+ * mamba_scan_fwd_ex). */
+int mamba_state_step_ex(const mamba_scan_shape* s, int discretization, float* state, const void* x,
+                        const void* delta, const float* A, const void* B, const void* C, const float* D,
+                        const void* z, const float* delta_bias, int softplus_flag, void* y, void* stream);
 
 /*
  * Allocation-free variant of mamba_scan_fwd.  The pages describe nothing like it: it exists for
@@ -146,11 +185,11 @@ int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, const void*
  *   sum(dy * y) + sum(dlast_state * last_state),
  * i.e. the backward pass of training.  The expanded states are not stored by the forward pass;
  * this call recomputes them (visual guide section 3.4, "recomputation"): a forward sweep keeps
- * one state checkpoint per 16 positions (stream-ordered scratch, cudaMallocAsync on `stream`,
- * b * ceil(L/16) * d * 64 bytes, freed on the same stream), and a reverse sweep recomputes each
- * 16-position slot from its checkpoint and walks it backwards.
+ * one state checkpoint per 8 positions (stream-ordered scratch, cudaMallocAsync on `stream`,
+ * b * ceil(L/8) * d * 64 bytes, freed on the same stream), and a reverse sweep recomputes each
+ * 8-position slot from its checkpoint and walks it backwards.
  *
- *   discretization  MAMBA_DISC_SIMPLE (MAMBA_DISC_ZOH is rejected with MAMBA_ERR_ARG for now).
+ *   discretization  MAMBA_DISC_SIMPLE or MAMBA_DISC_ZOH: the one the forward pass used.
  *   u .. h0         the forward inputs, as for mamba_scan_fwd_state (z, D, delta_bias, h0 may be
  *                   NULL with the same meaning).  dstate must be <= 16.
  *   dy              [b, d, L]  in_dtype: gradient of the loss with respect to y.

@@ -6,7 +6,8 @@ the computation runs in the library's sm_103a kernels; there is no fallback.  If
 library is missing, importing this package raises ImportError.
 
 Entry points (names as in include/mamba_scan.h):
-  mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, y=None, last_state=None)
+  mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, y=None, last_state=None, h0=None,
+                 disc="simple")   (h0 -> mamba_scan_fwd_state; disc="zoh" -> mamba_scan_fwd_ex)
   mamba_scan_fwd_noalloc(...)   same arguments; the library allocates no device memory
   mamba_state_step(state, x, delta, A, B, C, D, z, delta_bias, softplus, y=None)
   mamba_scan_bwd(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0=None, dlast_state=None)
@@ -50,6 +51,13 @@ def _load() -> ctypes.CDLL:
         getattr(lib, name).argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, I, P, P, P]
     lib.mamba_scan_fwd_state.restype = I
     lib.mamba_scan_fwd_state.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, I, P, P, P, P]
+    lib.mamba_scan_fwd_ex.restype = I
+    lib.mamba_scan_fwd_ex.argtypes = [ctypes.POINTER(Shape), I, P, P, P, P, P, P, P, P, I, P, P, P, P]
+    lib.mamba_scan_fwd_conv.restype = I
+    lib.mamba_scan_fwd_conv.argtypes = [ctypes.POINTER(Shape), I, P, P, P, I, I, P, P, P, P, P, P, P, P, I, P, P, P,
+                                        P]
+    lib.mamba_state_step_ex.restype = I
+    lib.mamba_state_step_ex.argtypes = [ctypes.POINTER(Shape), I, P, P, P, P, P, P, P, P, P, I, P, P]
     lib.mamba_state_step.restype = I
     lib.mamba_state_step.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, I, P, P]
     lib.mamba_scan_bwd.restype = I
@@ -68,8 +76,8 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 
 # symbols the header declares; the tests check that every one of them is exported
-EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_state", "mamba_state_step",
-            "mamba_scan_bwd", "mamba_scan_last_error", "mamba_scan_version", "mamba_scan_device_status",
+EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_state", "mamba_scan_fwd_ex",
+            "mamba_scan_fwd_conv", "mamba_state_step", "mamba_state_step_ex", "mamba_scan_bwd", "mamba_scan_last_error", "mamba_scan_version", "mamba_scan_device_status",
             "mamba_scan_launch_count")
 MAMBA_DISC_SIMPLE, MAMBA_DISC_ZOH = 0, 1
 _DISC = {"simple": MAMBA_DISC_SIMPLE, "zoh": MAMBA_DISC_ZOH}
@@ -133,16 +141,64 @@ class PreparedCall:
 
 
 def mamba_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
-                   last_state=None, want_state=True, stream=None, h0=None):
+                   last_state=None, want_state=True, stream=None, h0=None, disc="simple"):
     """Selective scan.  u, delta, z [b, d, L]; B, C [b, N, L] (float32 or bfloat16, all the same);
     A [d, N], D [d], delta_bias [d] float32; h0 [b, d, N] float32 initial state (None = zero; it may
-    be the last_state tensor itself).  Returns (y [b, d, L] in the input dtype, last_state
-    [b, d, N] float32 or None)."""
+    be the last_state tensor itself); disc "simple" (Bbar = Delta B) or "zoh" (exact zero-order
+    hold).  Returns (y [b, d, L] in the input dtype, last_state [b, d, N] float32 or None)."""
+    if disc != "simple":
+        return _scan(_lib.mamba_scan_fwd_ex, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
+                     want_state, stream, h0, disc)
     if h0 is not None:
         return _scan(_lib.mamba_scan_fwd_state, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
                      want_state, stream, h0)
     return _scan(_lib.mamba_scan_fwd, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
                  want_state, stream)
+
+
+def mamba_scan_fwd_conv(x, conv_w, conv_bias, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                        conv_silu=True, conv_prev=None, h0=None, disc="simple", y=None, last_state=None,
+                        want_state=True, stream=None):
+    """The scan with the block's causal depthwise convolution fused in front: x [b, d, L] (input
+    dtype) replaces u, conv_w [d, K] (K <= 4) and conv_bias [d] float32, conv_prev [b, d, K-1]
+    float32 (inputs before position 0, or None).  Other arguments and the result as for
+    mamba_scan_fwd."""
+    args, _shape, y, last_state = _conv_args(x, conv_w, conv_bias, delta, A, B, C, D, z, delta_bias, softplus,
+                                             conv_silu, conv_prev, h0, disc, y, last_state, want_state, stream)
+    _check(_lib.mamba_scan_fwd_conv(*args))
+    return y, last_state
+
+
+def prepare_scan_fwd_conv(x, conv_w, conv_bias, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                          conv_silu=True, conv_prev=None, h0=None, disc="simple", y=None, last_state=None,
+                          want_state=True, stream=None):
+    """mamba_scan_fwd_conv with its arguments checked once.  Returns (call, y, last_state)."""
+    args, shape, y, last_state = _conv_args(x, conv_w, conv_bias, delta, A, B, C, D, z, delta_bias, softplus,
+                                            conv_silu, conv_prev, h0, disc, y, last_state, want_state, stream)
+    keep = (shape, x, conv_w, conv_bias, conv_prev, delta, A, B, C, D, z, delta_bias, h0, y, last_state)
+    return PreparedCall(_lib.mamba_scan_fwd_conv, args, keep), y, last_state
+
+
+def _conv_args(x, conv_w, conv_bias, delta, A, B, C, D, z, delta_bias, softplus, conv_silu, conv_prev, h0, disc,
+               y, last_state, want_state, stream):
+    bsz, dim, L = x.shape
+    N = A.shape[1]
+    K = conv_w.shape[1]
+    dt = x.dtype
+    if y is None:
+        y = torch.empty_like(x)
+    if last_state is None and want_state:
+        last_state = torch.empty((bsz, dim, N), device=x.device, dtype=torch.float32)
+    shape = Shape(bsz, dim, N, L, _dtype_code(x))
+    args = (ctypes.byref(shape), _DISC[disc], _ptr(x, (bsz, dim, L), dt, "x"),
+            _ptr(conv_w, (dim, K), torch.float32, "conv_w"), _ptr(conv_bias, (dim,), torch.float32, "conv_bias"),
+            int(K), int(bool(conv_silu)), _ptr(conv_prev, (bsz, dim, K - 1), torch.float32, "conv_prev"),
+            _ptr(delta, (bsz, dim, L), dt, "delta"), _ptr(A, (dim, N), torch.float32, "A"),
+            _ptr(B, (bsz, N, L), dt, "B"), _ptr(C, (bsz, N, L), dt, "C"), _ptr(D, (dim,), torch.float32, "D"),
+            _ptr(z, (bsz, dim, L), dt, "z"), _ptr(delta_bias, (dim,), torch.float32, "delta_bias"),
+            int(bool(softplus)), _ptr(h0, (bsz, dim, N), torch.float32, "h0"), _ptr(y, (bsz, dim, L), dt, "y"),
+            _ptr(last_state, (bsz, dim, N), torch.float32, "last_state"), _stream(stream, x.device))
+    return args, shape, y, last_state
 
 
 def mamba_scan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
@@ -154,7 +210,8 @@ def mamba_scan_fwd_noalloc(u, delta, A, B, C, D=None, z=None, delta_bias=None, s
                  want_state, stream)
 
 
-def _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream, h0=None):
+def _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream, h0=None,
+               disc="simple"):
     bsz, dim, L = u.shape
     N = A.shape[1]
     dt = u.dtype
@@ -164,46 +221,55 @@ def _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
     if last_state is None and want_state:
         last_state = torch.empty((bsz, dim, N), device=u.device, dtype=torch.float32)
     shape = Shape(bsz, dim, N, L, code)
-    args = (
-        ctypes.byref(shape), _ptr(u, (bsz, dim, L), dt, "u"), _ptr(delta, (bsz, dim, L), dt, "delta"),
+    lead = (ctypes.byref(shape), _DISC[disc]) if fn is _lib.mamba_scan_fwd_ex else (ctypes.byref(shape),)
+    args = lead + (
+        _ptr(u, (bsz, dim, L), dt, "u"), _ptr(delta, (bsz, dim, L), dt, "delta"),
         _ptr(A, (dim, N), torch.float32, "A"), _ptr(B, (bsz, N, L), dt, "B"),
         _ptr(C, (bsz, N, L), dt, "C"), _ptr(D, (dim,), torch.float32, "D"),
         _ptr(z, (bsz, dim, L), dt, "z"), _ptr(delta_bias, (dim,), torch.float32, "delta_bias"),
         int(bool(softplus)))
-    if fn is _lib.mamba_scan_fwd_state:
+    if fn is _lib.mamba_scan_fwd_state or fn is _lib.mamba_scan_fwd_ex:
         args = args + (_ptr(h0, (bsz, dim, N), torch.float32, "h0"),)
     args = args + (_ptr(y, (bsz, dim, L), dt, "y"), _ptr(last_state, (bsz, dim, N), torch.float32, "last_state"),
                    _stream(stream, u.device))
     return args, shape, y, last_state
 
 
-def _scan(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream, h0=None):
+def _scan(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want_state, stream, h0=None,
+          disc="simple"):
     args, _shape, y, last_state = _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
-                                             want_state, stream, h0)
+                                             want_state, stream, h0, disc)
     _check(fn(*args))
     return y, last_state
 
 
 def prepare_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
-                     last_state=None, want_state=True, stream=None, noalloc=False):
-    """mamba_scan_fwd (or mamba_scan_fwd_noalloc) with its arguments checked once.  Returns
-    (call, y, last_state); call() enqueues the scan on the stream current at preparation."""
-    fn = _lib.mamba_scan_fwd_noalloc if noalloc else _lib.mamba_scan_fwd
+                     last_state=None, want_state=True, stream=None, noalloc=False, disc="simple"):
+    """mamba_scan_fwd (or mamba_scan_fwd_noalloc; mamba_scan_fwd_ex for disc="zoh") with its
+    arguments checked once.  Returns (call, y, last_state); call() enqueues the scan on the stream
+    current at preparation."""
+    if disc != "simple":
+        if noalloc:
+            raise ValueError("the allocation-free entry point takes the simplified discretisation only")
+        fn = _lib.mamba_scan_fwd_ex
+    else:
+        fn = _lib.mamba_scan_fwd_noalloc if noalloc else _lib.mamba_scan_fwd
     args, shape, y, last_state = _scan_args(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state,
-                                            want_state, stream)
+                                            want_state, stream, None, disc)
     keep = (shape, u, delta, A, B, C, D, z, delta_bias, y, last_state)
     return PreparedCall(fn, args, keep), y, last_state
 
 
-def _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream):
+def _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream, disc="simple"):
     bsz, dim, N = state.shape
     dt = x.dtype
     code = _dtype_code(x)
     if y is None:
         y = torch.empty_like(x)
     shape = Shape(bsz, dim, N, 1, code)
-    args = (
-        ctypes.byref(shape), _ptr(state, (bsz, dim, N), torch.float32, "state"),
+    lead = (ctypes.byref(shape),) if disc == "simple" else (ctypes.byref(shape), _DISC[disc])
+    args = lead + (
+        _ptr(state, (bsz, dim, N), torch.float32, "state"),
         _ptr(x, (bsz, dim), dt, "x"), _ptr(delta, (bsz, dim), dt, "delta"),
         _ptr(A, (dim, N), torch.float32, "A"), _ptr(B, (bsz, N), dt, "B"), _ptr(C, (bsz, N), dt, "C"),
         _ptr(D, (dim,), torch.float32, "D"), _ptr(z, (bsz, dim), dt, "z"),
@@ -213,20 +279,22 @@ def _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream):
 
 
 def mamba_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
-                     stream=None):
+                     stream=None, disc="simple"):
     """One decode step.  state [b, d, N] float32 (updated in place); x, delta, z [b, d];
-    B, C [b, N]; returns y [b, d] in the input dtype."""
-    args, _shape, y = _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream)
-    _check(_lib.mamba_state_step(*args))
+    B, C [b, N]; disc as for mamba_scan_fwd; returns y [b, d] in the input dtype."""
+    args, _shape, y = _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream, disc)
+    _check((_lib.mamba_state_step if disc == "simple" else _lib.mamba_state_step_ex)(*args))
     return y
 
 
 def prepare_state_step(state, x, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
-                       stream=None):
-    """mamba_state_step with its arguments checked once.  Returns (call, y)."""
-    args, shape, y = _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream)
+                       stream=None, disc="simple"):
+    """mamba_state_step (mamba_state_step_ex for disc="zoh") with its arguments checked once.
+    Returns (call, y)."""
+    args, shape, y = _step_args(state, x, delta, A, B, C, D, z, delta_bias, softplus, y, stream, disc)
     keep = (shape, state, x, delta, A, B, C, D, z, delta_bias, y)
-    return PreparedCall(_lib.mamba_state_step, args, keep), y
+    fn = _lib.mamba_state_step if disc == "simple" else _lib.mamba_state_step_ex
+    return PreparedCall(fn, args, keep), y
 
 
 def _bwd_args(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0, dlast_state, disc, stream, out):

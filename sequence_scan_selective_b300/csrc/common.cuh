@@ -60,10 +60,44 @@ __device__ __forceinline__ float softplus1(float x) { return softplus2(make_floa
 // silu(z) = z / (1 + e^-z)
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.f + ex2_approx(-z * kLog2e)); }
 
+__device__ __forceinline__ float sigmoid_approx(float x) { return rcp_approx(1.f + ex2_approx(-x * kLog2e)); }
+
 __device__ __forceinline__ float2 silu2(float2 z) {
     const float2 e = make_float2(ex2_approx(-z.x * kLog2e), ex2_approx(-z.y * kLog2e));
     const float2 den = fadd2(e, make_float2(1.f, 1.f));
     return fmul2(z, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+}
+
+// ------------------------------------------------------------------------------ zero-order hold
+// The hold's factor (e^x - 1) / x and, for gradients, its derivative companion
+// (x e^x - (e^x - 1)) / x^2, as Taylor series for small |x|.  The argument is given in base-2
+// units, X = x log2(e) (the exponent the kernels already form for exp2), so the coefficients are
+// ln2^k / (k+1)! and k ln2^(k-1) / (k+1)!; the series are used for |x| < 1/4, where six terms leave
+// a relative error below 5e-8.
+constexpr double kLn2d = 0.6931471805599453;
+constexpr float kZohSeriesLimit = (float)(0.25 * 1.4426950408889634);  // |X| bound for the series
+
+__device__ __forceinline__ float2 zoh_phi2(float2 X) {
+    constexpr double l = kLn2d;
+    const float2 c5 = make_float2((float)(l * l * l * l * l / 720.0), (float)(l * l * l * l * l / 720.0));
+    float2 p = ffma2(c5, X, make_float2((float)(l * l * l * l / 120.0), (float)(l * l * l * l / 120.0)));
+    p = ffma2(p, X, make_float2((float)(l * l * l / 24.0), (float)(l * l * l / 24.0)));
+    p = ffma2(p, X, make_float2((float)(l * l / 6.0), (float)(l * l / 6.0)));
+    p = ffma2(p, X, make_float2((float)(l / 2.0), (float)(l / 2.0)));
+    return ffma2(p, X, make_float2(1.f, 1.f));
+}
+
+__device__ __forceinline__ float zoh_phi(float X) { return zoh_phi2(make_float2(X, X)).x; }
+
+// psi(x) = (x e^x - (e^x - 1)) / x^2 = sum_{k>=1} k x^(k-1) / (k+1)!, argument in base-2 units.
+__device__ __forceinline__ float zoh_psi(float X) {
+    constexpr double l = kLn2d;
+    float p = (float)(6.0 * l * l * l * l * l / 5040.0);
+    p = fmaf(p, X, (float)(5.0 * l * l * l * l / 720.0));
+    p = fmaf(p, X, (float)(4.0 * l * l * l / 120.0));
+    p = fmaf(p, X, (float)(3.0 * l * l / 24.0));
+    p = fmaf(p, X, (float)(2.0 * l / 6.0));
+    return fmaf(p, X, 0.5f);
 }
 
 }  // namespace mscan

@@ -313,7 +313,7 @@ static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, bool softpl
     // N <= 16 with MAMBA_SCAN_TMEM=1: the variant that feeds B/C through tensor memory (not the
     // default: slower on the measured workloads)
     if constexpr (NP == 16) {
-        if (getenv("MAMBA_SCAN_TMEM") != nullptr)
+        if (getenv("MAMBA_SCAN_TMEM") != nullptr && !a.zoh && a.conv_w == nullptr)
             return fwd_run<TIn, NP, true, 4>(s, a, softplus, gate, scratch, scratch_cap, st);
         // lanes per channel: 2 (8 states per lane, 16 channels per warp) or 4
         if (env_int("MAMBA_SCAN_LPC", 4) == 2)
@@ -358,10 +358,10 @@ static int step_dispatch(const StepArgs& a, cudaStream_t st) {
     return MAMBA_OK;
 }
 
-template <typename TIn>
+template <typename TIn, bool ZOH>
 static int bwd_launch(const BwdArgs& a, bool vec, cudaStream_t st) {
     static std::atomic<unsigned long long> attr_vec{0}, attr_scalar{0};
-    auto kern = vec ? scan_bwd_kernel<TIn, true> : scan_bwd_kernel<TIn, false>;
+    auto kern = vec ? scan_bwd_kernel<TIn, true, ZOH> : scan_bwd_kernel<TIn, false, ZOH>;
     int rc = allow_smem(kern, vec ? attr_vec : attr_scalar);
     if (rc) return rc;
     const dim3 grid((unsigned)((a.dim + bwd::kCh - 1) / bwd::kCh), (unsigned)a.batch);
@@ -376,13 +376,23 @@ static int bwd_launch(const BwdArgs& a, bool vec, cudaStream_t st) {
 
 using namespace mscan;
 
+struct ConvSpec {
+    const float* w = nullptr;
+    const float* bias = nullptr;
+    const float* prev = nullptr;
+    int k = 0;
+    int silu = 0;
+};
+
 static int scan_fwd_impl(const mamba_scan_shape* s, const void* u, const void* delta, const float* A, const void* B,
                          const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
                          const float* h0, void* y, float* last_state, float2* scratch, size_t scratch_cap,
-                         void* stream) {
+                         void* stream, int discretization = MAMBA_DISC_SIMPLE, ConvSpec conv = ConvSpec()) {
     t_err.clear();
     int rc = check_shape(s, true);
     if (rc) return rc;
+    if (discretization != MAMBA_DISC_SIMPLE && discretization != MAMBA_DISC_ZOH)
+        return fail(MAMBA_ERR_ARG, "unknown discretization %d", discretization);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const long long chans = (long long)s->batch * s->dim;
     if (s->seqlen == 0) {
@@ -413,6 +423,9 @@ static int scan_fwd_impl(const mamba_scan_shape* s, const void* u, const void* d
     a.y = y; a.last_state = last_state; a.h0 = h0;
     a.batch = s->batch; a.dim = s->dim; a.dstate = s->dstate;
     a.L = s->seqlen;
+    a.zoh = discretization == MAMBA_DISC_ZOH;
+    a.conv_w = conv.w; a.conv_bias = conv.bias; a.conv_prev = conv.prev;
+    a.conv_k = conv.k; a.conv_silu = conv.silu;
     const bool sp = softplus_flag != 0, gate = z != nullptr;
     const bool bf = s->in_dtype == MAMBA_BF16;
     if (s->dstate <= 16)
@@ -436,6 +449,28 @@ extern "C" int mamba_scan_fwd_state(const mamba_scan_shape* s, const void* u, co
                                     float* last_state, void* stream) {
     return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, h0, y, last_state, nullptr, 0,
                          stream);
+}
+
+extern "C" int mamba_scan_fwd_ex(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
+                                 const float* A, const void* B, const void* C, const float* D, const void* z,
+                                 const float* delta_bias, int softplus_flag, const float* h0, void* y,
+                                 float* last_state, void* stream) {
+    return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, h0, y, last_state, nullptr, 0,
+                         stream, discretization);
+}
+
+extern "C" int mamba_scan_fwd_conv(const mamba_scan_shape* s, int discretization, const void* x, const float* conv_w,
+                                   const float* conv_bias, int conv_k, int conv_silu, const float* conv_prev,
+                                   const void* delta, const float* A, const void* B, const void* C, const float* D,
+                                   const void* z, const float* delta_bias, int softplus_flag, const float* h0,
+                                   void* y, float* last_state, void* stream) {
+    t_err.clear();
+    if (!conv_w) return fail(MAMBA_ERR_ARG, "conv_w is required");
+    if (conv_k < 1 || conv_k > 4) return fail(MAMBA_ERR_ARG, "conv_k must be in [1, 4]");
+    ConvSpec cs;
+    cs.w = conv_w; cs.bias = conv_bias; cs.prev = conv_prev; cs.k = conv_k; cs.silu = conv_silu != 0;
+    return scan_fwd_impl(s, x, delta, A, B, C, D, z, delta_bias, softplus_flag, h0, y, last_state, nullptr, 0, stream,
+                         discretization, cs);
 }
 
 // ---------------------------------------------------------------------------- allocation-free variant
@@ -478,12 +513,14 @@ extern "C" int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, 
                          (size_t)MAMBA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
-extern "C" int mamba_state_step(const mamba_scan_shape* s, float* state, const void* x, const void* delta,
-                                const float* A, const void* B, const void* C, const float* D, const void* z,
-                                const float* delta_bias, int softplus_flag, void* y, void* stream) {
+static int state_step_impl(const mamba_scan_shape* s, int discretization, float* state, const void* x,
+                           const void* delta, const float* A, const void* B, const void* C, const float* D,
+                           const void* z, const float* delta_bias, int softplus_flag, void* y, void* stream) {
     t_err.clear();
     int rc = check_shape(s, false);
     if (rc) return rc;
+    if (discretization != MAMBA_DISC_SIMPLE && discretization != MAMBA_DISC_ZOH)
+        return fail(MAMBA_ERR_ARG, "unknown discretization %d", discretization);
     if (!state || !x || !delta || !A || !B || !C || !y)
         return fail(MAMBA_ERR_ARG, "state, x, delta, A, B, C and y are required");
     const long long chans = (long long)s->batch * s->dim;
@@ -497,12 +534,27 @@ extern "C" int mamba_state_step(const mamba_scan_shape* s, float* state, const v
     a.A = A; a.D = D; a.bias = delta_bias; a.y = y;
     a.batch = s->batch; a.dim = s->dim; a.dstate = s->dstate;
     a.softplus = softplus_flag != 0;
+    a.zoh = discretization == MAMBA_DISC_ZOH;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool bf = s->in_dtype == MAMBA_BF16;
     if (s->dstate <= 4) return bf ? step_dispatch<uint16_t, 4>(a, st) : step_dispatch<float, 4>(a, st);
     if (s->dstate <= 16) return bf ? step_dispatch<uint16_t, 16>(a, st) : step_dispatch<float, 16>(a, st);
     if (s->dstate <= 32) return bf ? step_dispatch<uint16_t, 32>(a, st) : step_dispatch<float, 32>(a, st);
     return bf ? step_dispatch<uint16_t, 64>(a, st) : step_dispatch<float, 64>(a, st);
+}
+
+extern "C" int mamba_state_step(const mamba_scan_shape* s, float* state, const void* x, const void* delta,
+                                const float* A, const void* B, const void* C, const float* D, const void* z,
+                                const float* delta_bias, int softplus_flag, void* y, void* stream) {
+    return state_step_impl(s, MAMBA_DISC_SIMPLE, state, x, delta, A, B, C, D, z, delta_bias, softplus_flag, y,
+                           stream);
+}
+
+extern "C" int mamba_state_step_ex(const mamba_scan_shape* s, int discretization, float* state, const void* x,
+                                   const void* delta, const float* A, const void* B, const void* C, const float* D,
+                                   const void* z, const float* delta_bias, int softplus_flag, void* y,
+                                   void* stream) {
+    return state_step_impl(s, discretization, state, x, delta, A, B, C, D, z, delta_bias, softplus_flag, y, stream);
 }
 
 extern "C" int mamba_scan_bwd(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
@@ -515,7 +567,6 @@ extern "C" int mamba_scan_bwd(const mamba_scan_shape* s, int discretization, con
     if (rc) return rc;
     if (discretization != MAMBA_DISC_SIMPLE && discretization != MAMBA_DISC_ZOH)
         return fail(MAMBA_ERR_ARG, "unknown discretization %d", discretization);
-    if (discretization == MAMBA_DISC_ZOH) return fail(MAMBA_ERR_ARG, "the backward pass takes the simplified discretization only");
     if (s->dstate > 16) return fail(MAMBA_ERR_ARG, "the backward pass supports dstate <= 16");
     if (s->batch > 65535) return fail(MAMBA_ERR_ARG, "the backward pass supports batch <= 65535");
     if (s->seqlen > (1LL << 34)) return fail(MAMBA_ERR_ARG, "seqlen too large");
@@ -573,7 +624,11 @@ extern "C" int mamba_scan_bwd(const mamba_scan_shape* s, int discretization, con
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(state checkpoints)");
     }
     a.ckpt = ckpt;
-    rc = s->in_dtype == MAMBA_BF16 ? bwd_launch<uint16_t>(a, vec, st) : bwd_launch<float>(a, vec, st);
+    const bool zoh = discretization == MAMBA_DISC_ZOH;
+    if (s->in_dtype == MAMBA_BF16)
+        rc = zoh ? bwd_launch<uint16_t, true>(a, vec, st) : bwd_launch<uint16_t, false>(a, vec, st);
+    else
+        rc = zoh ? bwd_launch<float, true>(a, vec, st) : bwd_launch<float, false>(a, vec, st);
     if (ckpt) {
         e = cudaFreeAsync(ckpt, st);
         if (rc == MAMBA_OK && e != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(state checkpoints)");

@@ -3,9 +3,10 @@
 // The forward pass keeps the expanded state h[b, d, n, t] in registers and never writes it (visual
 // guide to Mamba and SSMs, section 3.4, kernel fusion); the backward pass needs it, and the guide's
 // answer (same section, "recomputation") is to recompute it from what is cheap to keep.  Here that
-// is one checkpoint of the state per 16 steps (written by a forward sweep, 1/4 of the size of u in
-// fp32 at N = 16), from which each 16-step slot is recomputed into registers and then walked in
-// reverse.
+// is one checkpoint of the state per 8 steps (written by a forward sweep, half the size of u in
+// fp32 at N = 16), from which each 8-step slot is recomputed into registers and then walked in
+// reverse.  (8 rather than 16 steps: the slot's states then fit in 128 registers per thread, and
+// four CTAs share an SM.)
 //
 // With a_t = exp(Delta_t A), h_t = a_t h_{t-1} + Delta_t B_t x_t, ypre_t = C_t h_t + D x_t and
 // y_t = ypre_t silu(z_t), the reverse walk carries mu_t = dL/dh_t from the later steps:
@@ -19,7 +20,7 @@
 //
 // Work layout: a CTA of 4 warps owns 32 channels of one batch row for the whole sequence; a warp
 // owns 8 channels, lane (c = lane % 8, g = lane / 8) holds states 4g..4g+3 of channel c (N <= 16).
-// Tiles of 32 steps of u, delta, z, dy (per channel) and B, C (per batch row) are staged in shared
+// Tiles of 16 steps of u, delta, z, dy (per channel) and B, C (per batch row) are staged in shared
 // memory by cp.async, double-buffered.  The sums over channels (dB, dC) are reduced across the 8
 // channel lanes of a warp by a shuffle reduce-scatter, across the 4 warps in shared memory, and
 // across CTAs of the same batch row with vector atomics; the sums over states (dDelta, dx, ypre)
@@ -53,7 +54,7 @@ struct BwdArgs {
     float* dD;          // [d] or null, accumulated
     float* dbias;       // [d] or null, accumulated
     float* dh0;         // [b, d, N] or null
-    float* ckpt;        // [b, nslot, d, 16] state before each 16-step slot (slot 0 unused)
+    float* ckpt;        // [b, nslot, d, 16] state before each slot of kSlot steps (slot 0 unused)
     int batch, dim, dstate;
     long long L;
     int ntile, nslot;
@@ -65,10 +66,13 @@ namespace bwd {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kCh = kWarps * 8;  // channels per CTA
-constexpr int kT = 32;           // steps per tile
-constexpr int kSlot = 16;        // steps per recomputed slot
+constexpr int kT = 16;           // steps per tile
+constexpr int kSPL = kT / 4;     // steps per lane in the per-(channel, step) phases
+constexpr int kSlot = 8;         // steps per recomputed slot (its states live in registers)
+constexpr int kSlots = kT / kSlot;
 constexpr int kNS = 16;          // state capacity (lanes per channel x 4)
-constexpr int kPad = kT + 1;     // padded row (floats) of the per-channel and per-state sums
+constexpr int kPad = kT + 1;     // padded row (floats) of the per-channel sums r[k][c][t]
+constexpr int kPartPitch = 33;   // padded row (floats) of the dB/dC partials part[t][32 columns]
 constexpr int kBcqPitch = 36;    // floats per step in the B/C step buffer (padded)
 
 template <typename TIn>
@@ -90,7 +94,7 @@ struct Layout {
     static constexpr int OFF_Q = OFF_BCQ + kT * kBcqPitch * 4;
     static constexpr int OFF_R = OFF_Q + kWarps * kT * 8 * 16;
     static constexpr int OFF_PART = OFF_R + kWarps * 3 * 8 * kPad * 4;
-    static constexpr int BYTES = OFF_PART + kWarps * kT * kPad * 4;
+    static constexpr int BYTES = OFF_PART + kWarps * kT * kPartPitch * 4;
 };
 
 // v[0..7] held by every lane; returns, in the lane with (lane & 7) == k, the sum of v[k] over the
@@ -129,7 +133,6 @@ __device__ __forceinline__ float reduce_scatter3(float v0, float v1, float v2, i
     return keep + __shfl_xor_sync(0xffffffffu, send, 8);
 }
 
-__device__ __forceinline__ float sigmoid_f(float x) { return rcp_approx(1.f + ex2_approx(-x * kLog2e)); }
 
 // Stage tile k (steps 32k .. 32k+31) of the CTA's channel rows (u, delta; z and dy when `full`) and
 // of B (and C when `full`) rows n < N.  Positions past L or past the last channel read as zero.
@@ -194,14 +197,20 @@ __device__ __forceinline__ void load_tile(uint8_t* st, const BwdArgs& a, int b, 
     }
 }
 
-// 8 consecutive staged elements (steps 8g .. 8g+7) of one row, widened to fp32.
+// kSPL consecutive staged elements (steps kSPL*g ..) of one row, widened to fp32.
 template <typename TIn>
-__device__ __forceinline__ void row8(const uint8_t* row, int g, float (&v)[8]) {
+__device__ __forceinline__ void row_steps(const uint8_t* row, int g, float (&v)[kSPL]) {
+    static_assert(kSPL == 4 || kSPL == 8, "vector widths");
     if constexpr (sizeof(TIn) == 4) {
-        const float4 p0 = reinterpret_cast<const float4*>(row)[2 * g];
-        const float4 p1 = reinterpret_cast<const float4*>(row)[2 * g + 1];
-        v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
-        v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
+#pragma unroll
+        for (int i = 0; i < kSPL / 4; ++i) {
+            const float4 p = reinterpret_cast<const float4*>(row)[(kSPL / 4) * g + i];
+            v[4 * i] = p.x; v[4 * i + 1] = p.y; v[4 * i + 2] = p.z; v[4 * i + 3] = p.w;
+        }
+    } else if constexpr (kSPL == 4) {
+        const uint2 p = reinterpret_cast<const uint2*>(row)[g];
+        v[0] = __uint_as_float(p.x << 16); v[1] = __uint_as_float(p.x & 0xffff0000u);
+        v[2] = __uint_as_float(p.y << 16); v[3] = __uint_as_float(p.y & 0xffff0000u);
     } else {
         const uint4 p = reinterpret_cast<const uint4*>(row)[g];
         const uint32_t w[4] = {p.x, p.y, p.z, p.w};
@@ -213,28 +222,31 @@ __device__ __forceinline__ void row8(const uint8_t* row, int g, float (&v)[8]) {
     }
 }
 
-// Store 8 consecutive outputs of one row at steps tg0 .. tg0+7 (those below L).
+// Store kSPL consecutive outputs of one row at steps tg0 .. (those below L).
 template <typename TIn, bool VEC>
-__device__ __forceinline__ void store8(TIn* p, long long tg0, long long L, const float (&v)[8]) {
-    if (VEC && tg0 + 8 <= L) {
+__device__ __forceinline__ void store_steps(TIn* p, long long tg0, long long L, const float (&v)[kSPL]) {
+    if (VEC && tg0 + kSPL <= L) {
         if constexpr (sizeof(TIn) == 4) {
-            reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-            reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+#pragma unroll
+            for (int i = 0; i < kSPL / 4; ++i)
+                reinterpret_cast<float4*>(p)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        } else if constexpr (kSPL == 4) {
+            reinterpret_cast<uint2*>(p)[0] = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
         } else {
             reinterpret_cast<uint4*>(p)[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
                                                         pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < kSPL; ++j)
             if (tg0 + j < L) store_out<TIn>(p + j, v[j]);
     }
 }
 
 }  // namespace bwd
 
-template <typename TIn, bool VEC>
-__global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArgs a) {
+template <typename TIn, bool VEC, bool ZOH>
+__global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArgs a) {
     using namespace bwd;
     using Lt = bwd::Layout<TIn>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -251,7 +263,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
     float* bcq = reinterpret_cast<float*>(smem + Lt::OFF_BCQ);
     float4* q = reinterpret_cast<float4*>(smem + Lt::OFF_Q) + warp * kT * 8;        // [t][c]
     float* R = reinterpret_cast<float*>(smem + Lt::OFF_R) + warp * 3 * 8 * kPad;     // [k][c][t]
-    float* part = reinterpret_cast<float*>(smem + Lt::OFF_PART) + warp * kT * kPad;  // [t][col]
+    float* part = reinterpret_cast<float*>(smem + Lt::OFF_PART) + warp * kT * kPartPitch;  // [t][col]
 
     // B/C rows of states n >= N stay zero in both stages: their states never move
     for (int i = tid; i < 2 * 2 * kNS * Lt::ROW / 16; i += kThreads) {
@@ -260,13 +272,19 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
     }
     __syncthreads();
 
-    float Aj[4], A2[4];
+    float Aj[4], A2[4], invA[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int n = 4 * g + j;
         Aj[j] = (dvalid && n < N) ? a.A[(long long)d * N + n] : 0.f;
         A2[j] = Aj[j] * kLog2e;
+        invA[j] = 1.f / Aj[j];  // hold only; infinite at A = 0, where the series branch is taken
     }
+    // Bbar x / (B x): Delta, or the hold's (exp(Delta A) - 1) / A (series for small |Delta A|)
+    auto kfac = [&](float dt, float X, float abar, int j) -> float {
+        if (!ZOH) return dt;
+        return fabsf(X) < kZohSeriesLimit ? dt * zoh_phi(X) : (abar - 1.f) * invA[j];
+    };
     const float bias_c = (dvalid && a.bias) ? a.bias[d] : 0.f;
     const float D_c = (dvalid && a.D) ? a.D[d] : 0.f;
     const long long chrow = ((long long)b * a.dim + d) * a.L;  // start of the channel's rows
@@ -280,24 +298,25 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
     float* ck = a.ckpt ? a.ckpt + (((long long)b * a.nslot) * a.dim + d) * kNS + 4 * g : nullptr;
     const long long ckstride = (long long)a.dim * kNS;  // floats between consecutive slots
 
-    // Phase A: per (channel, step) quantities of tile k for this lane's channel c, steps 8g..8g+7.
+    // Phase A: per (channel, step) quantities of tile k for this lane's channel c, steps
+    // kSPL*g .. kSPL*g + kSPL-1.
     auto phase_a = [&](const uint8_t* st, int k, bool full) {
         const long long t0 = (long long)k * kT;
-        float dl[8], uu[8], zz[8], dyv[8];
-        row8<TIn>(st + Lt::OFF_DL + row * Lt::ROW, g, dl);
-        row8<TIn>(st + Lt::OFF_U + row * Lt::ROW, g, uu);
+        float dl[kSPL], uu[kSPL], zz[kSPL], dyv[kSPL];
+        row_steps<TIn>(st + Lt::OFF_DL + row * Lt::ROW, g, dl);
+        row_steps<TIn>(st + Lt::OFF_U + row * Lt::ROW, g, uu);
         if (full) {
-            row8<TIn>(st + Lt::OFF_DY + row * Lt::ROW, g, dyv);
-            if (gate) row8<TIn>(st + Lt::OFF_Z + row * Lt::ROW, g, zz);
+            row_steps<TIn>(st + Lt::OFF_DY + row * Lt::ROW, g, dyv);
+            if (gate) row_steps<TIn>(st + Lt::OFF_Z + row * Lt::ROW, g, zz);
         }
 #pragma unroll
-        for (int j = 0; j < 8; j += 2) {
+        for (int j = 0; j < kSPL; j += 2) {
             float2 s2 = make_float2(dl[j] + bias_c, dl[j + 1] + bias_c);
             if (a.softplus) s2 = softplus2(s2);
             const float sv[2] = {s2.x, s2.y};
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const int t = 8 * g + j + i;
+                const int t = kSPL * g + j + i;
                 const bool ok = dvalid && t0 + t < a.L;
                 const float dt = ok ? sv[i] : 0.f;
                 const float x = ok ? uu[j + i] : 0.f;
@@ -308,19 +327,19 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
         }
     };
 
-    // B (and C) of the tile, one step per row of bcq: thread (t = lane, warp) moves states 4w..4w+3.
-    auto transpose_bc = [&](const uint8_t* st, bool withC) {
-        const TIn* Bs = reinterpret_cast<const TIn*>(st + Lt::OFF_B);
-        const TIn* Cs = reinterpret_cast<const TIn*>(st + Lt::OFF_C);
+    // B and C of the tile, one step per row of bcq: item (t, kind, quad) moves 4 states of B
+    // (kind 0) or C (kind 1) at step t.  (C is stale and unused in the forward sweep.)
+    auto transpose_bc = [&](const uint8_t* st) {
         constexpr int RW = Lt::ROW / (int)sizeof(TIn);
-        const int t = lane, n0 = 4 * warp;
-        float4 bq = make_float4(In<TIn>::to_f32(Bs[(n0 + 0) * RW + t]), In<TIn>::to_f32(Bs[(n0 + 1) * RW + t]),
-                                In<TIn>::to_f32(Bs[(n0 + 2) * RW + t]), In<TIn>::to_f32(Bs[(n0 + 3) * RW + t]));
-        *reinterpret_cast<float4*>(bcq + t * kBcqPitch + n0) = bq;
-        if (withC) {
-            float4 cq = make_float4(In<TIn>::to_f32(Cs[(n0 + 0) * RW + t]), In<TIn>::to_f32(Cs[(n0 + 1) * RW + t]),
-                                    In<TIn>::to_f32(Cs[(n0 + 2) * RW + t]), In<TIn>::to_f32(Cs[(n0 + 3) * RW + t]));
-            *reinterpret_cast<float4*>(bcq + t * kBcqPitch + 16 + n0) = cq;
+#pragma unroll
+        for (int r = 0; r < kT * 8 / kThreads; ++r) {
+            const int it = tid + r * kThreads;
+            const int t = it % kT, grp = it / kT;
+            const int kind = grp >> 2, n0 = 4 * (grp & 3);
+            const TIn* S = reinterpret_cast<const TIn*>(st + (kind ? Lt::OFF_C : Lt::OFF_B));
+            const float4 v = make_float4(In<TIn>::to_f32(S[(n0 + 0) * RW + t]), In<TIn>::to_f32(S[(n0 + 1) * RW + t]),
+                                         In<TIn>::to_f32(S[(n0 + 2) * RW + t]), In<TIn>::to_f32(S[(n0 + 3) * RW + t]));
+            *reinterpret_cast<float4*>(bcq + t * kBcqPitch + 16 * kind + n0) = v;
         }
     };
 
@@ -341,12 +360,12 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
                 load_tile<TIn, VEC>(st, a, b, d0, k, false);
             }
             __syncthreads();
-            transpose_bc(st, false);
+            transpose_bc(st);
             phase_a(st, k, false);
             __syncthreads();
 #pragma unroll 1
-            for (int s = 0; s < 2; ++s) {
-                const int gs = 2 * k + s;
+            for (int s = 0; s < kSlots; ++s) {
+                const int gs = kSlots * k + s;
                 if (gs >= a.nslot) break;
                 if (gs >= 1 && dvalid) *reinterpret_cast<float4*>(ck + gs * ckstride) = make_float4(h[0], h[1], h[2], h[3]);
 #pragma unroll
@@ -356,7 +375,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
                     const float4 bq = *reinterpret_cast<const float4*>(bcq + t * kBcqPitch + 4 * g);
                     const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) h[j] = fmaf(ex2_approx(qq.x * A2[j]), h[j], qq.y * bv[j]);
+                    for (int j = 0; j < 4; ++j) {
+                        const float X = qq.x * A2[j], ab = ex2_approx(X);
+                        h[j] = fmaf(ab, h[j], ZOH ? kfac(qq.x, X, ab, j) * qq.w * bv[j] : qq.y * bv[j]);
+                    }
                 }
             }
             __syncthreads();
@@ -387,13 +409,13 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
             load_tile<TIn, VEC>(st, a, b, d0, k, true);
         }
         __syncthreads();
-        transpose_bc(st, true);
+        transpose_bc(st);
         phase_a(st, k, true);
         __syncthreads();
 
 #pragma unroll 1
-        for (int s = 1; s >= 0; --s) {
-            const int gs = 2 * k + s;
+        for (int s = kSlots - 1; s >= 0; --s) {
+            const int gs = kSlots * k + s;
             if (gs >= a.nslot) continue;  // wholly past L: nothing moves there
             float h[4];
             if (gs == 0) {
@@ -412,7 +434,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
                 const float bv[4] = {bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    h[j] = fmaf(ex2_approx(qq.x * A2[j]), h[j], qq.y * bv[j]);
+                    const float X = qq.x * A2[j], ab = ex2_approx(X);
+                    h[j] = fmaf(ab, h[j], ZOH ? kfac(qq.x, X, ab, j) * qq.w * bv[j] : qq.y * bv[j]);
                     hist[i][j] = h[j];
                 }
             }
@@ -430,44 +453,57 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float ht = hist[i][j];
-                    const float bx = qq.y * bv[j];
-                    const float ah = ht - bx;  // a_t h_{t-1}
+                    const float X = qq.x * A2[j], ab = ex2_approx(X);
                     const float lam = fmaf(qq.z, cv[j], mu[j]);
                     sch = fmaf(cv[j], ht, sch);
                     v[j] = qq.z * ht;
-                    v[4 + j] = lam * qq.y;
-                    sub = fmaf(lam, bv[j], sub);
-                    sdt = fmaf(lam, fmaf(Aj[j], ah, bv[j] * qq.w), sdt);
-                    dAacc[j] = fmaf(lam * ah, qq.x, dAacc[j]);
-                    mu[j] = ex2_approx(qq.x * A2[j]) * lam;
+                    if (!ZOH) {
+                        const float ah = ht - qq.y * bv[j];  // a_t h_{t-1}
+                        v[4 + j] = lam * qq.y;
+                        sub = fmaf(lam, bv[j], sub);
+                        sdt = fmaf(lam, fmaf(Aj[j], ah, bv[j] * qq.w), sdt);
+                        dAacc[j] = fmaf(lam * ah, qq.x, dAacc[j]);
+                    } else {
+                        // h_t = a h_{t-1} + k B x: dk/dDelta = a, dk/dA = Delta^2 psi(Delta A)
+                        const float kf = kfac(qq.x, X, ab, j);
+                        const float bxs = bv[j] * qq.w;  // B x
+                        const float ah = fmaf(-kf, bxs, ht);
+                        const float dkdA = fabsf(X) < kZohSeriesLimit ? qq.x * qq.x * zoh_psi(X)
+                                                                      : (qq.x * ab - kf) * invA[j];
+                        v[4 + j] = lam * kf * qq.w;
+                        sub = fmaf(lam * kf, bv[j], sub);
+                        sdt = fmaf(lam, fmaf(Aj[j], ah, ab * bxs), sdt);
+                        dAacc[j] = fmaf(lam, fmaf(qq.x, ah, dkdA * bxs), dAacc[j]);
+                    }
+                    mu[j] = ab * lam;
                 }
-                part[t * kPad + col] = reduce_scatter8(v, lane);
+                part[t * kPartPitch + col] = reduce_scatter8(v, lane);
                 const float r3 = reduce_scatter3(sdt, sub, sch, lane);
                 if (g < 3) R[(g * 8 + c) * kPad + t] = r3;
             }
         }
         __syncwarp();
 
-        // Phase C: per (channel, step) gradients for channel c, steps 8g .. 8g+7 of the tile
+        // Phase C: per (channel, step) gradients for channel c, steps kSPL*g .. of the tile
         {
-            float dl[8], zz[8], dyv[8], o_du[8], o_dd[8], o_dz[8];
-            row8<TIn>(st + Lt::OFF_DL + row * Lt::ROW, g, dl);
-            row8<TIn>(st + Lt::OFF_DY + row * Lt::ROW, g, dyv);
-            if (gate) row8<TIn>(st + Lt::OFF_Z + row * Lt::ROW, g, zz);
+            float dl[kSPL], zz[kSPL], dyv[kSPL], o_du[kSPL], o_dd[kSPL], o_dz[kSPL];
+            row_steps<TIn>(st + Lt::OFF_DL + row * Lt::ROW, g, dl);
+            row_steps<TIn>(st + Lt::OFF_DY + row * Lt::ROW, g, dyv);
+            if (gate) row_steps<TIn>(st + Lt::OFF_Z + row * Lt::ROW, g, zz);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int t = 8 * g + j;
+            for (int j = 0; j < kSPL; ++j) {
+                const int t = kSPL * g + j;
                 const bool ok = dvalid && t0 + t < a.L;
                 const float4 qq = q[t * 8 + c];
                 const float sdt = R[(0 * 8 + c) * kPad + t];
                 const float sub = R[(1 * 8 + c) * kPad + t];
                 const float sch = R[(2 * 8 + c) * kPad + t];
                 const float sarg = dl[j] + bias_c;
-                const float gdt = a.softplus ? sdt * sigmoid_f(sarg) : sdt;
+                const float gdt = a.softplus ? sdt * sigmoid_approx(sarg) : sdt;
                 o_dd[j] = gdt;
-                o_du[j] = fmaf(sub, qq.x, qq.z * D_c);
+                o_du[j] = fmaf(sub, ZOH ? 1.f : qq.x, qq.z * D_c);  // the hold's k already holds Delta
                 if (gate) {
-                    const float sg = sigmoid_f(zz[j]);
+                    const float sg = sigmoid_approx(zz[j]);
                     const float ypre = fmaf(D_c, qq.w, sch);
                     o_dz[j] = dyv[j] * ypre * sg * fmaf(zz[j], 1.f - sg, 1.f);
                 }
@@ -477,10 +513,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
                 }
             }
             if (dvalid) {
-                const long long off = chrow + t0 + 8 * g;
-                store8<TIn, VEC>(static_cast<TIn*>(a.du) + off, t0 + 8 * g, a.L, o_du);
-                store8<TIn, VEC>(static_cast<TIn*>(a.ddelta) + off, t0 + 8 * g, a.L, o_dd);
-                if (gate && a.dz) store8<TIn, VEC>(static_cast<TIn*>(a.dz) + off, t0 + 8 * g, a.L, o_dz);
+                const long long tg0 = t0 + kSPL * g, off = chrow + tg0;
+                store_steps<TIn, VEC>(static_cast<TIn*>(a.du) + off, tg0, a.L, o_du);
+                store_steps<TIn, VEC>(static_cast<TIn*>(a.ddelta) + off, tg0, a.L, o_dd);
+                if (gate && a.dz) store_steps<TIn, VEC>(static_cast<TIn*>(a.dz) + off, tg0, a.L, o_dz);
             }
         }
         __syncthreads();
@@ -489,16 +525,16 @@ __global__ void __launch_bounds__(bwd::kThreads, 2) scan_bwd_kernel(const BwdArg
         {
             const float* P = reinterpret_cast<const float*>(smem + Lt::OFF_PART);
 #pragma unroll
-            for (int rep = 0; rep < 2; ++rep) {
-                const int gi = tid + rep * kThreads;  // 256 groups: (column, 4 steps)
-                const int colr = gi >> 3, tq = gi & 7;
+            for (int rep = 0; rep < kT * 8 / kThreads; ++rep) {
+                const int gi = tid + rep * kThreads;  // 32 columns x kT/4 groups of 4 steps
+                const int colr = gi / (kT / 4), tq = gi % (kT / 4);
                 const int kind = colr >> 4, n = colr & 15;
                 if (n < N) {
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w)
 #pragma unroll
-                        for (int tt = 0; tt < 4; ++tt) acc[tt] += P[w * kT * kPad + (tq * 4 + tt) * kPad + colr];
+                        for (int tt = 0; tt < 4; ++tt) acc[tt] += P[w * kT * kPartPitch + (tq * 4 + tt) * kPartPitch + colr];
                     const long long tg = t0 + tq * 4;
                     float* dst = (kind ? a.dB : a.dC) + ((long long)b * N + n) * a.L + tg;
                     if (VEC) {

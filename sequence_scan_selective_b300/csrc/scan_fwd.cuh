@@ -37,6 +37,7 @@
 //    the scan operator (a2, b2) o (a1, b1) = (a1 a2, a2 b1 + b2), which is associative (guide
 //    section 3.3).
 #pragma once
+#include <type_traits>
 #include <cuda.h>
 #include <stdint.h>
 
@@ -89,6 +90,16 @@ struct FwdArgs {
     int wlo;     // CTAs with this many units use the narrow u/delta/z maps (index 0)
     int nstage;  // stages in the ring
     int stage_bytes, bc_off, quad_off, scratch_off, src_off, bar_off;
+    int zoh;     // nonzero: exact zero-order hold for B (Bbar = (exp(Delta A) - 1) / A * B)
+    // Causal depthwise convolution in front of the scan (conv_w non-NULL): `u` then holds the
+    // block's pre-convolution input x and the scan consumes
+    //   u[t] = act(conv_bias[d] + sum_{k<K} conv_w[d, k] x[t-K+1+k])   (act: silu if conv_silu)
+    // with x before position 0 taken from conv_prev [batch][dim][K-1] (oldest first) or zero.
+    const float* conv_w;     // [dim][conv_k] or NULL
+    const float* conv_bias;  // [dim] or NULL
+    const float* conv_prev;  // [batch][dim][conv_k - 1] or NULL
+    int conv_k;              // 1..4
+    int conv_silu;
 };
 
 // u, delta, z maps: [0] box of wlo units' rows, [1] of (wlo+1) units' rows; B, C: box [N, TC].
@@ -278,7 +289,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const float bias = (cvalid && a.bias != nullptr) ? a.bias[dch] : 0.f;
     const float Dd = (!AGG && cvalid && a.D != nullptr) ? a.D[dch] : 0.f;
 
-    float2 A2[G / 2];
+    const bool zoh = a.zoh != 0;
+    float2 A2[G / 2], invA[G / 2];
     float2 h[G / 2];
     const float* h0 = (!AGG && cvalid && a.h0 != nullptr) ? a.h0 + row * N : nullptr;
 #pragma unroll
@@ -287,6 +299,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         A2[p].x = (cvalid && n0 < N) ? a.A[(long long)dch * N + n0] * kLog2e : 0.f;
         A2[p].y = (cvalid && n1 < N) ? a.A[(long long)dch * N + n1] * kLog2e : 0.f;
         h[p] = make_float2((h0 && n0 < N) ? h0[n0] : 0.f, (h0 && n1 < N) ? h0[n1] : 0.f);
+        // 1/A for the hold (infinite at A = 0 or a padding state: that lane of k then always takes
+        // the series branch, the other branch's value is discarded)
+        invA[p] = make_float2(1.f / ((cvalid && n0 < N) ? a.A[(long long)dch * N + n0] : 0.f),
+                              1.f / ((cvalid && n1 < N) ? a.A[(long long)dch * N + n1] : 0.f));
     }
     if (!AGG && seg > 0 && cvalid) {
         // fold the carries of segments 0 .. seg-1 in order: h <- prod Abar * h + h_end
@@ -316,11 +332,70 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         return __all_sync(0xffffffffu, mbar_wait_bounded(&qready[k % NS], (uint32_t)((k / NS) & 1), kWaitLimitNs));
     };
 
+    // ---- causal convolution in front of the scan: x of the 3 steps before the lane's window,
+    // carried from slot to slot (taps are right-aligned in a 4-tap window, unused taps are zero)
+    const bool conv = a.conv_w != nullptr;
+    float xcarry[3] = {0.f, 0.f, 0.f};
+    if (conv && cvalid) {
+        const int K = a.conv_k;
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const long long pos = t_begin - 3 + q;  // input position of carry slot q
+            if (pos >= 0)
+                xcarry[q] = In<TIn>::to_f32(static_cast<const TIn*>(a.u)[row * a.L + pos]);
+            else if (a.conv_prev != nullptr && pos >= -(K - 1))
+                xcarry[q] = a.conv_prev[row * (K - 1) + (K - 1) + pos];
+        }
+    }
+    // u of the OWN owned steps of slot i from the x tile (or global x) and the carry.
+    auto conv_slot = [&](int i, const unsigned char* st, float* uc) {
+        const int sl = i % SPC;
+        float xv[OWN];
+#pragma unroll
+        for (int j4 = 0; j4 < OWN / 4; ++j4) {
+            const int tl = g * OWN + 4 * j4;
+            const long long to = t_begin + (long long)i * kSlot + tl;
+            if (TMA) {
+                tile_load4<TIn>(st + wid * UB, c, (sl * kSlot + tl) * ES, xv + 4 * j4);
+            } else {
+                const TIn* gu = static_cast<const TIn*>(a.u) + row * a.L;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) xv[4 * j4 + j] = (cvalid && to + j < t_end) ? In<TIn>::to_f32(gu[to + j]) : 0.f;
+            }
+        }
+        float prev[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const float up = __shfl_up_sync(0xffffffffu, xv[OWN - 3 + q], CPW);  // lane group g-1
+            prev[q] = g > 0 ? up : xcarry[q];
+            xcarry[q] = __shfl_sync(0xffffffffu, xv[OWN - 3 + q], (LPC - 1) * CPW + c);
+        }
+        const int K = a.conv_k;
+        float w4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w4[q] = (cvalid && q >= 4 - K) ? a.conv_w[(long long)dch * K + q - (4 - K)] : 0.f;
+        const float cb = (cvalid && a.conv_bias != nullptr) ? a.conv_bias[dch] : 0.f;
+#pragma unroll
+        for (int j = 0; j < OWN; ++j) {
+            float acc = cb;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int p = j - 3 + q;  // window position relative to the lane's first step
+                acc = fmaf(w4[q], p >= 0 ? xv[p] : prev[3 + p], acc);
+            }
+            uc[j] = a.conv_silu ? acc * sigmoid_approx(acc) : acc;
+        }
+    };
+
     // Phase A of slot i: Delta, Delta*u of the OWN owned steps -> pairs in wsq[i & 1]; returns
     // D*u and the gate of the owned steps (skip[j], gate[j] cover steps 2j, 2j+1) for phase C.
-    auto phase_a = [&](int i, float2* skip, float2* gate) {
+    auto phase_a = [&](int i, float2* skip, float2* gate, auto mode_c) {
+        constexpr bool ZOH = (decltype(mode_c)::value & 1) != 0;
+        constexpr bool CONV = (decltype(mode_c)::value & 2) != 0;
         const int k = i / SPC, sl = i % SPC;
         const unsigned char* st = smem + (k % NS) * a.stage_bytes;
+        float uc[OWN];  // convolution outputs of the owned steps (convolution mode)
+        if constexpr (CONV) conv_slot(i, st, uc);
 #pragma unroll
         for (int j4 = 0; j4 < OWN / 4; ++j4) {
             const int tl = g * OWN + 4 * j4;                          // first step of this group in the slot
@@ -343,6 +418,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                     zv[j] = (in && has_z) ? In<TIn>::to_f32(gz[to + j]) : 0.f;
                 }
             }
+            if constexpr (CONV) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) uv[j] = uc[4 * j4 + j];
+            }
             float2 dt01 = make_float2(dv[0] + bias, dv[1] + bias);
             float2 dt23 = make_float2(dv[2] + bias, dv[3] + bias);
             if (SOFTPLUS) {
@@ -356,8 +435,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 if (nv < 3) dt23.x = 0.f;
                 dt23.y = 0.f;
             }
-            const float2 du01 = fmul2(dt01, make_float2(uv[0], uv[1]));
-            const float2 du23 = fmul2(dt23, make_float2(uv[2], uv[3]));
+            // the hold's second pair member is u itself (its Bbar needs u, not Delta*u)
+            const float2 du01 = ZOH ? make_float2(uv[0], uv[1]) : fmul2(dt01, make_float2(uv[0], uv[1]));
+            const float2 du23 = ZOH ? make_float2(uv[2], uv[3]) : fmul2(dt23, make_float2(uv[2], uv[3]));
             float4* qw = reinterpret_cast<float4*>(wsq + (i & 1) * LY::QBUF + c * kQPitch);
             qw[tl / 2] = make_float4(dt01.x, du01.x, dt01.y, du01.y);
             qw[tl / 2 + 1] = make_float4(dt23.x, du23.x, dt23.y, du23.y);
@@ -401,6 +481,39 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
     };
 
+    // Phase B with the exact zero-order hold: Bbar x = k B u with k = (exp(Delta A) - 1) / A.
+    // k B u is evaluated as (Abar - 1) (u / A) B where |Delta A| >= 1/4, and as
+    // phi(Delta A) (Delta u) B with phi(x) = (e^x - 1) / x from its Taylor series where |Delta A|
+    // < 1/4 (there Abar - 1 would lose up to 2 digits; the series' first omitted term is below
+    // 5e-8 relative).  A = 0 takes the series branch (k = Delta).
+    auto phase_b_zoh = [&](int i, float* yp) {
+        const int k = i / SPC, sl = i % SPC;
+        const float4* qrow = reinterpret_cast<const float4*>(wsq + (i & 1) * LY::QBUF + c * kQPitch);
+        const float4* bc = reinterpret_cast<const float4*>(smem + (k % NS) * a.stage_bytes + a.quad_off) +
+                           sl * kSlot * NPAIR + g * (G / 2);
+#pragma unroll
+        for (int t = 0; t < kSlot; ++t) {
+            const float4 q2 = qrow[t >> 1];  // (Delta_t, u_t, Delta_t+1, u_t+1)
+            const float dq = (t & 1) ? q2.z : q2.x, uq = (t & 1) ? q2.w : q2.y;
+            const float duq = dq * uq;
+            if (AGG) sumdt += dq;
+            float2 ya;
+#pragma unroll
+            for (int p = 0; p < G / 2; ++p) {
+                const float4 w = bc[t * NPAIR + p];
+                const float2 x = fmul2(make_float2(dq, dq), A2[p]);  // Delta A log2(e)
+                const float2 abar = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                const float2 ser = fmul2(zoh_phi2(x), make_float2(duq, duq));
+                const float2 big = fmul2(fadd2(abar, make_float2(-1.f, -1.f)), fmul2(invA[p], make_float2(uq, uq)));
+                const float2 kx = make_float2(fabsf(x.x) < kZohSeriesLimit ? ser.x : big.x,
+                                              fabsf(x.y) < kZohSeriesLimit ? ser.y : big.y);
+                h[p] = ffma2(abar, h[p], fmul2(kx, make_float2(w.x, w.y)));
+                if (!AGG) ya = p == 0 ? fmul2(make_float2(w.z, w.w), h[p]) : ffma2(make_float2(w.z, w.w), h[p], ya);
+            }
+            if (!AGG) yp[t] = ya.x + ya.y;
+        }
+    };
+
     // Phase C of slot i: sum the LPC lanes' partials of the owned steps, skip term, gate, store.
     auto phase_c = [&](int i, const float2* skip, const float2* gate) {
 #pragma unroll
@@ -429,29 +542,43 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
     };
 
-    float2 skip[OWN / 2], gate[OWN / 2];
+    // the slot loop, compiled once per mode (bit 0: hold, bit 1: convolution); the choice is made
+    // once per launch, so the default loop carries nothing of the other modes
+    auto slot_loop = [&](auto mode_c) {
+        constexpr bool ZOH = (decltype(mode_c)::value & 1) != 0;
+        float2 skip[OWN / 2], gate[OWN / 2];
 #pragma unroll 1
-    for (int i = 0; i < nslots && ok; ++i) {
-        const int k = i / SPC, sl = i % SPC;
-        if (sl == 0) {
-            ok = wait_tiles(k);
-            if (ok) ok = wait_quads(k);
-        }
-        if (!ok) break;
-        phase_a(i, skip, gate);
-        __syncwarp();
-        float yp[kSlot];
-        phase_b(i, yp);
-        __syncwarp();
-        if (sl == SPC - 1 || i + 1 == nslots) mbar_arrive(&empty[k % NS]);
-        if (!AGG) {
-            float4* yw = reinterpret_cast<float4*>(wsy + (g * CPW + c) * kYPitch);
+        for (int i = 0; i < nslots && ok; ++i) {
+            const int k = i / SPC, sl = i % SPC;
+            if (sl == 0) {
+                ok = wait_tiles(k);
+                if (ok) ok = wait_quads(k);
+            }
+            if (!ok) break;
+            phase_a(i, skip, gate, mode_c);
+            __syncwarp();
+            float yp[kSlot];
+            if constexpr (ZOH)
+                phase_b_zoh(i, yp);
+            else
+                phase_b(i, yp);
+            __syncwarp();
+            if (sl == SPC - 1 || i + 1 == nslots) mbar_arrive(&empty[k % NS]);
+            if (!AGG) {
+                float4* yw = reinterpret_cast<float4*>(wsy + (g * CPW + c) * kYPitch);
 #pragma unroll
-            for (int j = 0; j < kSlot / 4; ++j) yw[j] = make_float4(yp[4 * j], yp[4 * j + 1], yp[4 * j + 2], yp[4 * j + 3]);
+                for (int j = 0; j < kSlot / 4; ++j) yw[j] = make_float4(yp[4 * j], yp[4 * j + 1], yp[4 * j + 2], yp[4 * j + 3]);
+            }
+            __syncwarp();
+            if (!AGG) phase_c(i, skip, gate);
+            __syncwarp();
         }
-        __syncwarp();
-        if (!AGG) phase_c(i, skip, gate);
-        __syncwarp();
+    };
+    switch ((zoh ? 1 : 0) | (conv ? 2 : 0)) {
+        case 0: slot_loop(std::integral_constant<int, 0>{}); break;
+        case 1: slot_loop(std::integral_constant<int, 1>{}); break;
+        case 2: slot_loop(std::integral_constant<int, 2>{}); break;
+        default: slot_loop(std::integral_constant<int, 3>{}); break;
     }
     if (!ok) {
         if (lane == 0) atomicExch(&g_status, 1);

@@ -2,7 +2,8 @@
 //
 // Recurrent form of the discretised SSM (visual guide to Mamba and SSMs, section 2.4) used for
 // autoregressive inference with constant work per token (news write-up, "architecture" section):
-//   h <- exp(Delta A) h + Delta B x,   y = (C.h + D x) silu(z).
+//   h <- exp(Delta A) h + Delta B x,   y = (C.h + D x) silu(z)
+// (with the exact zero-order hold, Delta B x becomes (exp(Delta A) - 1) / A * B x).
 // The state [b, d, N] fp32 dominates the traffic (read + write); each thread owns 4 consecutive
 // states of one channel so that a warp streams 512 contiguous bytes of state per 128-bit access,
 // and the NP/4 lanes of a channel combine their partial C.h with warp shuffles.
@@ -27,6 +28,7 @@ struct StepArgs {
     void* y;
     int batch, dim, dstate;
     int softplus;
+    int zoh;  // nonzero: exact zero-order hold for B
 };
 
 template <typename TIn, int NP, bool VEC4>
@@ -69,8 +71,11 @@ __global__ void __launch_bounds__(256) state_step_kernel(const StepArgs a) {
         for (int i = 0; i < Q; ++i) {
             const int n = n0 + i;
             if (VEC4 || n < N) {
-                const float abar = ex2_approx(dt * (Ap[n] * kLog2e));
-                hv[i] = fmaf(abar, hv[i], du * In<TIn>::to_f32(Bp[n]));
+                const float xe = dt * (Ap[n] * kLog2e);
+                const float abar = ex2_approx(xe);
+                float bx = du;  // Bbar x / B
+                if (a.zoh) bx = fabsf(xe) < kZohSeriesLimit ? du * zoh_phi(xe) : (abar - 1.f) * (xv / Ap[n]);
+                hv[i] = fmaf(abar, hv[i], bx * In<TIn>::to_f32(Bp[n]));
                 part = fmaf(In<TIn>::to_f32(Cp[n]), hv[i], part);
             }
         }

@@ -41,6 +41,8 @@ _T_U, _T_DELTA, _T_Z, _T_B, _T_C, _T_D, _T_BIAS, _T_H0 = range(1, 9)
 _T_DX, _T_DDELTA, _T_DZ, _T_DB, _T_DC = range(11, 16)
 # backward-pass inputs: gradient at y, gradient at last_state, initial state of a scan
 _T_DY, _T_DLAST, _T_SH0 = range(21, 24)
+# causal convolution in front of the scan: weights, bias, inputs before position 0
+_T_CW, _T_CB, _T_CPREV = range(31, 34)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -245,6 +247,23 @@ def grad_inputs(cfg: ScanConfig, seqlen: Optional[int] = None) -> dict:
     return {"dy": grad_rows(cfg, rows, L).reshape(cfg.batch, cfg.dim, L),
             "dlast": state_rows(cfg, rows, "dlast").reshape(cfg.batch, cfg.dim, cfg.dstate),
             "h0": state_rows(cfg, rows, "h0").reshape(cfg.batch, cfg.dim, cfg.dstate)}
+
+
+# ----------------------------------------------------------------------------------------- convolution
+def conv_params(cfg: ScanConfig, K: int = 4) -> dict:
+    """Depthwise causal convolution of width K in front of the scan: conv_w [dim, K] and
+    conv_bias [dim], uniform on [-1/sqrt(K), 1/sqrt(K)] (the fan-in scale of a depthwise
+    convolution).  The scan's u tensor then serves as the convolution's input x."""
+    lim = 1.0 / np.sqrt(K)
+    w = _rng(cfg.seed, _T_CW, K).uniform(-lim, lim, size=(cfg.dim, K)).astype(np.float32)
+    b = _rng(cfg.seed, _T_CB, K).uniform(-lim, lim, size=cfg.dim).astype(np.float32)
+    return {"conv_w": w, "conv_bias": b}
+
+
+def conv_prev(cfg: ScanConfig, K: int = 4) -> np.ndarray:
+    """Inputs before position 0 for a convolution of width K: N(0, 1), fp32 [batch, dim, K-1]."""
+    g = _rng(cfg.seed, _T_CPREV, K)
+    return g.standard_normal((cfg.batch, cfg.dim, max(K - 1, 0)), dtype=np.float32)
 
 
 # ----------------------------------------------------------------------------------------- decode

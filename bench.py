@@ -111,11 +111,11 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per launch of the scan kernel from the committed ncu record, if it was taken on
-    the current kernel sources; otherwise None."""
+def ncu_traffic(workload: str, kernel: str = "scan_fwd"):
+    """DRAM bytes per launch of the kernel from the committed ncu record, if it was taken on the
+    current kernel sources; otherwise None."""
     try:
-        with open(os.path.join(ROOT, "profiles", f"scan_fwd_{workload}.json")) as f:
+        with open(os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")) as f:
             rec = json.load(f)
     except Exception:
         return None
@@ -360,8 +360,9 @@ def run_ours(args, cfg, rank, world, local_rank):
     sb = scan_bytes(cfg)
     achieved = sb / (scan_avg_ms * 1e-3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    plain = not args.conv and args.disc == "simple"  # the committed ncu records are of the default kernel mode
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload),
+                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload) if plain else None,
                 "peak_source": f"{kind} hbm_gbs", "kernel": "scan_fwd_kernel",
                 "algorithmic_bytes_per_launch": sb, "kernel_avg_us": round(scan_avg_ms * 1e3, 2)}
     line = {
@@ -603,8 +604,8 @@ def run_bwd(args, cfg, rank, world, local_rank):
                    "elements_per_step": elems_step, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2; two input sets alternate"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": f"{kind} hbm_gbs",
-                     "kernel": "scan_bwd_kernel", "algorithmic_bytes_per_launch": bb,
+                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload, "scan_bwd"),
+                     "peak_source": f"{kind} hbm_gbs", "kernel": "scan_bwd_kernel", "algorithmic_bytes_per_launch": bb,
                      "kernel_avg_us": round(avg_ms * 1e3, 2)},
         "clocks": clk.summary(),
         "gpu_launches": launches,

@@ -101,13 +101,19 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def source_hash() -> str:
+# the sources each profiled kernel (and the host code that plans its launches) is built from
+KERNEL_SOURCES = {
+    "scan_fwd": ("ptx.cuh", "common.cuh", "scan_fwd.cuh", "mamba_scan.cu"),
+    "scan_bwd": ("ptx.cuh", "common.cuh", "scan_bwd.cuh", "mamba_scan.cu"),
+}
+
+
+def source_hash(kernel: str = "scan_fwd") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sequence_scan_selective_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
@@ -119,7 +125,7 @@ def ncu_traffic(workload: str, kernel: str = "scan_fwd"):
             rec = json.load(f)
     except Exception:
         return None
-    if rec.get("source_hash") != source_hash():
+    if rec.get("source_hash") != source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 

@@ -17,6 +17,7 @@ NVCC_FLAGS = [
     "-O3", "-lineinfo", "-std=c++17",
     "-Xcompiler", "-fPIC", "-shared",
     "--expt-relaxed-constexpr",
+    "--split-compile", "0",  # optimise the many kernel instantiations on all host threads
 ]
 
 

@@ -132,3 +132,39 @@ def test_bwd_host_argument_checks(ms):
     assert b"dz" in lib.mamba_scan_last_error()
     assert lib.mamba_scan_bwd(*args(_shape(ms), A=None)) == -1
     assert lib.mamba_scan_bwd(*args(_shape(ms, seqlen=-3))) == -1
+
+
+def test_discretisation_and_conv_host_checks(ms):
+    lib = ms.lib()
+    P = ctypes.c_void_p
+    d = P(256)  # never dereferenced: every case below fails validation first
+    s = _shape(ms)
+    # unknown discretisation
+    assert lib.mamba_scan_fwd_ex(ctypes.byref(s), 5, d, d, d, d, d, None, None, None, 1, None, P(1 << 40), None,
+                                 None) == -1
+    assert b"discretization" in lib.mamba_scan_last_error()
+    assert lib.mamba_state_step_ex(ctypes.byref(s), -1, d, d, d, d, d, d, None, None, None, 1, d, None) == -1
+    # convolution: weights required, width 1..4
+    conv = lambda w, k: lib.mamba_scan_fwd_conv(ctypes.byref(s), 0, d, w, None, k, 1, None, d, d, d, d, None, None,
+                                                None, 1, None, P(1 << 40), None, None)
+    assert conv(None, 4) == -1 and b"conv_w" in lib.mamba_scan_last_error()
+    assert conv(d, 0) == -1 and b"conv_k" in lib.mamba_scan_last_error()
+    assert conv(d, 5) == -1 and b"conv_k" in lib.mamba_scan_last_error()
+
+
+def test_bench_byte_counts():
+    """The algorithmic byte formulas the roofline divides by, against a hand count of one shape."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    import synth
+    cfg = synth.CONFIGS["m130"]
+    b, d, n, L = 8, 1536, 16, 2048
+    # forward: u, delta, z read and y written (fp32), B and C read, A/D/bias, last_state
+    assert bench.scan_bytes(cfg) == 4 * 4 * b * d * L + 2 * 4 * b * n * L + 4 * d * (n + 2) + 4 * b * d * n
+    assert bench.scan_bytes(cfg) == 405647360
+    # backward: u, delta, z, dy read, du, ddelta, dz written; B, C read, dB, dC written (fp32);
+    # A, D, bias read and their gradients written; h0, dlast read, dh0 written
+    assert bench.bwd_bytes(cfg) == (7 * 4 * b * d * L + 4 * 4 * b * n * L + 2 * 4 * d * (n + 2)
+                                    + 3 * 4 * b * d * n)

@@ -58,3 +58,29 @@ def test_decode_inputs_subset():
         assert np.array_equal(one[k][0], allin[k][2, 1])
     h = synth.decode_state0(cfg)
     assert h.shape == (3, 8, 16) and np.array_equal(synth.decode_state0(cfg, [2])[0], h[2])
+
+
+def test_backward_inputs_are_addressable_and_seeded():
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=6, dstate=5, seqlen=21)
+    g = synth.grad_inputs(cfg)
+    assert g["dy"].shape == (2, 6, 21) and g["dlast"].shape == (2, 6, 5) and g["h0"].shape == (2, 6, 5)
+    rows = [11, 0, 7]
+    assert np.array_equal(synth.grad_rows(cfg, rows), g["dy"].reshape(-1, 21)[rows])
+    assert np.array_equal(synth.state_rows(cfg, rows, "h0"), g["h0"].reshape(-1, 5)[rows])
+    # the gradient streams differ from the input streams and from each other
+    inp = synth.scan_inputs(cfg)
+    assert not np.array_equal(g["dy"], inp["u"]) and not np.array_equal(g["h0"], g["dlast"])
+    bf = synth.grad_inputs(cfg.replace(dtype="bf16"))
+    assert bf["dy"].dtype == np.uint16 and np.array_equal(bf["dy"], synth.f32_to_bf16_bits(g["dy"]))
+
+
+def test_convolution_recipe():
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=300, seqlen=8)
+    for K in (1, 2, 4):
+        p = synth.conv_params(cfg, K)
+        lim = 1.0 / np.sqrt(K)
+        assert p["conv_w"].shape == (300, K) and p["conv_bias"].shape == (300,)
+        assert np.all(np.abs(p["conv_w"]) <= lim) and np.all(np.abs(p["conv_bias"]) <= lim)
+        assert abs(float(np.mean(p["conv_w"]))) < 0.1 * lim
+        assert np.array_equal(synth.conv_params(cfg, K)["conv_w"], p["conv_w"])  # seeded
+        assert synth.conv_prev(cfg, K).shape == (2, 300, K - 1)

@@ -197,3 +197,32 @@ def test_zoh_decode_steps_equal_scan():
                                c["delta_bias"], softplus, "f32", disc="zoh")
         assert _rel(yt, y[:, :, t]) < 1e-13
     assert _rel(state, st) < 1e-13
+
+
+@pytest.mark.parametrize("disc", ["simple", "zoh"])
+def test_lti_input_gradient_is_a_correlation(disc):
+    """Time-invariant case (constant Delta, B, C; no gate): y = K * u + D u with
+    K_k = sum_n C_n Abar_n^k Bbar_n (visual guide, sections 2.5-2.7), so the gradient of
+    sum_t dy_t y_t with respect to u_s is sum_{t >= s} dy_t K_{t-s} + D dy_s: a correlation of dy
+    with the kernel, computed here by brute force from the closed-form kernel."""
+    rng = np.random.default_rng(77)
+    dim, N, L = 3, 4, 40
+    A = -np.exp(rng.uniform(-1, 1, size=(dim, N))).astype(np.float32)
+    dt = rng.uniform(0.05, 0.4, size=dim)
+    B = rng.normal(size=(1, N, 1)).astype(np.float32).repeat(L, axis=2)
+    C = rng.normal(size=(1, N, 1)).astype(np.float32).repeat(L, axis=2)
+    D = rng.normal(size=dim).astype(np.float32)
+    u = rng.normal(size=(1, dim, L)).astype(np.float32)
+    delta = np.repeat(dt[None, :, None], L, axis=2).astype(np.float32)
+    dy = rng.normal(size=(1, dim, L))
+    g = oracle.scan_bwd(u, delta, A, B, C, dy, D, None, None, False, "f32", disc=disc)
+    for d in range(dim):
+        a = A[d].astype(np.float64)
+        step = float(delta[0, d, 0])
+        abar = np.exp(step * a)
+        kfac = step if disc == "simple" else np.expm1(step * a) / a
+        bbar = kfac * B[0, :, 0].astype(np.float64)
+        K = np.array([np.sum(C[0, :, 0] * abar ** k * bbar) for k in range(L)])
+        want = np.array([sum(dy[0, d, t] * K[t - s] for t in range(s, L)) for s in range(L)])
+        want += float(D[d]) * dy[0, d]
+        assert _rel(g["du"][0, d], want) < 1e-12, (d, _rel(g["du"][0, d], want))

@@ -548,6 +548,80 @@ def run_reference(args, cfg, rank):
     }
 
 
+def _reference_line(args, cfg, value, K, W, dt, nthreads, sample, workload):
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": args.gpus,
+        "steps": K, "warmup": W, "ms_per_step": dt / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, recipe of the workload)",
+        "config": {"workload": workload, "batch": cfg.batch, "d_inner": cfg.dim, "d_state": cfg.dstate,
+                   "seq_len": cfg.seqlen, "storage": cfg.dtype},
+        "cpu_baseline": {"value": value, "unit": "elements/s", "cores": nthreads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_reference_bwd(args, cfg, rank):
+    """Reference arm of the backward pass: the oracle's gradients on a bounded, evenly spaced
+    sample of channels (full L each), per step."""
+    if rank != 0:
+        return None
+    import oracle
+    nthreads = os.cpu_count() or 1
+    K, W = max(1, args.steps), max(0, args.warmup)
+    p = synth.params(cfg)
+    bc = synth.scan_bc(cfg)
+    L, N = cfg.seqlen, cfg.dstate
+
+    def step(rows):
+        x = synth.scan_rows(cfg, rows)
+        dy = synth.widen(synth.grad_rows(cfg, rows), cfg.dtype)
+        t = time.perf_counter()
+        oracle.scan_bwd_rows(rows, cfg.batch, cfg.dim, x["u"], x["delta"], x["z"], p["A"], p["D"],
+                             p["delta_bias"], bc["B"], bc["C"], dy, True, cfg.dtype,
+                             synth.state_rows(cfg, rows, "h0").astype(np.float64),
+                             synth.state_rows(cfg, rows, "dlast").astype(np.float64), nthreads=nthreads)
+        return time.perf_counter() - t
+
+    probe = _sample_rows(cfg, max(4 * nthreads, 16))
+    rate = len(probe) / max(step(probe), 1e-4)
+    rows = _sample_rows(cfg, max(1.0, (60.0 / (K + W)) * rate))
+    for _ in range(W):
+        step(rows)
+    dt = sum(step(rows) for _ in range(K))  # oracle time only (input generation excluded)
+    value = len(rows) * L * K / dt
+    sample = f"{len(rows)} of {cfg.batch * cfg.dim} channels per step, full L={L} backward pass"
+    return _reference_line(args, cfg, value, K, W, dt, nthreads, sample,
+                           WORKLOADS[args.workload].replace("scan+decode", "backward pass"))
+
+
+def run_reference_decode(args, cfg, rank):
+    """Reference arm of the decode workload: the oracle's decode step over a bounded sample of
+    channels, fresh inputs per step."""
+    if rank != 0:
+        return None
+    import oracle
+    nthreads = os.cpu_count() or 1
+    K, W = max(1, args.steps), max(0, args.warmup)
+    p = synth.params(cfg)
+    bsz = cfg.batch
+    n = bsz * cfg.dim
+    rows = _sample_rows(cfg, min(n, 65536))
+    rb, rd = rows // cfg.dim, rows % cfg.dim
+    state = synth.decode_state0(cfg).reshape(n, cfg.dstate)[rows].astype(np.float64)
+    steps = [synth.decode_step_inputs(cfg, s) for s in range(min(K + W, 8))]
+    dt = 0.0
+    for i in range(K + W):
+        s = steps[i % len(steps)]
+        t = time.perf_counter()
+        oracle.state_step_rows(rows, cfg.dim, state, s["x"][rb, rd], s["delta"][rb, rd], s["z"][rb, rd], p["A"],
+                               p["D"], p["delta_bias"], s["B"], s["C"], True, cfg.dtype, nthreads=nthreads)
+        if i >= W:
+            dt += time.perf_counter() - t
+    value = len(rows) * K / dt
+    sample = f"{len(rows)} of {n} channels per step, {K} steps"
+    return _reference_line(args, cfg, value, K, W, dt, nthreads, sample, WORKLOADS["decode"])
+
+
 def run_decode(args, cfg, rank, world, local_rank):
     """Consecutive decode steps (mamba_state_step) on the decode workload, each step with fresh
     x, delta, z, B, C: timed as one block of plain launches and, separately, as the same steps
@@ -724,7 +798,11 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = synth.CONFIGS[args.workload]
-    if args.impl == "reference":
+    if args.impl == "reference" and args.workload == "decode":
+        line = run_reference_decode(args, cfg, rank)
+    elif args.impl == "reference" and args.which == "bwd":
+        line = run_reference_bwd(args, cfg, rank)
+    elif args.impl == "reference":
         line = run_reference(args, cfg, rank)
     elif args.workload == "decode":
         line = run_decode(args, cfg, rank, world, local_rank)

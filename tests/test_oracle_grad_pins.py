@@ -226,3 +226,23 @@ def test_lti_input_gradient_is_a_correlation(disc):
         want = np.array([sum(dy[0, d, t] * K[t - s] for t in range(s, L)) for s in range(L)])
         want += float(D[d]) * dy[0, d]
         assert _rel(g["du"][0, d], want) < 1e-12, (d, _rel(g["du"][0, d], want))
+
+
+def test_bf16_storage_gradients_equal_widened_fp32():
+    """The gradient oracle reads bf16 storage by exact widening: bf16 inputs give the gradients of
+    the same values stored as fp32."""
+    import synth
+    c, dy, ds, softplus = _case(31, L=12)
+    c16 = {k: (None if v is None or k in ("A", "D", "delta_bias", "h0") else synth.f32_to_bf16_bits(v))
+           for k, v in c.items()}
+    for k in ("A", "D", "delta_bias", "h0"):
+        c16[k] = c[k]
+    c32 = {k: (synth.bf16_bits_to_f32(v) if k not in ("A", "D", "delta_bias", "h0") and v is not None else v)
+           for k, v in c16.items()}
+    a = oracle.scan_bwd(c16["u"], c16["delta"], c["A"], c16["B"], c16["C"], dy, c["D"], c16["z"],
+                        c["delta_bias"], softplus, "bf16", h0=c["h0"], dlast_state=ds)
+    b = oracle.scan_bwd(c32["u"], c32["delta"], c["A"], c32["B"], c32["C"], dy, c["D"], c32["z"],
+                        c["delta_bias"], softplus, "f32", h0=c["h0"], dlast_state=ds)
+    for k in a:
+        if a[k] is not None:
+            np.testing.assert_array_equal(a[k], b[k])

@@ -71,6 +71,8 @@ GRAD_MUTANTS = {
 CONV_MUTANTS = {
     "conv_taps_reversed": ("const long long s = t - (K - 1) + k;", "const long long s = t - k;"),
     "conv_previous_inputs_ignored": ("else if (x_prev_rows)", "else if (0)"),
+    "conv_previous_inputs_reversed": ("xv = x_prev_rows[i * (K - 1) + (K - 1) + s];",
+                                      "xv = x_prev_rows[i * (K - 1) - 1 - s];"),
     "conv_bias_dropped": ("double acc = conv_bias ? (double)conv_bias[d] : 0.0;", "double acc = 0.0;"),
     "conv_activation_dropped": ("u_rows[i * seqlen + t] = act_silu ? silu(acc) : acc;",
                                 "u_rows[i * seqlen + t] = acc;"),

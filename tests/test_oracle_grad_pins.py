@@ -239,10 +239,11 @@ def test_bf16_storage_gradients_equal_widened_fp32():
         c16[k] = c[k]
     c32 = {k: (synth.bf16_bits_to_f32(v) if k not in ("A", "D", "delta_bias", "h0") and v is not None else v)
            for k, v in c16.items()}
+    # one thread: the sums over channels then run in the same order in both calls
     a = oracle.scan_bwd(c16["u"], c16["delta"], c["A"], c16["B"], c16["C"], dy, c["D"], c16["z"],
-                        c["delta_bias"], softplus, "bf16", h0=c["h0"], dlast_state=ds)
+                        c["delta_bias"], softplus, "bf16", h0=c["h0"], dlast_state=ds, nthreads=1)
     b = oracle.scan_bwd(c32["u"], c32["delta"], c["A"], c32["B"], c32["C"], dy, c["D"], c32["z"],
-                        c["delta_bias"], softplus, "f32", h0=c["h0"], dlast_state=ds)
+                        c["delta_bias"], softplus, "f32", h0=c["h0"], dlast_state=ds, nthreads=1)
     for k in a:
         if a[k] is not None:
             np.testing.assert_array_equal(a[k], b[k])

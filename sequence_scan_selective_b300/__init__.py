@@ -11,6 +11,8 @@ Entry points (names as in include/mamba_scan.h):
   mamba_scan_fwd_noalloc(...)   same arguments; the library allocates no device memory
   mamba_state_step(state, x, delta, A, B, C, D, z, delta_bias, softplus, y=None)
   mamba_scan_bwd(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0=None, dlast_state=None)
+  selective_scan(u, delta, A, B, C, D, z, delta_bias, softplus, h0=None, disc="simple")
+                                 the scan as an autograd operation (forward + backward above)
 """
 from __future__ import annotations
 
@@ -349,6 +351,37 @@ def prepare_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, sof
                                  stream, out)
     keep = (shape, u, delta, A, B, C, dy, D, z, delta_bias, h0, dlast_state, out)
     return PreparedCall(_lib.mamba_scan_bwd, args, keep), out
+
+
+class _SelectiveScan(torch.autograd.Function):
+    """The scan as an autograd operation: the forward pass is mamba_scan_fwd (or its _state / _ex
+    forms), the backward pass mamba_scan_bwd, which recomputes the states instead of keeping them
+    (only the inputs are saved)."""
+
+    @staticmethod
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, h0, softplus, disc):
+        y, last_state = mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0, disc=disc)
+        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias, h0)
+        ctx.softplus, ctx.disc = softplus, disc
+        return y, last_state
+
+    @staticmethod
+    def backward(ctx, dy, dlast_state):
+        u, delta, A, B, C, D, z, delta_bias, h0 = ctx.saved_tensors
+        dy = torch.zeros_like(u) if dy is None else dy.contiguous()
+        dlast_state = None if dlast_state is None else dlast_state.contiguous()
+        g = mamba_scan_bwd(u, delta, A, B, C, dy, D, z, delta_bias, ctx.softplus, h0=h0, dlast_state=dlast_state,
+                           disc=ctx.disc)
+        like = lambda t, ref: None if t is None else t.to(ref.dtype)  # dB, dC come as fp32
+        return (g["du"], g["ddelta"], g["dA"], like(g["dB"], B), like(g["dC"], C), g["dD"], g["dz"],
+                g["ddelta_bias"], g["dh0"], None, None)
+
+
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, disc="simple"):
+    """(y, last_state) of the scan, differentiable with respect to u, delta, A, B, C, D, z,
+    delta_bias and h0 (backward pass: mamba_scan_bwd, d_state <= 16).  Arguments as for
+    mamba_scan_fwd."""
+    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, h0, bool(softplus), disc)
 
 
 def device_status(stream=None) -> None:

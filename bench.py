@@ -4,8 +4,10 @@
 One step = one pass of the whole path over one batch of the workload: the fused forward scan over
 the sequence (Delta map, discretisation, recurrence, readout, skip, gate, final state) followed by
 one recurrent decode step that continues from the scan's final state.  Default workload: the
-Mamba-130M layer shape (batch 8, d_inner 1536, N 16, L 2048, fp32); `--workload b14` selects the
-Mamba-1.4B layer shape (batch 4, d_inner 4096, bf16 inputs, fp32 state).
+Mamba-1.4B layer shape (batch 4, d_inner 4096, N 16, L 2048, bf16 inputs, fp32 state); `--workload
+m130` selects the Mamba-130M layer shape (batch 8, d_inner 1536, fp32).  The default line also
+times the million-token scan (batch 1, d_inner 1536, N 16, L 2^20, fp32) and reports its
+per-element rate next to the main workload's scan rate (`long_sequence`).
 
 Prints one JSON line (rank 0).  `value` = elements (batch * d_inner * (L + 1)) per second over all
 ranks, device-timed with CUDA events, inputs resident in HBM.  `e2e` = the same metric through the
@@ -51,7 +53,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="m130")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="b14")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the million-token scan that the b14 and m130 lines report beside their own rate")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -390,11 +394,66 @@ def run_ours(args, cfg, rank, world, local_rank):
         "gpu_launches": launches,
         "e2e": e2e,
     }
+    if not args.no_long and plain and args.workload in ("b14", "m130"):
+        del sets, scans
+        line["long_sequence"] = long_sequence_rate(dev, local_rank, cfg, scan_avg_ms, peak, kind)
     if rank == 0 and not args.no_cpu_baseline and not args.conv and args.disc == "simple":
         line["cpu_baseline"] = cpu_baseline(cfg, inp, dec)
     if dist:
         dist.destroy_process_group()
     return line
+
+
+def long_sequence_rate(dev, local_rank, main_cfg, main_scan_ms, peak, peak_kind, steps=3, warmup=2):
+    """The million-token scan (batch 1, d_inner 1536, N 16, L 2^20, fp32) through the same
+    prepared entry point: inputs generated block by block straight into device memory (25.9 GB of
+    algorithmic traffic per scan, far beyond L2), `warmup` untimed scans, then `steps` scans timed
+    one by one with CUDA events on the launching stream.  Its per-element rate is reported next to
+    the main workload's scan rate (elements b*d*L per second of the scan launch alone)."""
+    import torch
+    import sequence_scan_selective_b300 as ms
+
+    cfg = synth.CONFIGS["long"]
+    n, L = cfg.batch * cfg.dim, cfg.seqlen
+    d = {k: torch.empty((cfg.batch, cfg.dim, L), device=dev, dtype=torch.float32) for k in ("u", "delta", "z")}
+    for lo in range(0, n, 64):
+        hi = min(n, lo + 64)
+        r = synth.scan_rows(cfg, range(lo, hi))
+        for k in ("u", "delta", "z"):
+            d[k].view(n, L)[lo:hi].copy_(torch.from_numpy(r[k]))
+    for k, v in synth.scan_bc(cfg).items():
+        d[k] = to_torch(v, "f32", dev)
+    p = {k: to_torch(v, "f32", dev) for k, v in synth.params(cfg).items()}
+    call, y, st = ms.prepare_scan_fwd(d["u"], d["delta"], p["A"], d["B"], d["C"], p["D"], d["z"], p["delta_bias"],
+                                      True)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    ms.device_status()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    n0 = ms.launch_count()
+    with ClockSampler(local_rank) as clk:
+        clk.mark(True)
+        for a, b in evs:
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        clk.mark(False)
+    launches = ms.launch_count() - n0
+    ms.device_status()
+    avg_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    rate = n * L / (avg_ms * 1e-3)
+    main_rate = main_cfg.batch * main_cfg.dim * main_cfg.seqlen / (main_scan_ms * 1e-3)
+    gbs = scan_bytes(cfg) / (avg_ms * 1e-3) / 1e9
+    del d, y, st, call
+    torch.cuda.empty_cache()
+    return {"workload": WORKLOADS["long"].replace("scan+decode", "scan"), "steps": steps, "warmup": warmup,
+            "ms_per_scan": avg_ms, "elements_per_s": rate, "main_scan_elements_per_s": main_rate,
+            "ratio_to_main_scan_rate": rate / main_rate, "launches_per_scan": launches / steps,
+            "algorithmic_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
+            "peak_source": f"{peak_kind} hbm_gbs", "clocks": clk.summary()}
 
 
 def aggregate_ranks(dist, device, total_ms: float, scan_avg_ms: float, launches: int):

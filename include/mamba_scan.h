@@ -168,7 +168,9 @@ int mamba_state_step_ex(const mamba_scan_shape* s, int discretization, float* st
  *    ((segments - 1) * batch * dim * dstate * 8 bytes) is rejected with MAMBA_ERR_ARG and a message
  *    stating both sizes; nothing is launched.
  *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *    with that device current, then caches it; make that first call before any stream capture.
+ *    with that device current, then caches it under the unique id of the CUDA context that made
+ *    the call; a call from another context, or after cudaDeviceReset, repeats the lookup.  Make
+ *    the first call in each context before any stream capture.
  *  - All calls on a device share the one array and it keeps the last call's contents.  Every
  *    carry a call reads is written earlier in the same call, so nothing needs clearing.  Calls
  *    that can run at the same time on the GPU (for example on two streams with no ordering between

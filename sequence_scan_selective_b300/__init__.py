@@ -380,7 +380,12 @@ class _SelectiveScan(torch.autograd.Function):
 def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, disc="simple"):
     """(y, last_state) of the scan, differentiable with respect to u, delta, A, B, C, D, z,
     delta_bias and h0 (backward pass: mamba_scan_bwd, d_state <= 16).  Arguments as for
-    mamba_scan_fwd."""
+    mamba_scan_fwd.  A d_state above 16 is refused here, before the forward pass, when a gradient
+    would be needed."""
+    ins = (u, delta, A, B, C, D, z, delta_bias, h0)
+    if torch.is_grad_enabled() and any(t is not None and t.requires_grad for t in ins) and A.shape[1] > 16:
+        raise ValueError(f"selective_scan: the backward pass supports d_state <= 16, got {A.shape[1]}; "
+                         "call mamba_scan_fwd for a forward pass without gradients")
     return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, h0, bool(softplus), disc)
 
 

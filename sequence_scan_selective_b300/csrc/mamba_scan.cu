@@ -478,24 +478,61 @@ extern "C" int mamba_scan_fwd_conv(const mamba_scan_shape* s, int discretization
 // device array, so it exists on every device that loads this library, from module load to exit.
 static __device__ __align__(256) float2 g_noalloc_scratch[MAMBA_NOALLOC_SCRATCH_BYTES / sizeof(float2)];
 
-// Device address of g_noalloc_scratch on the current device.  In host code the symbol is only a
-// host-side stand-in, so its device address is looked up once per device (with that device
-// current) and cached.
+// Unique id of the CUDA context current on this thread (0 if none is current or the driver
+// entry points are missing).  Ids are never reused within a process, so an id stays tied to one
+// context even after cudaDeviceReset replaces the primary context at the same address.
+static unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of g_noalloc_scratch in the CUDA context current on this thread.  In host code
+// the symbol is only a host-side stand-in, so its device address is looked up with
+// cudaGetSymbolAddress the first time a context calls (the set-up of that device in that
+// context) and cached under the context's unique id; a reset device or another context (driver
+// API) gets a fresh lookup instead of a stale address.
 static int noalloc_scratch(float2** out) {
     static std::mutex mu;
-    static float2* addr[256] = {};
+    struct Entry {
+        unsigned long long ctx;
+        float2* addr;
+    };
+    static Entry cache[256] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= 256) return fail(MAMBA_ERR_ARG, "device ordinal %d out of range", dev);
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-        addr[dev] = static_cast<float2*>(p);
+    unsigned long long ctx = current_context_id();
+    if (ctx != 0 && cache[dev].ctx == ctx && cache[dev].addr != nullptr) {
+        *out = cache[dev].addr;
+        return MAMBA_OK;
     }
-    *out = addr[dev];
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // makes the device's context current if needed
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    if (ctx == 0) ctx = current_context_id();
+    cache[dev].ctx = ctx;  // 0 (no id available) never matches, so the lookup then repeats
+    cache[dev].addr = static_cast<float2*>(p);
+    *out = cache[dev].addr;
     return MAMBA_OK;
 }
 

@@ -90,16 +90,19 @@ def test_state_handoff_scan_then_decode(ms):
     assert rel_err(from_dev(last), st_ref) <= TOL["bf16"]
 
 
-def test_decode_workload_full_size(ms):
-    """128 x 5120 x 16, bf16 inputs, fp32 state, 1000 successive steps; sampled channels vs oracle."""
-    cfg = synth.CONFIGS["decode"]
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_decode_workload_full_size(ms, dtype):
+    """128 x 5120 x 16, fp32 state, 1000 successive steps with bf16 inputs (the primary reading of
+    the decode workload) and with fp32 inputs; sampled channels vs oracle."""
+    cfg = synth.CONFIGS["decode"].replace(dtype=dtype)
     p = synth.params(cfg)
     pd = _params_dev(p)
     allin = synth.decode_inputs(cfg)
     dev = {k: to_dev(v, cfg.dtype) for k, v in allin.items()}
     h0 = synth.decode_state0(cfg)
     st = torch.from_numpy(h0).cuda()
-    ys = torch.empty((cfg.decode_steps, cfg.batch, cfg.dim), device="cuda", dtype=torch.bfloat16)
+    ys = torch.empty((cfg.decode_steps, cfg.batch, cfg.dim), device="cuda",
+                     dtype=torch.bfloat16 if dtype == "bf16" else torch.float32)
     for s in range(cfg.decode_steps):
         ms.mamba_state_step(st, dev["x"][s], dev["delta"][s], pd["A"], dev["B"][s], dev["C"][s], pd["D"],
                             dev["z"][s], pd["delta_bias"], True, y=ys[s])
@@ -117,3 +120,5 @@ def test_decode_workload_full_size(ms):
     sg = from_dev(st.reshape(-1, cfg.dstate)[idx])
     assert rel_err(yg, y_ref) <= TOL[cfg.dtype]
     assert rel_err(sg, st_ref) <= TOL[cfg.dtype]
+    del dev, st, ys
+    torch.cuda.empty_cache()

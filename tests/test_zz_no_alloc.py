@@ -7,6 +7,8 @@ CUDA allocator.  These tests call that entry point through the C ABI on shapes t
 sequence, and check its results against mamba_scan_fwd's, on two calls in a row (the scratch array
 is shared and keeps the previous call's contents).  This file is collected last on purpose.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -27,19 +29,58 @@ def _args(d):
     return (d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], True)
 
 
+class _DefaultPool:
+    """The current device's default memory pool (the one cudaMallocAsync draws from), through the
+    driver API: its high-water mark of memory in use, which a test can reset to zero."""
+
+    USED_MEM_HIGH = 8  # CU_MEMPOOL_ATTR_USED_MEM_HIGH
+
+    def __init__(self):
+        self.cu = ctypes.CDLL("libcuda.so.1")
+        assert self.cu.cuInit(0) == 0
+        dev = ctypes.c_int()
+        assert self.cu.cuDeviceGet(ctypes.byref(dev), torch.cuda.current_device()) == 0
+        self.pool = ctypes.c_void_p()
+        assert self.cu.cuDeviceGetDefaultMemPool(ctypes.byref(self.pool), dev) == 0
+
+    def reset_high(self):
+        zero = ctypes.c_uint64(0)
+        assert self.cu.cuMemPoolSetAttribute(self.pool, self.USED_MEM_HIGH, ctypes.byref(zero)) == 0
+
+    def high(self) -> int:
+        v = ctypes.c_uint64(0)
+        assert self.cu.cuMemPoolGetAttribute(self.pool, self.USED_MEM_HIGH, ctypes.byref(v)) == 0
+        return int(v.value)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_noalloc_matches_regular_entry_point_twice(ms, dtype):
     # 32 channels and 8192 steps: too few channels for the GPU, so the time axis is split into
     # segments and the carries go through the scratch array
+    pool = _DefaultPool()
     outs = []
     for call, seed in enumerate((41, 42)):
         cfg = synth.CONFIGS["long"].replace(batch=1, dim=32, seqlen=8192, dtype=dtype, seed=seed)
         d = dev_inputs(synth.scan_inputs(cfg), dtype)
-        y_ref, st_ref = ms.mamba_scan_fwd(*_args(d))
+        y_ref = torch.empty_like(d["u"])
+        st_ref = torch.empty((cfg.batch, cfg.dim, cfg.dstate), device="cuda")
         y = torch.full_like(y_ref, float("nan"))
         st = torch.full_like(st_ref, float("nan"))
+        torch.cuda.synchronize()
+        # positive control: the regular entry point takes the carries from the stream-ordered
+        # allocator, so the pool's high-water mark rises; two launches show the split ran
+        pool.reset_high()
+        n0 = ms.launch_count()
+        ms.mamba_scan_fwd(*_args(d), y=y_ref, last_state=st_ref)
+        torch.cuda.synchronize()
+        assert ms.launch_count() - n0 == 2
+        assert pool.high() > 0
+        pool.reset_high()
+        n0 = ms.launch_count()
         ms.mamba_scan_fwd_noalloc(*_args(d), y=y, last_state=st)
         torch.cuda.synchronize()
+        assert ms.launch_count() - n0 == 2, "the shape no longer splits the time axis"
+        assert pool.high() == 0, "the allocation-free entry point drew memory from the pool"
         ms.device_status()
         assert rel_err(from_dev(y), from_dev(y_ref)) <= TOL[dtype], f"call {call}"
         assert rel_err(from_dev(st), from_dev(st_ref)) <= TOL[dtype], f"call {call}"

@@ -30,8 +30,8 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16 = 0, 1
-_DT = {"f32": F32, "bf16": BF16}
+F32, BF16, F64 = 0, 1, 2
+_DT = {"f32": F32, "bf16": BF16, "f64": F64}
 
 
 _P, _I, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong
@@ -85,7 +85,9 @@ def _c(a, dtype):
 
 
 def _storage(a, dt):
-    return None if a is None else np.ascontiguousarray(a, dtype=np.uint16 if dt == BF16 else np.float32)
+    if a is None:
+        return None
+    return np.ascontiguousarray(a, dtype={BF16: np.uint16, F32: np.float32, F64: np.float64}[dt])
 
 
 def scan_rows(rows, dim, u_rows, delta_rows, z_rows, A, D, delta_bias, B, C, softplus=True,

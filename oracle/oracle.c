@@ -39,8 +39,10 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_F64 2 /* inputs already in double (e.g. a convolution computed by this oracle) */
 
 static double widen(const void* p, long long i, int dtype) {
+    if (dtype == ORACLE_F64) return ((const double*)p)[i];
     if (dtype == ORACLE_BF16) {
         uint32_t bits = ((uint32_t)((const uint16_t*)p)[i]) << 16;
         float f;
@@ -77,7 +79,8 @@ int oracle_version(void) { return 2; }
  * Forward selective scan over a list of channels ("rows").
  *
  * Row i is channel (row_b[i], row_d[i]).  u_rows, delta_rows, z_rows hold that channel's inputs,
- * [nrows, seqlen] in in_dtype.  A [dim, dstate] fp32, D and delta_bias [dim] fp32 (either may be
+ * [nrows, seqlen] in in_dtype (fp32, bf16, or double: ORACLE_F64 takes values that are already
+ * double, such as this oracle's own convolution output).  A [dim, dstate] fp32, D and delta_bias [dim] fp32 (either may be
  * NULL for zero); B, C [batch, dstate, seqlen] in in_dtype; z_rows may be NULL (no gate).
  * h0_rows [nrows, dstate] is the initial state (NULL = zero).
  * Outputs: y_rows [nrows, seqlen] and state_rows [nrows, dstate] (may be NULL), fp64.
@@ -91,7 +94,7 @@ int oracle_scan_rows_ex(long long nrows, const int* row_b, const int* row_d, int
     if (nrows < 0 || dim <= 0 || dstate <= 0 || dstate > 256 || seqlen < 0) return -1;
     if (nrows > 0 && (!row_b || !row_d || !u_rows || !delta_rows || !A || !B || !C || !y_rows))
         return -1;
-    if (in_dtype != ORACLE_F32 && in_dtype != ORACLE_BF16) return -1;
+    if (in_dtype != ORACLE_F32 && in_dtype != ORACLE_BF16 && in_dtype != ORACLE_F64) return -1;
 #ifdef _OPENMP
     if (nthreads <= 0) nthreads = omp_get_max_threads();
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)

@@ -1,7 +1,7 @@
 """GPU parity of the scan with the block's causal depthwise convolution fused in front of it
-(mamba_scan_fwd_conv) against the fp64 oracle: the oracle's convolution gives u, the oracle's scan
-consumes it (u rounded once to fp32, as the kernel keeps it; bf16 inputs are widened exactly).
-Tolerances as for the scan: 1e-4 (fp32 storage), 2e-2 (bf16 storage).
+(mamba_scan_fwd_conv) against the fp64 oracle: the oracle's convolution gives u in fp64 and the
+oracle's scan consumes it as it is (every other input widened exactly to fp64).  Tolerances as for
+the scan: 1e-4 (fp32 storage), 2e-2 (bf16 storage).
 """
 import numpy as np
 import pytest
@@ -20,8 +20,8 @@ def ms():
     return m
 
 
-def _f32(a, dtype):
-    return synth.widen(a, dtype).astype(np.float32)
+def _f64(a, dtype):
+    return synth.widen(a, dtype)
 
 
 def _oracle(inp, cp, dtype, silu, prev=None, h0=None, disc="simple", rows=None):
@@ -32,9 +32,9 @@ def _oracle(inp, cp, dtype, silu, prev=None, h0=None, disc="simple", rows=None):
     K = cp["conv_w"].shape[1]
     u = oracle.causal_conv_rows(rows, dim, r(inp["u"], L)[rows], cp["conv_w"], cp["conv_bias"], silu, dtype,
                                 None if prev is None else r(prev, K - 1)[rows].astype(np.float64))
-    return oracle.scan_rows(rows, dim, u.astype(np.float32), _f32(r(inp["delta"], L)[rows], dtype),
-                            _f32(r(inp["z"], L)[rows], dtype), inp["A"], inp["D"], inp["delta_bias"],
-                            _f32(inp["B"], dtype), _f32(inp["C"], dtype), True, "f32",
+    return oracle.scan_rows(rows, dim, u, _f64(r(inp["delta"], L)[rows], dtype),
+                            _f64(r(inp["z"], L)[rows], dtype), inp["A"], inp["D"], inp["delta_bias"],
+                            _f64(inp["B"], dtype), _f64(inp["C"], dtype), True, "f64",
                             None if h0 is None else r(h0, inp["A"].shape[1])[rows].astype(np.float64), disc=disc)
 
 

@@ -304,6 +304,23 @@ def test_bf16_widening_matches_fp32():
     assert np.array_equal(y16, y32) and np.array_equal(s16, s32)
 
 
+def test_f64_inputs_match_fp32_and_keep_extra_bits():
+    """Inputs given as doubles: on fp32-representable values the run equals the fp32 run exactly;
+    an input perturbed below fp32 resolution changes the result (the doubles are not rounded)."""
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=5, seqlen=30, seed=3)
+    inp = synth.scan_inputs(cfg)
+    w = {k: inp[k].astype(np.float64) for k in ("u", "delta", "B", "C", "z")}
+    y32, s32 = oracle.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                           inp["delta_bias"], True, "f32")
+    y64, s64 = oracle.scan(w["u"], w["delta"], inp["A"], w["B"], w["C"], inp["D"], w["z"],
+                           inp["delta_bias"], True, "f64")
+    assert np.array_equal(y32, y64) and np.array_equal(s32, s64)
+    u2 = w["u"].copy()
+    u2[0, 0, 0] += 1e-12
+    y2, _ = oracle.scan(u2, w["delta"], inp["A"], w["B"], w["C"], inp["D"], w["z"], inp["delta_bias"], True, "f64")
+    assert not np.array_equal(y2, y64)
+
+
 def test_rows_subset_equals_full():
     cfg = synth.CONFIGS["m130"].replace(batch=3, dim=10, seqlen=50)
     inp = synth.scan_inputs(cfg)

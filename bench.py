@@ -65,8 +65,13 @@ def parse():
                     help="fwd pass: fuse a causal depthwise convolution of this width (1-4) in front of the scan")
     ap.add_argument("--disc", choices=["simple", "zoh"], default="simple",
                     help="discretisation of B in the forward scan and decode step")
+    ap.add_argument("--kernel", choices=["auto", "lane", "warp"], default="auto",
+                    help="forward scan kernel: the library's choice, one channel per lane, or four lanes per channel")
     ap.add_argument("--decode-inputs", type=int, default=200,
                     help="decode workload: distinct pre-generated steps of inputs, cycled")
+    ap.add_argument("--decode-states", type=int, default=6,
+                    help="decode workload: state buffers cycled in the second timing (their total is "
+                         "kept above twice the L2 size, so the state streams from HBM)")
     return ap.parse_args()
 
 
@@ -111,6 +116,8 @@ def measured_peaks():
 # the sources each profiled kernel (and the host code that plans its launches) is built from
 KERNEL_SOURCES = {
     "scan_fwd": ("ptx.cuh", "common.cuh", "scan_fwd.cuh", "mamba_scan.cu"),
+    "scan_fwd_cl": ("ptx.cuh", "common.cuh", "scan_fwd.cuh", "scan_fwd_cl.cuh", "mamba_scan.cu"),
+    "state_step": ("ptx.cuh", "common.cuh", "state_step.cuh", "mamba_scan.cu"),
     "scan_bwd": ("ptx.cuh", "common.cuh", "scan_bwd.cuh", "mamba_scan.cu"),
 }
 
@@ -374,9 +381,11 @@ def run_ours(args, cfg, rank, world, local_rank):
     achieved = sb / (scan_avg_ms * 1e-3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     plain = not args.conv and args.disc == "simple"  # the committed ncu records are of the default kernel mode
+    kname = fwd_kernel_name(args, cfg)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload) if plain else None,
-                "peak_source": f"{kind} hbm_gbs", "kernel": "scan_fwd_kernel",
+                "frac": round(achieved / peak, 4),
+                "traffic": ncu_traffic(args.workload, kname.replace("_kernel", "")) if plain else None,
+                "peak_source": f"{kind} hbm_gbs", "kernel": kname,
                 "algorithmic_bytes_per_launch": sb, "kernel_avg_us": round(scan_avg_ms * 1e3, 2)}
     line = {
         "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": K, "warmup": W,
@@ -388,6 +397,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                            + (f"; causal conv (width {args.conv}) fused in front of the scan" if args.conv else "")
                            + ("; exact zero-order hold" if args.disc == "zoh" else ""),
                    "elements_per_step": elems_step, "parallelism": f"replicas x{world}",
+                   "scan_kernel": kname,
                    "l2": "inputs larger than L2; two input sets alternate"},
         "roofline": roofline,
         "clocks": clk.summary(),
@@ -454,6 +464,15 @@ def long_sequence_rate(dev, local_rank, main_cfg, main_scan_ms, peak, peak_kind,
             "ratio_to_main_scan_rate": rate / main_rate, "launches_per_scan": launches / steps,
             "algorithmic_GBps": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
             "peak_source": f"{peak_kind} hbm_gbs", "clocks": clk.summary()}
+
+
+def fwd_kernel_name(args, cfg) -> str:
+    """The forward kernel the library picks for this run (the channel-per-lane kernel for N <= 16,
+    unless --kernel says otherwise)."""
+    lane_ok = cfg.dstate <= 16
+    if args.kernel == "warp" or not lane_ok:
+        return "scan_fwd_kernel"
+    return "scan_fwd_cl_kernel"
 
 
 def aggregate_ranks(dist, device, total_ms: float, scan_avg_ms: float, launches: int):
@@ -745,6 +764,28 @@ def run_decode(args, cfg, rank, world, local_rank):
     ev[3].record(stream)
     torch.cuda.synchronize()
     graph_ms = ev[2].elapsed_time(ev[3]) / (reps * S)
+    # the same steps on R state buffers used in turn (R independent decode streams, each step
+    # still one launch over the whole batch): the states total more than twice the L2, so every
+    # step streams its state from HBM and back
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    sbytes = state.numel() * 4
+    R = max(args.decode_states, -(-2 * l2 // sbytes) + 1)
+    rstates = [state.clone() for _ in range(R)]
+    rcalls = [ms.prepare_state_step(rstates[r], d["x"][i], d["delta"][i], p["A"], d["B"][i], d["C"][i], p["D"],
+                                    d["z"][i], p["delta_bias"], True, y=y[i])[0]
+              for r in range(R) for i in range(min(S, 8))]
+    nrc = len(rcalls)
+    for i in range(2 * R):
+        rcalls[i % nrc]()
+    torch.cuda.synchronize()
+    ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev2[0].record(stream)
+    for i in range(K):  # step i uses state buffer i % R
+        rcalls[(i % R) * min(S, 8) + (i // R) % min(S, 8)]()
+    ev2[1].record(stream)
+    torch.cuda.synchronize()
+    rot_ms = ev2[0].elapsed_time(ev2[1]) / K
+    del rstates, rcalls
     total_ms, avg_ms, launches = aggregate_ranks(dist, dev, total_ms, total_ms / K, launches)
     elems_step = cfg.batch * cfg.dim
     peaks, kind = measured_peaks()
@@ -765,6 +806,11 @@ def run_decode(args, cfg, rank, world, local_rank):
                      "kernel_avg_us": round(avg_ms * 1e3, 3)},
         "graph": {"us_per_step": round(graph_ms * 1e3, 3), "steps_per_graph": S,
                   "elements_per_s": elems_step * world / (graph_ms * 1e-3)},
+        "rotating_states": {"state_buffers": R, "state_bytes_total": R * sbytes, "l2_bytes": l2,
+                            "us_per_step": round(rot_ms * 1e3, 3),
+                            "elements_per_s": elems_step * world / (rot_ms * 1e-3),
+                            "achieved_GBps": round(sb / (rot_ms * 1e-3) / 1e9, 1),
+                            "frac_of_hbm": round(sb / (rot_ms * 1e-3) / 1e9 / peak, 4)},
         "clocks": clk.summary(),
         "gpu_launches": launches,
         "e2e": None,
@@ -853,6 +899,8 @@ def run_bwd(args, cfg, rank, world, local_rank):
 
 def main():
     args = parse()
+    if args.kernel != "auto":
+        os.environ["MAMBA_SCAN_KERNEL"] = args.kernel
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

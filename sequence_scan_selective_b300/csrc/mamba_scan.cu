@@ -15,7 +15,7 @@
 #include "mamba_scan.h"
 #include "common.cuh"
 #include "scan_fwd.cuh"
-#include "scan_fwd_tm.cuh"
+#include "scan_fwd_cl.cuh"
 #include "scan_bwd.cuh"
 #include "state_step.cuh"
 
@@ -88,16 +88,102 @@ struct FwdPlan {
     int stage_bytes, bc_off, quad_off, scratch_off, src_off, bar_off, smem_bytes;
 };
 
-// Work split.  Units (8 channels of one batch row, one consumer warp each) are the grain.  The
-// time axis is split into segments only when the units alone cannot give every SM several warps
-// (a split costs one extra pass over delta, u and B for all but the last segment).  Each
-// (segment, batch row) gets kcta CTAs with an even share of its units, so that the grid is about
-// one CTA per SM and the per-SM work differs by at most one unit.
-template <typename TIn, int NP, bool TM, int LPC>
-static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
+// Two forward kernels share the plan format and the split of the time axis:
+//  * scan_fwd_cl_kernel (channel per lane, N <= 16): work unit = 32 channels of one batch row,
+//    one consumer warp each, at most cl::kMaxWarps per CTA (one per SM sub-partition);
+//  * scan_fwd_kernel (4 lanes per channel, any N <= 64, also the exact hold and the fused
+//    convolution): work unit = 8 channels of one batch row.
+enum class FwdKernel { kChannelLane, kWarp };
+
+static int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Segments and CTAs for the channel-per-lane kernel.  A CTA runs one (segment, batch row) range of
+// at most wcap units, every warp on its own SM sub-partition, so a launch takes about
+// waves * segment length; a split adds the aggregate launch (about 3/4 of a segment's work, for
+// all but the last segment).  The segment count minimises that estimate.
+template <typename TIn, int NP>
+static int plan_cl(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     constexpr int TC = Chunk<TIn>::TC;
-    constexpr int CPW = TM ? kUnitCh : Layout<LPC>::CPW;  // channels per work unit
-    constexpr int UB = CPW * 128;                          // u/delta/z tile bytes per unit and chunk
+    constexpr int TILE = 32 * cl::kRowBytes;
+    const long long L = s->seqlen;
+    p.upr = (s->dim + 31) / 32;
+    auto stage_of = [&](int w) { return round_up(3 * w * TILE + 2 * NP * cl::kRowBytes + TC * cl::Quads<NP>::PITCH, 1024); };
+    auto smem_of = [&](int w, int ns) { return ns * stage_of(w) + w * 2 * cl::kYTile + (3 * ns + 1) * 8 + 1024; };
+    int wcap = cl::kMaxWarps;
+    while (wcap > 1 && smem_of(wcap, 2) > kSmemLimit) --wcap;
+    const int wforce = env_int("MAMBA_SCAN_WMAX", 0);
+    if (wforce > wcap) return fail(MAMBA_ERR_ARG, "MAMBA_SCAN_WMAX above %d", wcap);
+    const int wlim = wforce > 0 ? wforce : wcap;
+    auto kcta_of = [&](long long rows) {
+        long long k = wforce > 0 ? (p.upr + wforce - 1) / wforce : (rows >= nsm ? 1 : nsm / rows);
+        if (k > p.upr) k = p.upr;
+        const long long kmin = (p.upr + wlim - 1) / wlim;
+        if (k < kmin) k = kmin;
+        return k < 1 ? 1LL : k;
+    };
+    long long maxseg = L / (8LL * TC);
+    if (maxseg < 1) maxseg = 1;
+    if (maxseg > 4096) maxseg = 4096;
+    long long best = 1;
+    const long long want = env_int("MAMBA_SCAN_NSEG", 0);
+    if (want > 0) {
+        best = want < maxseg ? want : maxseg;
+    } else {
+        double best_cost = 0.0;
+        for (long long ns = 1; ns <= maxseg && ns <= 4LL * nsm; ++ns) {
+            const long long seg = (L + ns - 1) / ns;
+            const long long segr = (seg + TC - 1) / TC * TC;
+            const long long nseg = (L + segr - 1) / segr;
+            if (nseg != ns) continue;
+            const long long k = kcta_of((long long)s->batch * ns);
+            const long long waves = ((long long)s->batch * ns * k + nsm - 1) / nsm;
+            double cost = (double)waves * segr;
+            if (ns > 1) cost += 0.75 * (double)(((long long)s->batch * (ns - 1) * k + nsm - 1) / nsm) * segr;
+            if (ns == 1 || cost < best_cost * 0.98) {
+                best_cost = cost;
+                best = ns;
+            }
+        }
+    }
+    p.nseg = 1;
+    p.seg_len = L;
+    if (best > 1) {
+        long long seg = (L + best - 1) / best;
+        seg = (seg + TC - 1) / TC * TC;
+        p.seg_len = seg;
+        p.nseg = (int)((L + seg - 1) / seg);
+    }
+    const long long rows = (long long)s->batch * p.nseg;
+    const long long k = kcta_of(rows);
+    p.kcta = (int)k;
+    p.wmax = (int)((p.upr + k - 1) / k);
+    p.wlo = p.upr / p.kcta;
+    if (rows * k > 0x7fffffffLL) return fail(MAMBA_ERR_ARG, "grid too large");
+    p.bc_off = 3 * p.wmax * TILE;
+    p.quad_off = p.bc_off + 2 * NP * cl::kRowBytes;
+    p.stage_bytes = stage_of(p.wmax);
+    int ns = env_int("MAMBA_SCAN_STAGES", 4);
+    if (ns < 2) ns = 2;
+    while (ns > 2 && smem_of(p.wmax, ns) > kSmemLimit) --ns;
+    p.nstage = ns;
+    p.scratch_off = ns * p.stage_bytes;  // y staging tiles
+    p.src_off = p.scratch_off + p.wmax * 2 * cl::kYTile;
+    p.bar_off = p.src_off;
+    p.smem_bytes = smem_of(p.wmax, ns);
+    if (p.smem_bytes > kSmemLimit) return fail(MAMBA_ERR_ARG, "tiling needs %d bytes of shared memory", p.smem_bytes);
+    return MAMBA_OK;
+}
+
+// Work split of scan_fwd_kernel.  Units (8 channels of one batch row, one consumer warp each) are
+// the grain.  The time axis is split into segments only when the units alone cannot give every SM
+// several warps (a split costs one extra pass over delta, u and B for all but the last segment).
+// Each (segment, batch row) gets kcta CTAs with an even share of its units, so that the grid is
+// about one CTA per SM and the per-SM work differs by at most one unit.
+template <typename TIn, int NP>
+static int plan_warp(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
+    constexpr int TC = Chunk<TIn>::TC;
+    constexpr int CPW = kUnitCh;    // channels per work unit
+    constexpr int UB = CPW * 128;   // u/delta/z tile bytes per unit and chunk
     const long long L = s->seqlen;
     p.upr = (s->dim + CPW - 1) / CPW;
     const long long units = (long long)s->batch * p.upr;
@@ -123,12 +209,10 @@ static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     // shared memory: NS stages of [u | delta | z tiles (1 KB per unit each) | B, C tiles | quads],
     // then per-warp scratch, then 3 NS mbarriers.  Consumer warps per CTA are capped so that two
     // stages fit.
-    // (tensor-memory variant: no quads in the stages; two 8 KB copy sources; 4 more mbarriers)
-    const int bc_bytes = 2 * NP * 128, quad_bytes = TM ? 0 : TC * (NP / 2) * 16;
-    const int wscratch = TM ? kWarpScratchT : Layout<LPC>::SCRATCH;
-    const int extra = TM ? 2 * kSrcBytes + 4 * 8 + 16 : 0;
+    const int bc_bytes = 2 * NP * 128, quad_bytes = TC * (NP / 2) * 16;
+    const int wscratch = kWarpScratch;
     auto stage_of = [&](int w) { return (3 * w * UB + bc_bytes + quad_bytes + 1023) / 1024 * 1024; };
-    auto smem_of = [&](int w, int ns) { return ns * stage_of(w) + w * wscratch + extra + 3 * ns * 8 + 1024; };
+    auto smem_of = [&](int w, int ns) { return ns * stage_of(w) + w * wscratch + 3 * ns * 8 + 1024; };
     int wcap = kMaxConsumerWarps;
     while (wcap > 1 && smem_of(wcap, 2) > kSmemLimit) --wcap;
     const int wforce = env_int("MAMBA_SCAN_WMAX", 0);
@@ -156,68 +240,133 @@ static int plan_fwd(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     p.nstage = ns;
     p.scratch_off = ns * p.stage_bytes;
     p.src_off = p.scratch_off + p.wmax * wscratch;
-    p.bar_off = p.src_off + (TM ? 2 * kSrcBytes : 0);
+    p.bar_off = p.src_off;
     p.smem_bytes = smem_of(p.wmax, ns);
     if (p.smem_bytes > kSmemLimit) return fail(MAMBA_ERR_ARG, "tiling needs %d bytes of shared memory", p.smem_bytes);
     return MAMBA_OK;
 }
 
-// Raises a kernel's dynamic shared memory limit once per device (the attribute is per function
-// and context; setting it on every call costs tens of microseconds of host time).
+// Raises a kernel's dynamic shared memory limit once per CUDA context (the attribute belongs to
+// the function in one context; setting it on every call costs tens of microseconds of host time).
+// Unique id of the CUDA context current on this thread (0 if none is current or the driver
+// entry points are missing).  Ids are never reused within a process, so an id stays tied to one
+// context even after cudaDeviceReset replaces the primary context at the same address.
+static unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+struct AttrCache {
+    std::atomic<unsigned long long> ctx[8] = {};
+};
+
 template <typename K>
-static int allow_smem(K kern, std::atomic<unsigned long long>& done_mask) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (done_mask.load(std::memory_order_acquire) & bit) return MAMBA_OK;
+static int allow_smem(K kern, AttrCache& cache) {
+    const unsigned long long id = current_context_id();
+    if (id != 0)
+        for (auto& c : cache.ctx)
+            if (c.load(std::memory_order_acquire) == id) return MAMBA_OK;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-    done_mask.fetch_or(bit, std::memory_order_acq_rel);
+    if (id != 0) cache.ctx[id % 8].store(id, std::memory_order_release);
     return MAMBA_OK;
 }
 
-template <typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE, bool TM, int LPC>
-static int launch_fwd_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
-    static std::atomic<unsigned long long> attr_done{0};
-    auto kern = TM ? scan_fwd_tm_kernel<TIn, TMA, AGG, SP, GATE> : scan_fwd_kernel<TIn, NP, LPC, TMA, AGG, SP, GATE>;
-    int rc = allow_smem(kern, attr_done);
+static int launch_kernel(void (*kern)(const FwdArgs, const FwdMaps), AttrCache& attr, const FwdArgs& a,
+                         const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
+    int rc = allow_smem(kern, attr);
     if (rc) return rc;
     kern<<<grid, 32 * (a.wmax + 1), smem_bytes, st>>>(a, maps);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "scan_fwd_kernel launch");
+    if (e != cudaSuccess) return cuda_fail(e, "forward scan kernel launch");
+    return MAMBA_OK;
+}
+
+// Channel-per-lane kernel: data path and discretisation / convolution mode are template
+// parameters; softplus and the gate are runtime flags.
+template <typename TIn, int NP, bool TMA, bool AGG, int MODE>
+static int launch_cl_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
+    static AttrCache attr;
+    return launch_kernel(scan_fwd_cl_kernel<TIn, NP, TMA, AGG, MODE>, attr, a, maps, grid, smem_bytes, st);
+}
+
+template <typename TIn, int NP, bool AGG>
+static int launch_cl(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, bool tma, int mode,
+                     cudaStream_t st) {
+    switch (mode) {
+        case 0: return tma ? launch_cl_one<TIn, NP, true, AGG, 0>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, false, AGG, 0>(a, maps, grid, smem_bytes, st);
+        case 1: return tma ? launch_cl_one<TIn, NP, true, AGG, 1>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, false, AGG, 1>(a, maps, grid, smem_bytes, st);
+        case 2: return tma ? launch_cl_one<TIn, NP, true, AGG, 2>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, false, AGG, 2>(a, maps, grid, smem_bytes, st);
+        default: return tma ? launch_cl_one<TIn, NP, true, AGG, 3>(a, maps, grid, smem_bytes, st)
+                            : launch_cl_one<TIn, NP, false, AGG, 3>(a, maps, grid, smem_bytes, st);
+    }
+}
+
+template <FwdKernel KIND, typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE>
+static int launch_fwd_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
+    static AttrCache attr;
+    auto kern = scan_fwd_kernel<TIn, NP, 4, TMA, AGG, SP, GATE>;
+    int rc = allow_smem(kern, attr);
+    if (rc) return rc;
+    kern<<<grid, 32 * (a.wmax + 1), smem_bytes, st>>>(a, maps);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "forward scan kernel launch");
     return MAMBA_OK;
 }
 
 // Selects the instantiation for the runtime flags (data path, softplus, gate).
-template <typename TIn, int NP, bool AGG, bool TM, int LPC>
+template <FwdKernel KIND, typename TIn, int NP, bool AGG>
 static int launch_fwd(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, bool tma, bool sp,
                       bool gate, cudaStream_t st) {
     if constexpr (AGG) {  // the aggregate pass reads no z
-        if (tma) return sp ? launch_fwd_one<TIn, NP, true, true, true, false, TM, LPC>(a, maps, grid, smem_bytes, st)
-                           : launch_fwd_one<TIn, NP, true, true, false, false, TM, LPC>(a, maps, grid, smem_bytes, st);
-        return sp ? launch_fwd_one<TIn, NP, false, true, true, false, TM, LPC>(a, maps, grid, smem_bytes, st)
-                  : launch_fwd_one<TIn, NP, false, true, false, false, TM, LPC>(a, maps, grid, smem_bytes, st);
+        if (tma) return sp ? launch_fwd_one<KIND, TIn, NP, true, true, true, false>(a, maps, grid, smem_bytes, st)
+                           : launch_fwd_one<KIND, TIn, NP, true, true, false, false>(a, maps, grid, smem_bytes, st);
+        return sp ? launch_fwd_one<KIND, TIn, NP, false, true, true, false>(a, maps, grid, smem_bytes, st)
+                  : launch_fwd_one<KIND, TIn, NP, false, true, false, false>(a, maps, grid, smem_bytes, st);
     } else {
         if (tma) {
-            if (sp) return gate ? launch_fwd_one<TIn, NP, true, false, true, true, TM, LPC>(a, maps, grid, smem_bytes, st)
-                                : launch_fwd_one<TIn, NP, true, false, true, false, TM, LPC>(a, maps, grid, smem_bytes, st);
-            return gate ? launch_fwd_one<TIn, NP, true, false, false, true, TM, LPC>(a, maps, grid, smem_bytes, st)
-                        : launch_fwd_one<TIn, NP, true, false, false, false, TM, LPC>(a, maps, grid, smem_bytes, st);
+            if (sp) return gate ? launch_fwd_one<KIND, TIn, NP, true, false, true, true>(a, maps, grid, smem_bytes, st)
+                                : launch_fwd_one<KIND, TIn, NP, true, false, true, false>(a, maps, grid, smem_bytes, st);
+            return gate ? launch_fwd_one<KIND, TIn, NP, true, false, false, true>(a, maps, grid, smem_bytes, st)
+                        : launch_fwd_one<KIND, TIn, NP, true, false, false, false>(a, maps, grid, smem_bytes, st);
         }
-        if (sp) return gate ? launch_fwd_one<TIn, NP, false, false, true, true, TM, LPC>(a, maps, grid, smem_bytes, st)
-                            : launch_fwd_one<TIn, NP, false, false, true, false, TM, LPC>(a, maps, grid, smem_bytes, st);
-        return gate ? launch_fwd_one<TIn, NP, false, false, false, true, TM, LPC>(a, maps, grid, smem_bytes, st)
-                    : launch_fwd_one<TIn, NP, false, false, false, false, TM, LPC>(a, maps, grid, smem_bytes, st);
+        if (sp) return gate ? launch_fwd_one<KIND, TIn, NP, false, false, true, true>(a, maps, grid, smem_bytes, st)
+                            : launch_fwd_one<KIND, TIn, NP, false, false, true, false>(a, maps, grid, smem_bytes, st);
+        return gate ? launch_fwd_one<KIND, TIn, NP, false, false, false, true>(a, maps, grid, smem_bytes, st)
+                    : launch_fwd_one<KIND, TIn, NP, false, false, false, false>(a, maps, grid, smem_bytes, st);
     }
 }
 
 // `scratch`/`scratch_cap`: when scratch is non-NULL the segment carries live there (no allocation);
 // otherwise they come from cudaMallocAsync on `st`.
-template <typename TIn, int NP, bool TM, int LPC>
+template <FwdKernel KIND, typename TIn, int NP>
 static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gate, float2* scratch,
                    size_t scratch_cap, cudaStream_t st) {
     constexpr int TC = Chunk<TIn>::TC;
+    constexpr int CPW = KIND == FwdKernel::kChannelLane ? 32 : kUnitCh;  // channels per work unit
     const int esize = (int)sizeof(TIn);
     const long long L = s->seqlen;
 
@@ -226,7 +375,11 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
 
     FwdPlan p;
-    int rc = plan_fwd<TIn, NP, TM, LPC>(s, nsm, p);
+    int rc;
+    if constexpr (KIND == FwdKernel::kChannelLane)
+        rc = plan_cl<TIn, NP>(s, nsm, p);
+    else
+        rc = plan_warp<TIn, NP>(s, nsm, p);
     if (rc) return rc;
 
     const bool tma_ok = encode_fn() != nullptr && (L * esize) % 16 == 0 && aligned16(a.u) && aligned16(a.delta) &&
@@ -241,12 +394,12 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
         bool ok = true;
         for (int m = 0; m < 3 && ok; ++m)
             for (int w = 0; w < 2 && ok; ++w) {
-                constexpr int CPW = TM ? kUnitCh : Layout<LPC>::CPW;
                 const int rowsbox = CPW * (w == 0 ? (p.wlo > 0 ? p.wlo : 1) : p.wlo + 1);
                 ok = encode_3d(&dst[m][w], src[m], esize, L, s->dim, s->batch, TC, rowsbox > 256 ? 256 : rowsbox);
             }
         ok = ok && encode_3d(&maps.B, a.B, esize, L, s->dstate, s->batch, TC, s->dstate) &&
              encode_3d(&maps.C, a.C, esize, L, s->dstate, s->batch, TC, s->dstate);
+        if (KIND == FwdKernel::kChannelLane) ok = ok && encode_3d(&maps.y, a.y, esize, L, s->dim, s->batch, TC, 32);
         if (!ok) return fail(MAMBA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     }
 
@@ -264,6 +417,16 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
     a.src_off = p.src_off;
     a.bar_off = p.bar_off;
     a.agg = nullptr;
+    // bounded waits: the full limit, or (test knob, read here on the host) a 1 ms limit for waits
+    // on other warps together with consumer warps that wait on a barrier nothing arrives on
+    a.wait_ns = kWaitLimitNs;
+    a.test_stall = 0;
+    a.softplus = softplus ? 1 : 0;
+    const int mode = (a.zoh ? 1 : 0) | (a.conv_w != nullptr ? 2 : 0);
+    if (KIND == FwdKernel::kChannelLane && env_int("MAMBA_SCAN_TEST_STALL", 0) != 0) {
+        a.wait_ns = 1000000ull;
+        a.test_stall = 1;
+    }
 
     bool owned = false;
     if (p.nseg > 1) {
@@ -294,11 +457,17 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
             }
         }
         const unsigned g1 = (unsigned)((long long)s->batch * (p.nseg - 1) * p.kcta);
-        rc = launch_fwd<TIn, NP, true, TM, LPC>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
+        if constexpr (KIND == FwdKernel::kChannelLane)
+            rc = launch_cl<TIn, NP, true>(a, maps, g1, p.smem_bytes, tma_ok, mode, st);
+        else
+            rc = launch_fwd<KIND, TIn, NP, true>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
     }
     if (rc == MAMBA_OK) {
         const unsigned g2 = (unsigned)((long long)s->batch * p.nseg * p.kcta);
-        rc = launch_fwd<TIn, NP, false, TM, LPC>(a, maps, g2, p.smem_bytes, tma_ok, softplus, gate, st);
+        if constexpr (KIND == FwdKernel::kChannelLane)
+            rc = launch_cl<TIn, NP, false>(a, maps, g2, p.smem_bytes, tma_ok, mode, st);
+        else
+            rc = launch_fwd<KIND, TIn, NP, false>(a, maps, g2, p.smem_bytes, tma_ok, softplus, gate, st);
     }
     if (owned) {
         cudaError_t e = cudaFreeAsync(a.agg, st);
@@ -307,19 +476,26 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
     return rc;
 }
 
+// Kernel choice: the channel-per-lane kernel for N <= 16, scan_fwd_kernel for wider states.
+// MAMBA_SCAN_KERNEL=warp or =lane forces one (tests, benchmarks).
 template <typename TIn, int NP>
 static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, bool gate, float2* scratch,
                         size_t scratch_cap, cudaStream_t st) {
-    // N <= 16 with MAMBA_SCAN_TMEM=1: the variant that feeds B/C through tensor memory (not the
-    // default: slower on the measured workloads)
-    if constexpr (NP == 16) {
-        if (getenv("MAMBA_SCAN_TMEM") != nullptr && !a.zoh && a.conv_w == nullptr)
-            return fwd_run<TIn, NP, true, 4>(s, a, softplus, gate, scratch, scratch_cap, st);
-        // lanes per channel: 2 (8 states per lane, 16 channels per warp) or 4
-        if (env_int("MAMBA_SCAN_LPC", 4) == 2)
-            return fwd_run<TIn, NP, false, 2>(s, a, softplus, gate, scratch, scratch_cap, st);
+    const char* force = getenv("MAMBA_SCAN_KERNEL");
+    const bool lane_ok = NP <= 16;
+    bool use_lane = lane_ok;
+    if (force && strcmp(force, "warp") == 0) use_lane = false;
+    if (force && strcmp(force, "lane") == 0) {
+        if (!lane_ok) return fail(MAMBA_ERR_ARG, "MAMBA_SCAN_KERNEL=lane: the channel-per-lane kernel takes N <= 16");
+        use_lane = true;
     }
-    return fwd_run<TIn, NP, false, 4>(s, a, softplus, gate, scratch, scratch_cap, st);
+    if constexpr (NP <= 16) {
+        if (use_lane) {
+            if (s->dstate <= 8) return fwd_run<FwdKernel::kChannelLane, TIn, 8>(s, a, softplus, gate, scratch, scratch_cap, st);
+            return fwd_run<FwdKernel::kChannelLane, TIn, 16>(s, a, softplus, gate, scratch, scratch_cap, st);
+        }
+    }
+    return fwd_run<FwdKernel::kWarp, TIn, NP>(s, a, softplus, gate, scratch, scratch_cap, st);
 }
 
 // ---------------------------------------------------------------------------- checks
@@ -342,12 +518,17 @@ static int check_shape(const mamba_scan_shape* s, bool need_len) {
 
 template <typename TIn, int NP>
 static int step_dispatch(const StepArgs& a, cudaStream_t st) {
-    constexpr int S = NP / 4;
+    constexpr int S = NP / (NP < 8 ? NP : 8);  // threads per channel (state_step_kernel)
     const long long threads = (long long)a.batch * a.dim * S;
     const int bs = 256;
     const long long blocks = (threads + bs - 1) / bs;
     if (blocks > 0x7fffffffLL) return fail(MAMBA_ERR_ARG, "too many channels");
-    const bool vec4 = (a.dstate == NP) && aligned16(a.state);
+    // vector accesses: whole rows of NP states, 16-byte aligned state and A rows, B/C rows aligned
+    // to their 4-element loads
+    const uintptr_t bc_align = sizeof(TIn) == 4 ? 15u : 7u;
+    const bool vec4 = (a.dstate == NP) && aligned16(a.state) && aligned16(a.A) &&
+                      (reinterpret_cast<uintptr_t>(a.B) & bc_align) == 0 &&
+                      (reinterpret_cast<uintptr_t>(a.C) & bc_align) == 0;
     if (vec4)
         state_step_kernel<TIn, NP, true><<<(unsigned)blocks, bs, 0, st>>>(a);
     else
@@ -360,7 +541,7 @@ static int step_dispatch(const StepArgs& a, cudaStream_t st) {
 
 template <typename TIn, bool ZOH>
 static int bwd_launch(const BwdArgs& a, bool vec, cudaStream_t st) {
-    static std::atomic<unsigned long long> attr_vec{0}, attr_scalar{0};
+    static AttrCache attr_vec, attr_scalar;
     auto kern = vec ? scan_bwd_kernel<TIn, true, ZOH> : scan_bwd_kernel<TIn, false, ZOH>;
     int rc = allow_smem(kern, vec ? attr_vec : attr_scalar);
     if (rc) return rc;
@@ -477,32 +658,6 @@ extern "C" int mamba_scan_fwd_conv(const mamba_scan_shape* s, int discretization
 // Scratch of mamba_scan_fwd_noalloc: the segment carries of a split time axis.  A file-scope
 // device array, so it exists on every device that loads this library, from module load to exit.
 static __device__ __align__(256) float2 g_noalloc_scratch[MAMBA_NOALLOC_SCRATCH_BYTES / sizeof(float2)];
-
-// Unique id of the CUDA context current on this thread (0 if none is current or the driver
-// entry points are missing).  Ids are never reused within a process, so an id stays tied to one
-// context even after cudaDeviceReset replaces the primary context at the same address.
-static unsigned long long current_context_id() {
-    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
-    static PFN_cuCtxGetId_v12000 get_id = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
-        p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
-    });
-    if (!get_current || !get_id) return 0;
-    CUcontext ctx = nullptr;
-    unsigned long long id = 0;
-    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
-    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
-    return id;
-}
 
 // Device address of g_noalloc_scratch in the CUDA context current on this thread.  In host code
 // the symbol is only a host-side stand-in, so its device address is looked up with

@@ -1,5 +1,6 @@
 // Inline-PTX helpers for sm_103a: mbarriers, TMA (cp.async.bulk.tensor) loads/stores, bulk-group
-// waits, proxy fences, packed fp32x2 arithmetic and the MUFU base-2 exponential.
+// waits, proxy fences, cp.async, vector reductions, packed fp32x2 arithmetic and the MUFU base-2
+// exponential.
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
@@ -113,41 +114,6 @@ __device__ __forceinline__ void red_add_v4(float* p, float4 v) {
                  : "memory");
 }
 
-// ------------------------------------------------------------------------------------ tensor memory
-// Allocation (one warp, all lanes): the base TMEM address is written to shared memory at `dst`.
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void tmem_fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tmem_fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor (no swizzle): start address, leading / stride byte offsets,
-// descriptor version 1 (bit 46).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)((lbo >> 4) & 0x3fffu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3fffu) << 32) | (1ull << 46);
-}
-
-// Copy a 128-row x 32-byte matrix from shared memory into TMEM columns [taddr, taddr+8) of all
-// 128 lanes (asynchronous).  With a zero stride between 8-row core matrices, one 8-row pattern
-// fills every 8-lane group.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t desc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-
-// Arrive once on `bar` when every tcgen05 copy issued so far by this thread has completed.
-__device__ __forceinline__ void tmem_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
 // ------------------------------------------------------------------------------------ math
 // MUFU base-2 exponential (flush-to-zero).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -197,75 +163,6 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
 // index (bits 4-6) is XORed with the row index modulo 8 (bits 7-9 of a 1024-byte aligned tile).
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t byte) {
     return row * 128u + ((((byte >> 4) ^ row) & 7u) << 4) + (byte & 15u);
-}
-
-// ------------------------------------------------------------------------------------ packed pairs
-// Two fp32 lanes held in one 64-bit register pair, operated on with the f32x2 instructions without
-// splitting them apart in between (a split/rejoin costs register moves).
-typedef unsigned long long f2p;
-
-__device__ __forceinline__ f2p ppack(float lo, float hi) {
-    f2p d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
-    return d;
-}
-__device__ __forceinline__ float plo(f2p v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return lo;
-}
-__device__ __forceinline__ float phi(f2p v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return hi;
-}
-__device__ __forceinline__ f2p pmul(f2p a, f2p b) {
-    f2p d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f2p pfma(f2p a, f2p b, f2p c) {
-    f2p d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ f2p padd(f2p a, f2p b) {
-    f2p d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-// (2^x.lo, 2^x.hi) with the MUFU base-2 exponential (flush-to-zero)
-__device__ __forceinline__ f2p pex2(f2p x) {
-    f2p d;
-    asm("{\n\t.reg .f32 a, b;\n\tmov.b64 {a, b}, %1;\n\tex2.approx.ftz.f32 a, a;\n\tex2.approx.ftz.f32 b, b;\n\t"
-        "mov.b64 %0, {a, b};\n\t}"
-        : "=l"(d)
-        : "l"(x));
-    return d;
-}
-// x.lo + x.hi
-__device__ __forceinline__ float psum(f2p x) {
-    float r;
-    asm("{\n\t.reg .f32 a, b;\n\tmov.b64 {a, b}, %1;\n\tadd.rn.f32 %0, a, b;\n\t}" : "=f"(r) : "l"(x));
-    return r;
-}
-
-// 32 columns of this thread's TMEM lane as 16 packed pairs (columns 2i, 2i+1 -> w[i]), waiting for
-// the data in the same statement.
-__device__ __forceinline__ void tmem_ld32_pairs(uint32_t taddr, f2p (&w)[16]) {
-    asm volatile(
-        "{\n\t.reg .b32 r<32>;\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {r0,r1,r2,r3,r4,r5,r6,r7,r8,r9,r10,r11,r12,r13,r14,r15,"
-        "r16,r17,r18,r19,r20,r21,r22,r23,r24,r25,r26,r27,r28,r29,r30,r31}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;\n\t"
-        "mov.b64 %0, {r0, r1};\n\tmov.b64 %1, {r2, r3};\n\tmov.b64 %2, {r4, r5};\n\tmov.b64 %3, {r6, r7};\n\t"
-        "mov.b64 %4, {r8, r9};\n\tmov.b64 %5, {r10, r11};\n\tmov.b64 %6, {r12, r13};\n\tmov.b64 %7, {r14, r15};\n\t"
-        "mov.b64 %8, {r16, r17};\n\tmov.b64 %9, {r18, r19};\n\tmov.b64 %10, {r20, r21};\n\tmov.b64 %11, {r22, r23};\n\t"
-        "mov.b64 %12, {r24, r25};\n\tmov.b64 %13, {r26, r27};\n\tmov.b64 %14, {r28, r29};\n\tmov.b64 %15, {r30, r31};\n\t}"
-        : "=l"(w[0]), "=l"(w[1]), "=l"(w[2]), "=l"(w[3]), "=l"(w[4]), "=l"(w[5]), "=l"(w[6]), "=l"(w[7]), "=l"(w[8]),
-          "=l"(w[9]), "=l"(w[10]), "=l"(w[11]), "=l"(w[12]), "=l"(w[13]), "=l"(w[14]), "=l"(w[15])
-        : "r"(taddr)
-        : "memory");
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` lands in the low half.

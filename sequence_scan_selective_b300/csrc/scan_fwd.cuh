@@ -100,11 +100,19 @@ struct FwdArgs {
     const float* conv_prev;  // [batch][dim][conv_k - 1] or NULL
     int conv_k;              // 1..4
     int conv_silu;
+    // Bound (ns of %globaltimer) on a wait for other warps of the CTA.  A wait for an
+    // asynchronous copy to land before the CTA exits always keeps kWaitLimitNs.
+    unsigned long long wait_ns;
+    // Test knob (host-set, never by default): consumer warps first wait on a barrier nothing
+    // arrives on, so every bounded wait of the launch runs out and the status word is set.
+    int test_stall;
+    int softplus;  // channel-per-lane kernel: Delta = softplus(delta + bias) (else delta + bias)
 };
 
 // u, delta, z maps: [0] box of wlo units' rows, [1] of (wlo+1) units' rows; B, C: box [N, TC].
 struct FwdMaps {
     CUtensorMap u[2], d[2], z[2], B, C;
+    CUtensorMap y;  // box [32 rows, TC] (channel-per-lane kernel: one warp's output tile)
 };
 
 // Steps per chunk: one 128-byte row of each input.
@@ -256,7 +264,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 if (!ok) break;
                 landed = k + 1;
             } else if (k >= NS) {
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (uint32_t)((k / NS - 1) & 1), kWaitLimitNs));
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[s], (uint32_t)((k / NS - 1) & 1), a.wait_ns));
                 if (!ok) break;
             }
             build_quads(k);
@@ -264,7 +272,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             // refill the stage of chunk k-1 with chunk k-1+NS once every consumer has left it
             if (TMA && k >= 1 && k - 1 + NS < nchunks) {
                 const int sp = (k - 1) % NS;
-                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[sp], (uint32_t)(((k - 1) / NS) & 1), kWaitLimitNs));
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[sp], (uint32_t)(((k - 1) / NS) & 1), a.wait_ns));
                 if (!ok) break;
                 if (lane == 0) issue(k - 1 + NS);
                 ++issued;
@@ -326,10 +334,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
 
     auto wait_tiles = [&](int k) -> bool {  // u, delta, z tiles of chunk k have landed
         if (!TMA) return true;
-        return __all_sync(0xffffffffu, mbar_wait_bounded(&full[k % NS], (uint32_t)((k / NS) & 1), kWaitLimitNs));
+        return __all_sync(0xffffffffu, mbar_wait_bounded(&full[k % NS], (uint32_t)((k / NS) & 1), a.wait_ns));
     };
     auto wait_quads = [&](int k) -> bool {  // the producer has written chunk k's B/C quads
-        return __all_sync(0xffffffffu, mbar_wait_bounded(&qready[k % NS], (uint32_t)((k / NS) & 1), kWaitLimitNs));
+        return __all_sync(0xffffffffu, mbar_wait_bounded(&qready[k % NS], (uint32_t)((k / NS) & 1), a.wait_ns));
     };
 
     // ---- causal convolution in front of the scan: x of the 3 steps before the lane's window,

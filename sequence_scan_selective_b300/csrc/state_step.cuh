@@ -4,9 +4,14 @@
 // autoregressive inference with constant work per token (news write-up, "architecture" section):
 //   h <- exp(Delta A) h + Delta B x,   y = (C.h + D x) silu(z)
 // (with the exact zero-order hold, Delta B x becomes (exp(Delta A) - 1) / A * B x).
-// The state [b, d, N] fp32 dominates the traffic (read + write); each thread owns 4 consecutive
-// states of one channel so that a warp streams 512 contiguous bytes of state per 128-bit access,
-// and the NP/4 lanes of a channel combine their partial C.h with warp shuffles.
+//
+// The fp32 state [b, d, N] dominates the traffic (read + write).  Each thread owns Q = min(N, 8)
+// consecutive states of one channel (S = ceil(N / Q) threads per channel, next to each other in
+// the warp) and moves them with 128-bit loads and stores; A[d, n..] arrives with 128-bit loads as
+// well, and B[b, n..], C[b, n..] -- the same for every channel of a batch row, so one broadcast
+// transaction per warp -- with 64-bit (bf16) or 128-bit (fp32) loads.  The S threads of a
+// channel each form Delta and the gate themselves (a few dozen operations, cheaper than an
+// exchange) and combine their partial C.h with shuffles.
 #pragma once
 #include <stdint.h>
 
@@ -31,11 +36,28 @@ struct StepArgs {
     int zoh;  // nonzero: exact zero-order hold for B
 };
 
-template <typename TIn, int NP, bool VEC4>
+// 4 consecutive inputs at p (16-byte aligned for fp32, 8-byte aligned for bf16) -> fp32
+template <typename TIn>
+__device__ __forceinline__ void load4(const TIn* p, float* v);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float* v) {
+    const float4 q = __ldg(reinterpret_cast<const float4*>(p));
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+template <>
+__device__ __forceinline__ void load4<uint16_t>(const uint16_t* p, float* v) {
+    const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+    v[0] = __uint_as_float(q.x << 16); v[1] = __uint_as_float(q.x & 0xffff0000u);
+    v[2] = __uint_as_float(q.y << 16); v[3] = __uint_as_float(q.y & 0xffff0000u);
+}
+
+// VEC: N is a multiple of Q (= 8, or 4 for N = 4) and every row is aligned for vector access;
+// otherwise element-wise accesses with bounds checks on the state index.
+template <typename TIn, int NP, bool VEC>
 __global__ void __launch_bounds__(256) state_step_kernel(const StepArgs a) {
-    constexpr int Q = 4;        // states per thread
-    constexpr int S = NP / Q;   // lanes per channel
-    static_assert(32 % S == 0, "a channel's lanes must sit in one warp");
+    constexpr int Q = NP < 8 ? NP : 8;   // states per thread
+    constexpr int S = NP / Q;            // threads per channel
+    static_assert(Q % 4 == 0 && 32 % S == 0, "a channel's threads must sit in one warp");
     const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long ch = gt / S;
     const int q = (int)(gt % S);
@@ -48,39 +70,49 @@ __global__ void __launch_bounds__(256) state_step_kernel(const StepArgs a) {
     if (valid) {
         const int b = (int)(ch / a.dim);
         d = (int)(ch % a.dim);
-        const TIn* X = static_cast<const TIn*>(a.x);
-        const TIn* Dl = static_cast<const TIn*>(a.delta);
-        xv = In<TIn>::to_f32(X[ch]);
-        float dt = In<TIn>::to_f32(Dl[ch]) + (a.bias ? a.bias[d] : 0.f);
+        xv = In<TIn>::to_f32(static_cast<const TIn*>(a.x)[ch]);
+        float dt = In<TIn>::to_f32(static_cast<const TIn*>(a.delta)[ch]) + (a.bias ? a.bias[d] : 0.f);
         if (a.softplus) dt = softplus1(dt);
         const float du = dt * xv;
-        const TIn* Bp = static_cast<const TIn*>(a.B) + (long long)b * N;
-        const TIn* Cp = static_cast<const TIn*>(a.C) + (long long)b * N;
-        const float* Ap = a.A + (long long)d * N;
-        float* hp = a.state + ch * N + q * Q;
         const int n0 = q * Q;
-        float hv[Q];
-        if (VEC4) {
-            const float4 v = *reinterpret_cast<const float4*>(hp);
-            hv[0] = v.x; hv[1] = v.y; hv[2] = v.z; hv[3] = v.w;
+        const TIn* Bp = static_cast<const TIn*>(a.B) + (long long)b * N + n0;
+        const TIn* Cp = static_cast<const TIn*>(a.C) + (long long)b * N + n0;
+        const float* Ap = a.A + (long long)d * N + n0;
+        float* hp = a.state + ch * N + n0;
+        float hv[Q], Av[Q], Bv[Q], Cv[Q];
+        if (VEC) {
+#pragma unroll
+            for (int i = 0; i < Q; i += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(hp + i);
+                hv[i] = v.x; hv[i + 1] = v.y; hv[i + 2] = v.z; hv[i + 3] = v.w;
+                const float4 w = __ldg(reinterpret_cast<const float4*>(Ap + i));
+                Av[i] = w.x; Av[i + 1] = w.y; Av[i + 2] = w.z; Av[i + 3] = w.w;
+                load4<TIn>(Bp + i, Bv + i);
+                load4<TIn>(Cp + i, Cv + i);
+            }
         } else {
 #pragma unroll
-            for (int i = 0; i < Q; ++i) hv[i] = (n0 + i < N) ? hp[i] : 0.f;
+            for (int i = 0; i < Q; ++i) {
+                const bool in = n0 + i < N;
+                hv[i] = in ? hp[i] : 0.f;
+                Av[i] = in ? Ap[i] : 0.f;
+                Bv[i] = in ? In<TIn>::to_f32(Bp[i]) : 0.f;
+                Cv[i] = in ? In<TIn>::to_f32(Cp[i]) : 0.f;
+            }
         }
 #pragma unroll
         for (int i = 0; i < Q; ++i) {
-            const int n = n0 + i;
-            if (VEC4 || n < N) {
-                const float xe = dt * (Ap[n] * kLog2e);
-                const float abar = ex2_approx(xe);
-                float bx = du;  // Bbar x / B
-                if (a.zoh) bx = fabsf(xe) < kZohSeriesLimit ? du * zoh_phi(xe) : (abar - 1.f) * (xv / Ap[n]);
-                hv[i] = fmaf(abar, hv[i], bx * In<TIn>::to_f32(Bp[n]));
-                part = fmaf(In<TIn>::to_f32(Cp[n]), hv[i], part);
-            }
+            const float xe = dt * (Av[i] * kLog2e);
+            const float abar = ex2_approx(xe);
+            float bx = du;  // Bbar x / B
+            if (a.zoh) bx = fabsf(xe) < kZohSeriesLimit ? du * zoh_phi(xe) : (abar - 1.f) * (xv / Av[i]);
+            hv[i] = fmaf(abar, hv[i], bx * Bv[i]);
+            part = fmaf(Cv[i], hv[i], part);
         }
-        if (VEC4) {
-            *reinterpret_cast<float4*>(hp) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+        if (VEC) {
+#pragma unroll
+            for (int i = 0; i < Q; i += 4)
+                *reinterpret_cast<float4*>(hp + i) = make_float4(hv[i], hv[i + 1], hv[i + 2], hv[i + 3]);
         } else {
 #pragma unroll
             for (int i = 0; i < Q; ++i)

@@ -60,104 +60,160 @@ def _check_full(ms, cfg, softplus=True, drop=(), env=None):
     return ey, es
 
 
-def test_tiny_workload(ms):
-    _check_full(ms, synth.CONFIGS["tiny"])
+# The two forward kernels: "lane" (one channel per lane, N <= 16, the default where it applies)
+# and "warp" (four lanes per channel, any N; also the exact hold and the fused convolution).
+KERNELS = ["lane", "warp"]
 
 
+def _kenv(kernel, **kv):
+    return dict(MAMBA_SCAN_KERNEL=kernel, **kv)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_tiny_workload(ms, kernel):
+    _check_full(ms, synth.CONFIGS["tiny"], env=_kenv(kernel))
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("L", [1, 7, 32, 77, 200, 1000])
-def test_ragged_lengths(ms, dtype, L):
+def test_ragged_lengths(ms, kernel, dtype, L):
     cfg = synth.CONFIGS["m130"].replace(batch=2, dim=40, seqlen=L, dtype=dtype, seed=10 + L)
-    _check_full(ms, cfg)
+    _check_full(ms, cfg, env=_kenv(kernel))
 
 
-@pytest.mark.parametrize("N", [1, 3, 4, 8, 15, 16, 17, 32, 33, 64])
-def test_state_sizes(ms, N):
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("N", [1, 3, 4, 8, 9, 15, 16, 17, 32, 33, 64])
+def test_state_sizes(ms, kernel, N):
+    if kernel == "lane" and N > 16:
+        pytest.skip("the channel-per-lane kernel holds at most 16 states per lane")
     cfg = synth.CONFIGS["m130"].replace(batch=2, dim=35, dstate=N, seqlen=160, seed=20 + N)
+    _check_full(ms, cfg, env=_kenv(kernel))
+
+
+def test_default_kernel_for_wide_state(ms):
+    """Without a forced kernel, N > 16 takes the four-lanes-per-channel kernel."""
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=35, dstate=24, seqlen=160, seed=19)
     _check_full(ms, cfg)
 
 
-@pytest.mark.parametrize("wmax,stages,lpc", [("1", "2", "4"), ("3", "3", "4"), ("15", "4", "4"), ("0", "2", "4"),
-                                             ("1", "2", "2"), ("4", "3", "2"), ("0", "4", "2")])
+def test_lane_kernel_refuses_what_it_cannot_do(ms):
+    x = torch.zeros((1, 4, 32), device="cuda")
+    with _env(MAMBA_SCAN_KERNEL="lane"), pytest.raises(ms.MambaScanError, match="N <= 16"):
+        ms.mamba_scan_fwd(x, x.clone(), -torch.ones((4, 32), device="cuda"), torch.zeros((1, 32, 32), device="cuda"),
+                          torch.zeros((1, 32, 32), device="cuda"))
+
+
+@pytest.mark.parametrize("kernel,wmax,stages", [("warp", "1", "2"), ("warp", "3", "3"), ("warp", "15", "4"),
+                                                ("warp", "0", "2"), ("lane", "1", "2"), ("lane", "2", "3"),
+                                                ("lane", "4", "2"), ("lane", "0", "4")])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_tiling_variants(ms, wmax, stages, lpc, dtype):
-    """Consumer warps per CTA (work units per CTA), ring depth and lanes per channel (2: 8 states
-    per lane, 16 channels per warp; 4: 4 states per lane, 8 channels per warp) change only the
-    schedule."""
+def test_tiling_variants(ms, kernel, wmax, stages, dtype):
+    """Consumer warps per CTA (work units per CTA) and ring depth change only the schedule."""
     cfg = synth.CONFIGS["m130"].replace(batch=2, dim=130, seqlen=333, dtype=dtype, seed=21)
-    _check_full(ms, cfg, env={"MAMBA_SCAN_WMAX": wmax, "MAMBA_SCAN_STAGES": stages, "MAMBA_SCAN_LPC": lpc})
+    _check_full(ms, cfg, env=_kenv(kernel, MAMBA_SCAN_WMAX=wmax, MAMBA_SCAN_STAGES=stages))
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("case", ["split", "ragged_n"])
-def test_two_lanes_per_channel(ms, dtype, case):
-    if case == "split":
-        cfg = synth.CONFIGS["long"].replace(batch=1, dim=40, seqlen=6000, dtype=dtype, seed=23)
-        env = {"MAMBA_SCAN_LPC": "2", "MAMBA_SCAN_NSEG": "3"}
-    else:
-        cfg = synth.CONFIGS["m130"].replace(batch=3, dim=37, dstate=11, seqlen=301, dtype=dtype, seed=24)
-        env = {"MAMBA_SCAN_LPC": "2"}
-    _check_full(ms, cfg, env=env)
-
-
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("drop", [("z",), ("D",), ("delta_bias",), ("z", "D", "delta_bias")])
-def test_optional_inputs(ms, drop):
+def test_optional_inputs(ms, kernel, drop):
     cfg = synth.CONFIGS["m130"].replace(batch=3, dim=33, seqlen=96, seed=5)
-    _check_full(ms, cfg, drop=drop)
+    _check_full(ms, cfg, drop=drop, env=_kenv(kernel))
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_softplus_off(ms, dtype):
+def test_softplus_off(ms, kernel, dtype):
     cfg = synth.CONFIGS["m130"].replace(batch=2, dim=32, seqlen=128, dtype=dtype, seed=6)
     inp = synth.scan_inputs(cfg)
     # without softplus the raw delta must itself be a valid step size: |delta| scaled down
     dl = (np.abs(synth.widen(inp["delta"], dtype)) * 0.01).astype(np.float32)
     inp["delta"] = synth.f32_to_bf16_bits(dl) if dtype == "bf16" else dl
     inp["delta_bias"] = np.zeros_like(inp["delta_bias"])
-    y, st = _run_gpu(ms, dev_inputs(inp, dtype), softplus=False)
+    with _env(**_kenv(kernel)):
+        y, st = _run_gpu(ms, dev_inputs(inp, dtype), softplus=False)
     y_ref, st_ref = oracle_scan_full(inp, dtype, softplus=False)
     assert rel_err(from_dev(y), y_ref) <= TOL[dtype]
     assert rel_err(from_dev(st), st_ref) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_unaligned_rows_take_plain_load_path(ms, dtype):
+def test_unaligned_rows_take_plain_load_path(ms, kernel, dtype):
     # L * element size not a multiple of 16 bytes: no TMA descriptor is possible for these rows
     cfg = synth.CONFIGS["m130"].replace(batch=2, dim=36, seqlen=301, dtype=dtype, seed=7)
-    _check_full(ms, cfg)
+    _check_full(ms, cfg, env=_kenv(kernel))
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_forced_plain_loads_match(ms, dtype):
+def test_forced_plain_loads_match(ms, kernel, dtype):
     cfg = synth.CONFIGS["b14"].replace(batch=2, dim=64, seqlen=256, dtype=dtype, seed=8)
-    _check_full(ms, cfg, env={"MAMBA_SCAN_NO_TMA": "1"})
+    _check_full(ms, cfg, env=_kenv(kernel, MAMBA_SCAN_NO_TMA="1"))
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("nseg", [2, 3, 7])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_split_time_axis(ms, nseg, dtype):
+def test_split_time_axis(ms, kernel, nseg, dtype):
     """Splitting L into segments (carry pass + per-segment scan) regroups the associative scan
     operator (guide section 3.3); results must stay within tolerance of the oracle."""
     cfg = synth.CONFIGS["long"].replace(batch=2, dim=24, seqlen=4000, dtype=dtype, seed=9)
-    _check_full(ms, cfg, env={"MAMBA_SCAN_NSEG": str(nseg)})
+    _check_full(ms, cfg, env=_kenv(kernel, MAMBA_SCAN_NSEG=str(nseg)))
 
 
-def test_split_with_plain_loads(ms):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_split_with_plain_loads(ms, kernel):
     cfg = synth.CONFIGS["long"].replace(batch=1, dim=40, seqlen=3001, seed=11)
-    _check_full(ms, cfg, env={"MAMBA_SCAN_NSEG": "3"})
+    _check_full(ms, cfg, env=_kenv(kernel, MAMBA_SCAN_NSEG="3"))
 
 
-def test_segment_count_invariance(ms):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_segment_count_invariance(ms, kernel):
     cfg = synth.CONFIGS["long"].replace(batch=1, dim=32, seqlen=8192, seed=12)
     d = dev_inputs(synth.scan_inputs(cfg), cfg.dtype)
     outs = []
     for nseg in ("1", "4", "16"):
-        with _env(MAMBA_SCAN_NSEG=nseg):
+        with _env(**_kenv(kernel, MAMBA_SCAN_NSEG=nseg)):
             y, st = _run_gpu(ms, d)
         outs.append((from_dev(y), from_dev(st)))
     for y, st in outs[1:]:
         assert rel_err(y, outs[0][0]) <= 1e-5
         assert rel_err(st, outs[0][1]) <= 1e-5
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_kernels_agree(ms, dtype):
+    """Both forward kernels compute the same scan (to rounding) on a shape several CTAs wide."""
+    cfg = synth.CONFIGS["b14"].replace(batch=3, dim=300, seqlen=700, dtype=dtype, seed=25)
+    d = dev_inputs(synth.scan_inputs(cfg), dtype)
+    outs = {}
+    for k in KERNELS:
+        with _env(MAMBA_SCAN_KERNEL=k):
+            outs[k] = [from_dev(t) for t in _run_gpu(ms, d)]
+    assert rel_err(outs["lane"][0], outs["warp"][0]) <= TOL[dtype]
+    assert rel_err(outs["lane"][1], outs["warp"][1]) <= 1e-5
+
+
+def test_bounded_wait_runs_out(ms):
+    """Failure detection on the device: with the test knob the consumer warps of the forward
+    kernel wait on a barrier that nothing arrives on, and every wait on another warp is limited to
+    1 ms.  The waits run out, the kernel returns (after its copies in flight have landed), the
+    status word reports a timeout, and the next call on the same context is correct again."""
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=70, seqlen=512, seed=26)
+    inp = synth.scan_inputs(cfg)
+    d = dev_inputs(inp, cfg.dtype)
+    ms.device_status()  # clear
+    with _env(MAMBA_SCAN_KERNEL="lane", MAMBA_SCAN_TEST_STALL="1"):
+        ms.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], True)
+        with pytest.raises(ms.MambaScanError) as ei:
+            ms.device_status()
+    assert ei.value.code == ms.MAMBA_ERR_TIMEOUT
+    ms.device_status()  # the word was cleared by the read
+    y, st = _run_gpu(ms, d)
+    y_ref, st_ref = oracle_scan_full(inp, cfg.dtype)
+    assert rel_err(from_dev(y), y_ref) <= TOL["f32"]
+    assert rel_err(from_dev(st), st_ref) <= TOL["f32"]
 
 
 def test_zero_length(ms):
@@ -202,9 +258,10 @@ def test_bad_arguments_raise(ms):
 
 
 # ------------------------------------------------------------------------------ full-size workloads
-def _check_sampled(ms, cfg, nsample, seed=0):
+def _check_sampled(ms, cfg, nsample, seed=0, env=None):
     inp = synth.scan_inputs(cfg)
-    y, st = _run_gpu(ms, dev_inputs(inp, cfg.dtype))
+    with _env(**(env or {})):
+        y, st = _run_gpu(ms, dev_inputs(inp, cfg.dtype))
     rows = sample_rows(cfg.batch * cfg.dim, nsample, seed)
     sub = {k: inp[k].reshape(cfg.batch * cfg.dim, cfg.seqlen)[rows] for k in ("u", "delta", "z")}
     y_ref, st_ref = oracle.scan_rows(rows, cfg.dim, sub["u"], sub["delta"], sub["z"], inp["A"], inp["D"],
@@ -217,12 +274,14 @@ def _check_sampled(ms, cfg, nsample, seed=0):
     assert es <= TOL[cfg.dtype], f"state rel err {es:.3e}"
 
 
-def test_mamba130m_layer_full_size(ms):
-    _check_sampled(ms, synth.CONFIGS["m130"], 192)
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_mamba130m_layer_full_size(ms, kernel):
+    _check_sampled(ms, synth.CONFIGS["m130"], 192, env=_kenv(kernel))
 
 
-def test_mamba14b_layer_full_size(ms):
-    _check_sampled(ms, synth.CONFIGS["b14"], 192)
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_mamba14b_layer_full_size(ms, kernel):
+    _check_sampled(ms, synth.CONFIGS["b14"], 192, env=_kenv(kernel))
 
 
 def test_wide_state_many_channels(ms):
@@ -231,31 +290,17 @@ def test_wide_state_many_channels(ms):
     _check_full(ms, cfg)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("case", ["plain", "split", "ragged"])
-def test_tensor_memory_variant(ms, dtype, case):
-    """The variant that stages B/C in tensor memory (tcgen05.cp / tcgen05.ld) computes the same scan."""
-    if case == "plain":
-        cfg = synth.CONFIGS["m130"].replace(batch=2, dim=130, seqlen=512, dtype=dtype, seed=16)
-        env = {"MAMBA_SCAN_TMEM": "1"}
-    elif case == "split":
-        cfg = synth.CONFIGS["long"].replace(batch=1, dim=40, seqlen=6000, dtype=dtype, seed=17)
-        env = {"MAMBA_SCAN_TMEM": "1", "MAMBA_SCAN_NSEG": "3"}
-    else:
-        cfg = synth.CONFIGS["m130"].replace(batch=2, dim=33, dstate=5, seqlen=301, dtype=dtype, seed=18)
-        env = {"MAMBA_SCAN_TMEM": "1"}
-    _check_full(ms, cfg, env=env)
-
-
 # ------------------------------------------------------------------------------ initial state
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_initial_state_matches_oracle(ms, dtype):
+def test_initial_state_matches_oracle(ms, kernel, dtype):
     cfg = synth.CONFIGS["m130"].replace(batch=2, dim=70, seqlen=300, dtype=dtype, seed=40)
     inp = synth.scan_inputs(cfg)
     h0 = np.random.default_rng(40).standard_normal((cfg.batch, cfg.dim, cfg.dstate)).astype(np.float32)
     d = dev_inputs(inp, dtype)
-    y, st = ms.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], True,
-                              h0=torch.from_numpy(h0).cuda())
+    with _env(MAMBA_SCAN_KERNEL=kernel):
+        y, st = ms.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], True,
+                                  h0=torch.from_numpy(h0).cuda())
     torch.cuda.synchronize()
     y_ref, st_ref = oracle.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
                                 inp["delta_bias"], True, dtype, h0=h0.astype(np.float64))
@@ -263,9 +308,10 @@ def test_initial_state_matches_oracle(ms, dtype):
     assert rel_err(from_dev(st), st_ref) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("shape", ["wide", "split"])
-def test_chunked_prefill_in_place(ms, dtype, shape):
+def test_chunked_prefill_in_place(ms, kernel, dtype, shape):
     """A sequence scanned in pieces, each piece continuing from the state the previous one left in
     the same buffer (h0 is last_state), gives the scan of the whole sequence (the recurrence only
     carries h across positions, visual guide section 2.4)."""
@@ -279,11 +325,12 @@ def test_chunked_prefill_in_place(ms, dtype, shape):
     d = dev_inputs(inp, dtype)
     state = torch.zeros((cfg.batch, cfg.dim, cfg.dstate), device="cuda")
     ys = []
-    for a_, b_ in zip(cuts[:-1], cuts[1:]):
-        piece = lambda k: d[k][:, :, a_:b_].contiguous()
-        y, _ = ms.mamba_scan_fwd(piece("u"), piece("delta"), d["A"], piece("B"), piece("C"), d["D"], piece("z"),
-                                 d["delta_bias"], True, h0=state, last_state=state)
-        ys.append(y)
+    with _env(MAMBA_SCAN_KERNEL=kernel):
+        for a_, b_ in zip(cuts[:-1], cuts[1:]):
+            piece = lambda k: d[k][:, :, a_:b_].contiguous()
+            y, _ = ms.mamba_scan_fwd(piece("u"), piece("delta"), d["A"], piece("B"), piece("C"), d["D"], piece("z"),
+                                     d["delta_bias"], True, h0=state, last_state=state)
+            ys.append(y)
     torch.cuda.synchronize()
     ms.device_status()
     y_ref, st_ref = oracle_scan_full(inp, dtype)

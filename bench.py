@@ -381,7 +381,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     achieved = sb / (scan_avg_ms * 1e-3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     plain = not args.conv and args.disc == "simple"  # the committed ncu records are of the default kernel mode
-    kname = fwd_kernel_name(args, cfg)
+    kname = fwd_kernel_name(args, cfg, torch.cuda.get_device_properties(dev).multi_processor_count)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": ncu_traffic(args.workload, kname.replace("_kernel", "")) if plain else None,
@@ -466,13 +466,21 @@ def long_sequence_rate(dev, local_rank, main_cfg, main_scan_ms, peak, peak_kind,
             "peak_source": f"{peak_kind} hbm_gbs", "clocks": clk.summary()}
 
 
-def fwd_kernel_name(args, cfg) -> str:
-    """The forward kernel the library picks for this run (the channel-per-lane kernel for N <= 16,
-    unless --kernel says otherwise)."""
-    lane_ok = cfg.dstate <= 16
-    if args.kernel == "warp" or not lane_ok:
+def fwd_kernel_name(args, cfg, nsm: int = 148) -> str:
+    """The forward kernel the library picks for this run: for N <= 16 the channel-per-lane kernel
+    when its 32-channel units fill the SM sub-partitions at least as well as the 8-channel units of
+    the four-lanes-per-channel kernel (the library's own rule), unless --kernel says otherwise."""
+    if cfg.dstate > 16 or args.kernel == "warp":
         return "scan_fwd_kernel"
-    return "scan_fwd_cl_kernel"
+    if args.kernel == "lane":
+        return "scan_fwd_cl_kernel"
+    slots = 4 * nsm
+    lane_units = cfg.batch * (-(-cfg.dim // 32))
+    if lane_units * 2 <= slots:
+        return "scan_fwd_cl_kernel"
+    warp_units = cfg.batch * (-(-cfg.dim // 8))
+    fill = lambda u: u / (slots * -(-u // slots))
+    return "scan_fwd_cl_kernel" if 1.07 * fill(lane_units) >= fill(warp_units) else "scan_fwd_kernel"
 
 
 def aggregate_ranks(dist, device, total_ms: float, scan_avg_ms: float, launches: int):

@@ -47,14 +47,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps (issuing nothing) until the phase completes
+// or about `hint_ns` have passed, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Gives up after `limit_ns` of
-// device time and returns false; the caller turns that into an error status, never a trap.
+// device time and returns false; the caller turns that into an error status, never a trap.  After
+// a first check, the waiting warp sleeps in suspend-time-hinted try_waits, so that it does not
+// take issue slots from the warps sharing its SM sub-partition.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const uint32_t hint = (uint32_t)(limit_ns < 200000ull ? limit_ns : 200000ull);
     for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, hint)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }

@@ -8,7 +8,10 @@
 // B300 SM's pipes:
 //  * Lane = channel.  A lane owns every state of its channel, so the per-element work (softplus
 //    step size, Delta x, D x, silu gate) is done once, by the lane that needs it, and the readout
-//    C.h is summed in registers: no exchange between lanes at all.
+//    C.h is summed in registers: no exchange between lanes at all.  When the channels give fewer
+//    than two warps per SM sub-partition, a channel's states can be split over two lanes instead
+//    (LPC = 2), which doubles the warps at the cost of duplicated per-element work and one
+//    shuffle per step.
 //  * B and C are the same for every channel of a batch row, so all 32 lanes of a warp read the
 //    same (B_n, B_n+1, C_n, C_n+1) quad at each step: a broadcast 16-byte shared-memory load,
 //    which the SM serves at about one per clock.  The producer warp builds the quads once per
@@ -32,9 +35,18 @@
 namespace mscan {
 namespace cl {
 
-constexpr int kMaxWarps = 4;       // consumer warps per CTA (one per SM sub-partition)
 constexpr int kRowBytes = 128;     // bytes per tile row (one chunk of one channel)
-constexpr int kYTile = 32 * kRowBytes;  // one warp's y staging tile
+
+// LPC lanes share one channel (LPC = 1: all NP states in one lane; LPC = 2: NP / 2 states in each
+// of lanes c and c + 16, which both do the channel's per-element work and add their readout
+// partials with one shuffle per step).  A CTA holds up to 4 * LPC consumer warps: one (LPC = 1) or
+// two (LPC = 2) per SM sub-partition.
+template <int LPC>
+struct Lanes {
+    static constexpr int CPW = 32 / LPC;                 // channels per warp (work unit)
+    static constexpr int MAX_WARPS = 4 * LPC;            // consumer warps per CTA
+    static constexpr int YTILE = CPW * kRowBytes;        // one warp's y staging tile
+};
 
 template <int NP>
 struct Quads {
@@ -86,19 +98,22 @@ __device__ __forceinline__ void tile_store16<uint16_t>(unsigned char* tile, int 
 // convolution in front of the scan (guide section 3.5): the u tile then holds the block input x,
 // and the lane forms u[t] = act(conv_bias + sum_k conv_w[k] x[t-K+1+k]) itself, keeping the last
 // three inputs of its channel in registers from block to block.
-template <typename TIn, int NP, bool TMA, bool AGG, int MODE>
-__global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
+template <typename TIn, int NP, int LPC, bool TMA, bool AGG, int MODE>
+__global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
     scan_fwd_cl_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps) {
     constexpr int TC = Chunk<TIn>::TC;
     constexpr int ES = (int)sizeof(TIn);
     constexpr int BLK = 16 / ES;  // steps per 16-byte tile read
     constexpr int NPAIR = NP / 2;
     constexpr int QPITCH = cl::Quads<NP>::PITCH;
-    constexpr int TILE = 32 * cl::kRowBytes;  // one warp's rows of one input tile
+    constexpr int CPW = cl::Lanes<LPC>::CPW;
+    constexpr int PL = NPAIR / LPC;            // state pairs per lane
+    constexpr int TILE = CPW * cl::kRowBytes;  // one warp's rows of one input tile
     constexpr bool ZOH = (MODE & 1) != 0;
     constexpr bool CONV = (MODE & 2) != 0;
     const bool has_z = !AGG && a.z != nullptr;
-    static_assert(NP % 2 == 0 && NP <= 16, "shape");
+    const bool softplus = a.softplus != 0;
+    static_assert(NP % (2 * LPC) == 0 && NP <= 16 && (LPC == 1 || LPC == 2), "shape");
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -143,7 +158,7 @@ __global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
             unsigned char* st = smem + s * a.stage_bytes;
             const int t0 = (int)(t_begin + (long long)k * TC);
             mbar_arrive_expect_tx(&full[s], tx);
-            const int r0 = u0 * 32;
+            const int r0 = u0 * CPW;
             tma_load_3d(st, &maps.u[mi], &full[s], t0, r0, b);
             tma_load_3d(st + W * TILE, &maps.d[mi], &full[s], t0, r0, b);
             if (has_z) tma_load_3d(st + 2 * W * TILE, &maps.z[mi], &full[s], t0, r0, b);
@@ -227,18 +242,20 @@ __global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
     if (wid >= nunits) return;
 
     // ====================================================================== consumer warps
-    const int dch = (u0 + wid) * 32 + lane;
+    const int c = lane % CPW, g = lane / CPW;  // channel within the unit, state group
+    const int dch = (u0 + wid) * CPW + c;
     const bool cvalid = dch < a.dim;
     const long long row = (long long)b * a.dim + (cvalid ? dch : 0);
     const float bias = (cvalid && a.bias != nullptr) ? a.bias[dch] : 0.f;
     const float Dd = (!AGG && cvalid && a.D != nullptr) ? a.D[dch] : 0.f;
-    const int trow = wid * 32 + lane;  // this lane's row in the CTA's u, delta, z tiles
+    const int trow = wid * CPW + c;  // this lane's row in the CTA's u, delta, z tiles
 
-    float2 A2[NPAIR], h[NPAIR], invA[ZOH ? NPAIR : 1];
+    // the lane's states: pairs g * PL .. g * PL + PL - 1
+    float2 A2[PL], h[PL], invA[ZOH ? PL : 1];
     const float* h0 = (!AGG && cvalid && a.h0 != nullptr) ? a.h0 + row * N : nullptr;
 #pragma unroll
-    for (int p = 0; p < NPAIR; ++p) {
-        const int n0 = 2 * p, n1 = n0 + 1;
+    for (int p = 0; p < PL; ++p) {
+        const int n0 = 2 * (g * PL + p), n1 = n0 + 1;
         const float a0 = (cvalid && n0 < N) ? a.A[(long long)dch * N + n0] : 0.f;
         const float a1 = (cvalid && n1 < N) ? a.A[(long long)dch * N + n1] : 0.f;
         A2[p] = make_float2(a0 * kLog2e, a1 * kLog2e);
@@ -270,15 +287,16 @@ __global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
         for (int q = 0; q < seg; ++q) {
             const float2* ag = a.agg + (((long long)q * a.batch + b) * a.dim + dch) * N;
 #pragma unroll
-            for (int p = 0; p < NPAIR; ++p) {
-                const int n0 = 2 * p, n1 = n0 + 1;
+            for (int p = 0; p < PL; ++p) {
+                const int n0 = 2 * (g * PL + p), n1 = n0 + 1;
                 if (n0 < N) { const float2 v = ag[n0]; h[p].x = fmaf(v.x, h[p].x, v.y); }
                 if (n1 < N) { const float2 v = ag[n1]; h[p].y = fmaf(v.x, h[p].y, v.y); }
             }
         }
     }
 
-    unsigned char* ystage = smem + a.scratch_off + wid * 2 * cl::kYTile;
+    constexpr int YTILE = cl::Lanes<LPC>::YTILE;
+    unsigned char* ystage = smem + a.scratch_off + wid * 2 * YTILE;
     float sumdt = 0.f;
     bool ok = true;
     if (a.test_stall) ok = __all_sync(0xffffffffu, mbar_wait_bounded(never, 0u, a.wait_ns));
@@ -291,21 +309,26 @@ __global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
         if (!ok) break;
         const unsigned char* st = smem + s * a.stage_bytes;
         const unsigned char* qbase = st + a.quad_off;
-        unsigned char* ybuf = ystage + (k & 1) * cl::kYTile;
+        unsigned char* ybuf = ystage + (k & 1) * YTILE;
         if (TMA && !AGG && k >= 2) {  // the store issued from this buffer two chunks ago has read it
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
         }
         const long long tc0 = t_begin + (long long)k * TC;
 
-#pragma unroll 1
-        for (int blk = 0; blk < TC / BLK; ++blk) {
+        // Per-element work of block blk: Delta, Delta*u, u, D*u and the gate, as pairs of steps.
+        struct Elem {
+            float2 dt[BLK / 2], du[BLK / 2], skip[BLK / 2], gate[BLK / 2];
+            float uv[BLK];
+        };
+        auto elem = [&](int blk, Elem& e) {
             const long long to = tc0 + blk * BLK;  // first step of this block
             float dv[BLK], uv[BLK], zv[BLK];
             if (TMA) {
                 cl::tile_load16<TIn>(st + W * TILE, trow, blk * 16, dv);
                 cl::tile_load16<TIn>(st, trow, blk * 16, uv);
-                if (has_z) cl::tile_load16<TIn>(st + 2 * W * TILE, trow, blk * 16, zv);
+                // read unconditionally (without z the slot holds stale data, and the gate selects 1)
+                cl::tile_load16<TIn>(st + 2 * W * TILE, trow, blk * 16, zv);
             } else {
                 const TIn* gd = static_cast<const TIn*>(a.delta) + row * a.L;
                 const TIn* gu = static_cast<const TIn*>(a.u) + row * a.L;
@@ -333,34 +356,46 @@ __global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
                 xh[0] = xw[BLK]; xh[1] = xw[BLK + 1]; xh[2] = xw[BLK + 2];
             }
             // per-element work of the block: Delta, Delta*u, D*u, gate
-            float2 dt[BLK / 2], du[BLK / 2], skip[BLK / 2], gate[BLK / 2];
 #pragma unroll
             for (int j = 0; j < BLK / 2; ++j) {
+                // straight-line code (selects, no branches) keeps the block one basic block
                 float2 d2 = make_float2(dv[2 * j] + bias, dv[2 * j + 1] + bias);
-                if (a.softplus) d2 = softplus2(d2);
+                const float2 sp2 = softplus2(d2);
+                d2 = make_float2(softplus ? sp2.x : d2.x, softplus ? sp2.y : d2.y);
                 // steps past the end (or past this segment) leave h unchanged
                 if (to + 2 * j >= t_end) d2.x = 0.f;
                 if (to + 2 * j + 1 >= t_end) d2.y = 0.f;
-                dt[j] = d2;
+                e.dt[j] = d2;
                 const float2 u2 = make_float2(uv[2 * j], uv[2 * j + 1]);
-                du[j] = fmul2(d2, u2);
+                e.du[j] = fmul2(d2, u2);
                 if (!AGG) {
-                    skip[j] = fmul2(make_float2(Dd, Dd), u2);
-                    gate[j] = has_z ? silu2(make_float2(zv[2 * j], zv[2 * j + 1])) : make_float2(1.f, 1.f);
+                    e.skip[j] = fmul2(make_float2(Dd, Dd), u2);
+                    const float2 sg = silu2(make_float2(zv[2 * j], zv[2 * j + 1]));
+                    e.gate[j] = make_float2(has_z ? sg.x : 1.f, has_z ? sg.y : 1.f);
                 }
             }
-            // the recurrence through the block's steps
+#pragma unroll
+            for (int j = 0; j < BLK; ++j) e.uv[j] = uv[j];
+        };
+        // The recurrence through block blk's steps, then its outputs.
+        auto recur = [&](int blk, const Elem& e) {
+            const long long to = tc0 + blk * BLK;
+            const float2* dt = e.dt;
+            const float2* du = e.du;
+            const float2* skip = e.skip;
+            const float2* gate = e.gate;
+            const float* uv = e.uv;
             float yv[BLK];
 #pragma unroll
             for (int j = 0; j < BLK; ++j) {
                 const float dq = (j & 1) ? dt[j / 2].y : dt[j / 2].x;
                 const float duq = (j & 1) ? du[j / 2].y : du[j / 2].x;
                 const float uq = uv[j];
-                const float4* qrow = reinterpret_cast<const float4*>(qbase + (blk * BLK + j) * QPITCH);
+                const float4* qrow = reinterpret_cast<const float4*>(qbase + (blk * BLK + j) * QPITCH) + g * PL;
                 float2 ya = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int p = 0; p < NPAIR; ++p) {
-                    const float4 w = qrow[p];  // (B_n, B_n+1, C_n, C_n+1), the same for every lane
+                for (int p = 0; p < PL; ++p) {
+                    const float4 w = qrow[p];  // (B_n, B_n+1, C_n, C_n+1), the same for every lane of a state group
                     const float2 x = fmul2(make_float2(dq, dq), A2[p]);
                     const float2 abar = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                     if constexpr (ZOH) {
@@ -379,6 +414,7 @@ __global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
                 }
                 if (AGG) sumdt += dq;
                 yv[j] = ya.x + ya.y;
+                if (LPC == 2 && !AGG) yv[j] += __shfl_xor_sync(0xffffffffu, yv[j], 16);
             }
             if (!AGG) {
                 float yo[BLK];
@@ -389,14 +425,21 @@ __global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
                     yo[2 * j + 1] = y2.y;
                 }
                 if (TMA) {
-                    cl::tile_store16<TIn>(ybuf, lane, blk * 16, yo);
-                } else if (cvalid) {
+                    if (g == 0) cl::tile_store16<TIn>(ybuf, c, blk * 16, yo);
+                } else if (cvalid && g == 0) {
                     TIn* gy = static_cast<TIn*>(a.y) + row * a.L;
 #pragma unroll
                     for (int j = 0; j < BLK; ++j)
                         if (to + j < t_end) store_out<TIn>(gy + to + j, yo[j]);
                 }
             }
+                };
+
+#pragma unroll 1
+        for (int blk = 0; blk < TC / BLK; ++blk) {
+            Elem e;
+            elem(blk, e);
+            recur(blk, e);
         }
         __syncwarp();
         mbar_arrive(&empty[s]);
@@ -405,7 +448,7 @@ __global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                tma_store_3d(&maps.y, ybuf, (int)tc0, (u0 + wid) * 32, b);
+                tma_store_3d(&maps.y, ybuf, (int)tc0, (u0 + wid) * CPW, b);
                 bulk_commit();
             }
         }
@@ -420,16 +463,16 @@ __global__ void __launch_bounds__(32 * (cl::kMaxWarps + 1), 1)
     if (AGG) {
         float2* ag = a.agg + (((long long)seg * a.batch + b) * a.dim + dch) * N;
 #pragma unroll
-        for (int p = 0; p < NPAIR; ++p) {
-            const int n0 = 2 * p, n1 = n0 + 1;
+        for (int p = 0; p < PL; ++p) {
+            const int n0 = 2 * (g * PL + p), n1 = n0 + 1;
             if (n0 < N) ag[n0] = make_float2(ex2_approx(A2[p].x * sumdt), h[p].x);
             if (n1 < N) ag[n1] = make_float2(ex2_approx(A2[p].y * sumdt), h[p].y);
         }
     } else if (a.last_state != nullptr && seg == a.nseg - 1) {
         float* ls = a.last_state + row * N;
 #pragma unroll
-        for (int p = 0; p < NPAIR; ++p) {
-            const int n0 = 2 * p, n1 = n0 + 1;
+        for (int p = 0; p < PL; ++p) {
+            const int n0 = 2 * (g * PL + p), n1 = n0 + 1;
             if (n0 < N) ls[n0] = h[p].x;
             if (n1 < N) ls[n1] = h[p].y;
         }

@@ -65,6 +65,9 @@ def parse():
                     help="fwd pass: fuse a causal depthwise convolution of this width (1-4) in front of the scan")
     ap.add_argument("--disc", choices=["simple", "zoh"], default="simple",
                     help="discretisation of B in the forward scan and decode step")
+    ap.add_argument("--seqlen", type=int, default=0,
+                    help="override the workload's sequence length (smaller cases of the same shape, e.g. for "
+                         "profiling under a size limit)")
     ap.add_argument("--kernel", choices=["auto", "lane", "warp"], default="auto",
                     help="forward scan kernel: the library's choice, one channel per lane, or four lanes per channel")
     ap.add_argument("--decode-inputs", type=int, default=200,
@@ -809,7 +812,9 @@ def run_decode(args, cfg, rank, world, local_rank):
                    "elements_per_step": elems_step, "distinct_step_inputs": S, "parallelism": f"replicas x{world}",
                    "l2": "state L2-resident between steps (41.9 MB); step inputs cycle through S distinct sets"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": f"{kind} hbm_gbs",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": ncu_traffic("decode", "state_step") if args.disc == "simple" else None,
+                     "peak_source": f"{kind} hbm_gbs",
                      "kernel": "state_step_kernel", "algorithmic_bytes_per_launch": sb,
                      "kernel_avg_us": round(avg_ms * 1e3, 3)},
         "graph": {"us_per_step": round(graph_ms * 1e3, 3), "steps_per_graph": S,
@@ -913,6 +918,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     cfg = synth.CONFIGS[args.workload]
+    if args.seqlen > 0 and args.workload != "decode":
+        cfg = cfg.replace(seqlen=args.seqlen)
+        WORKLOADS[args.workload] = WORKLOADS[args.workload].replace(
+            f"L {synth.CONFIGS[args.workload].seqlen}", f"L {args.seqlen}")
     if args.impl == "reference" and args.workload == "decode":
         line = run_reference_decode(args, cfg, rank)
     elif args.impl == "reference" and args.which == "bwd":

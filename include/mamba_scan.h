@@ -164,9 +164,17 @@ int mamba_state_step_ex(const mamba_scan_shape* s, int discretization, float* st
  * the per-segment carries go to a fixed scratch array of MAMBA_NOALLOC_SCRATCH_BYTES that the
  * library holds in device memory on every GPU where it is loaded, until the process exits.  No
  * cudaMalloc, cudaMallocAsync, cudaFree or other allocating call is made.
- *  - A shape whose carries need more than MAMBA_NOALLOC_SCRATCH_BYTES
- *    ((segments - 1) * batch * dim * dstate * 8 bytes) is rejected with MAMBA_ERR_ARG and a message
- *    stating both sizes; nothing is launched.
+ *  - A shape whose carries need more than MAMBA_NOALLOC_SCRATCH_BYTES, that is
+ *    (S - 1) * batch * dim * dstate * 8 bytes for S time segments, is rejected with MAMBA_ERR_ARG
+ *    and a message stating both sizes; nothing is launched.  S follows from the shape and the SM
+ *    count nSM of the device, and is at most max(1, seqlen / 256) (fp32) or seqlen / 512 (bf16):
+ *      dstate <= 16: S = 1 unless batch * ceil(dim / 32) <= 2 * nSM; then
+ *                    S <= ceil(4 * nSM / (batch * ceil(dim / 32))) + 1;
+ *      dstate > 16:  S = 1 unless batch * ceil(dim / 8) < 5 * nSM; then
+ *                    S = ceil(10 * nSM / (batch * ceil(dim / 8))).
+ *    For example the million-token workload (batch 1, dim 1536, dstate 16) splits into at most
+ *    14 segments on a 148-SM device, whose carries take at most 2.6 MB; batch 1, dim 32 (two
+ *    segments per 8192 steps or more) takes 4 KB per segment.
  *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
  *    with that device current, then caches it under the unique id of the CUDA context that made
  *    the call; a call from another context, or after cudaDeviceReset, repeats the lookup.  Make

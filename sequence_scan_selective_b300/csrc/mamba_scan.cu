@@ -126,13 +126,18 @@ static int plan_cl(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     long long maxseg = L / (8LL * TC);
     if (maxseg < 1) maxseg = 1;
     if (maxseg > 4096) maxseg = 4096;
+    // the time axis is split only when the units fill at most half of the 4 * nsm sub-partitions,
+    // into at most ceil(4 * nsm / units) + 1 segments (a bound callers of the allocation-free entry
+    // point can compute)
+    const long long units = (long long)s->batch * p.upr, slots = 4LL * nsm;
+    const long long smax = units * 2 <= slots ? (slots + units - 1) / units + 1 : 1;
     long long best = 1;
     const long long want = env_int("MAMBA_SCAN_NSEG", 0);
     if (want > 0) {
         best = want < maxseg ? want : maxseg;
     } else {
         double best_cost = 0.0;
-        for (long long ns = 1; ns <= maxseg && ns <= 4LL * nsm; ++ns) {
+        for (long long ns = 1; ns <= maxseg && ns <= smax; ++ns) {
             const long long seg = (L + ns - 1) / ns;
             const long long segr = (seg + TC - 1) / TC * TC;
             const long long nseg = (L + segr - 1) / segr;
@@ -541,20 +546,17 @@ static int check_shape(const mamba_scan_shape* s, bool need_len) {
 template <typename TIn, int NP>
 static int step_dispatch(const StepArgs& a, cudaStream_t st) {
     constexpr int S = NP / (NP < 8 ? NP : 8);  // threads per channel (state_step_kernel)
-    const long long threads = (long long)a.batch * a.dim * S;
     const int bs = 256;
-    const long long blocks = (threads + bs - 1) / bs;
-    if (blocks > 0x7fffffffLL) return fail(MAMBA_ERR_ARG, "too many channels");
-    // vector accesses: whole rows of NP states, 16-byte aligned state and A rows, B/C rows aligned
-    // to their 4-element loads
-    const uintptr_t bc_align = sizeof(TIn) == 4 ? 15u : 7u;
-    const bool vec4 = (a.dstate == NP) && aligned16(a.state) && aligned16(a.A) &&
-                      (reinterpret_cast<uintptr_t>(a.B) & bc_align) == 0 &&
-                      (reinterpret_cast<uintptr_t>(a.C) & bc_align) == 0;
+    const long long gx = ((long long)a.dim * S + bs - 1) / bs;  // blocks over channels
+    const long long gy = ((long long)a.batch + kStepRows - 1) / kStepRows;
+    if (gx > 0x7fffffffLL || gy > 65535) return fail(MAMBA_ERR_ARG, "too many channels or batch rows");
+    const dim3 grid((unsigned)gx, (unsigned)gy);
+    // vector accesses: whole rows of NP states, 16-byte aligned state and A rows
+    const bool vec4 = (a.dstate == NP) && aligned16(a.state) && aligned16(a.A);
     if (vec4)
-        state_step_kernel<TIn, NP, true><<<(unsigned)blocks, bs, 0, st>>>(a);
+        state_step_kernel<TIn, NP, true><<<grid, bs, 0, st>>>(a);
     else
-        state_step_kernel<TIn, NP, false><<<(unsigned)blocks, bs, 0, st>>>(a);
+        state_step_kernel<TIn, NP, false><<<grid, bs, 0, st>>>(a);
     g_launches.fetch_add(1, std::memory_order_relaxed);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "state_step_kernel launch");

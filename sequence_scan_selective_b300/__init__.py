@@ -9,6 +9,7 @@ Entry points (names as in include/mamba_scan.h):
   mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, y=None, last_state=None, h0=None,
                  disc="simple")   (h0 -> mamba_scan_fwd_state; disc="zoh" -> mamba_scan_fwd_ex)
   mamba_scan_fwd_noalloc(...)   same arguments; the library allocates no device memory
+  mamba_scan_fwd_pipelined(...)  the scan of host-resident inputs, batch rows pipelined over streams
   mamba_state_step(state, x, delta, A, B, C, D, z, delta_bias, softplus, y=None)
   mamba_scan_bwd(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0=None, dlast_state=None)
   selective_scan(u, delta, A, B, C, D, z, delta_bias, softplus, h0=None, disc="simple")
@@ -351,6 +352,84 @@ def prepare_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, sof
                                  stream, out)
     keep = (shape, u, delta, A, B, C, dy, D, z, delta_bias, h0, dlast_state, out)
     return PreparedCall(_lib.mamba_scan_bwd, args, keep), out
+
+
+class _HostPipeline:
+    """Device staging buffers and streams of mamba_scan_fwd_pipelined for one shape (kept between
+    calls, so that steady use allocates nothing)."""
+
+    def __init__(self, device, dim, N, L, dtype):
+        f = dict(device=device, dtype=dtype)
+        self.x = [{k: torch.empty((1, dim, L), **f) for k in ("u", "delta", "z")} for _ in range(2)]
+        for slot in self.x:
+            slot["B"] = torch.empty((1, N, L), **f)
+            slot["C"] = torch.empty((1, N, L), **f)
+            slot["y"] = torch.empty((1, dim, L), **f)
+        self.streams = [torch.cuda.Stream(device) for _ in range(3)]  # copy in, scan, copy out
+        self.key = (device, dim, N, L, dtype)
+
+
+_pipelines = {}
+
+
+def mamba_scan_fwd_pipelined(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
+                             last_state=None, stream=None):
+    """The forward scan of inputs that live in host memory, with y copied back to host memory.
+
+    u, delta, z [b, d, L] and B, C [b, N, L] are CPU tensors (pinned, for asynchronous copies); A, D,
+    delta_bias are CUDA tensors as for mamba_scan_fwd.  y (CPU, pinned; allocated when None) receives
+    the output and last_state (CUDA, [b, d, N] float32; allocated when None) the final state.  The
+    batch rows go through in turn on three streams, so that the copy of one row's inputs to the
+    device, the scan of the previous row (mamba_scan_fwd on that row) and the copy of the row
+    before back to the host overlap; device staging is double-buffered and kept for the next call
+    of the same shape.  The work is ordered after `stream` (default: the current stream) and the
+    current stream waits for all of it, so y may be read after synchronising that stream."""
+    bsz, dim, L = u.shape
+    N = A.shape[1]
+    dev = A.device
+    cur = stream if stream is not None else torch.cuda.current_stream(dev)
+    key = (dev, dim, N, L, u.dtype)
+    pipe = _pipelines.get(key)
+    if pipe is None:
+        pipe = _pipelines[key] = _HostPipeline(dev, dim, N, L, u.dtype)
+    if y is None:
+        y = torch.empty_like(u).pin_memory()
+    if last_state is None:
+        last_state = torch.empty((bsz, dim, N), device=dev, dtype=torch.float32)
+    s_in, s_scan, s_out = pipe.streams
+    for s_ in pipe.streams:
+        s_.wait_stream(cur)
+    scanned = [None, None]   # per slot: event after the scan that last used it
+    copied_out = [None, None]  # per slot: event after the copy-out that last read its y
+    for i in range(bsz):
+        slot = i % 2
+        buf = pipe.x[slot]
+        with torch.cuda.stream(s_in):
+            if scanned[slot] is not None:
+                s_in.wait_event(scanned[slot])
+            for k, src in (("u", u), ("delta", delta), ("z", z), ("B", B), ("C", C)):
+                if src is not None:
+                    buf[k].copy_(src[i:i + 1], non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(s_in)
+        with torch.cuda.stream(s_scan):
+            s_scan.wait_event(ready)
+            if copied_out[slot] is not None:
+                s_scan.wait_event(copied_out[slot])
+            mamba_scan_fwd(buf["u"], buf["delta"], A, buf["B"], buf["C"], D, buf["z"] if z is not None else None,
+                           delta_bias, softplus, y=buf["y"], last_state=last_state[i:i + 1], stream=s_scan)
+            done = torch.cuda.Event()
+            done.record(s_scan)
+            scanned[slot] = done
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(done)
+            y[i:i + 1].copy_(buf["y"], non_blocking=True)
+            out = torch.cuda.Event()
+            out.record(s_out)
+            copied_out[slot] = out
+    cur.wait_stream(s_scan)
+    cur.wait_stream(s_out)
+    return y, last_state
 
 
 class _SelectiveScan(torch.autograd.Function):

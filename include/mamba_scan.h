@@ -72,9 +72,15 @@ typedef struct {
  *                            any input.
  *   last_state    [b, d, N]  fp32 or NULL: h after the last position (zeros when L == 0).
  *
- * Sequences with few channels (b*d small against the GPU) are split along L: a first kernel
- * computes per-segment carries into stream-ordered scratch memory (cudaMallocAsync on `stream`,
- * freed on the same stream), a second kernel runs the fused scan per segment from its carry.
+ * Sequences with few channels (b*d small against the GPU) are split along L into segments that
+ * exchange carries (prod Abar, end state) through stream-ordered scratch memory (cudaMallocAsync
+ * on `stream`, freed on the same stream).  dstate <= 16: one kernel scans every segment at once
+ * (the first from the initial state, the others from zero) and a second adds to each later
+ * segment's outputs the decaying part of the state carried into it, dropping it once it has
+ * decayed below 2^-40 of its size at the segment start (visual guide section 3.3, associativity
+ * of the scan).  dstate > 16: a first kernel computes the carries and a second runs the fused
+ * scan per segment from its folded carry.  With bf16 y, outputs a segment's correction reaches
+ * are rounded twice (own part, then the sum).
  * Errors: MAMBA_ERR_ARG for bad arguments, MAMBA_ERR_CUDA if an allocation or launch fails.
  */
 int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const void* delta, const float* A,
@@ -165,7 +171,8 @@ int mamba_state_step_ex(const mamba_scan_shape* s, int discretization, float* st
  * library holds in device memory on every GPU where it is loaded, until the process exits.  No
  * cudaMalloc, cudaMallocAsync, cudaFree or other allocating call is made.
  *  - A shape whose carries need more than MAMBA_NOALLOC_SCRATCH_BYTES, that is
- *    (S - 1) * batch * dim * dstate * 8 bytes for S time segments, is rejected with MAMBA_ERR_ARG
+ *    S * batch * dim * dstate * 8 bytes for S time segments when dstate <= 16 (S - 1 instead of
+ *    S when dstate > 16), is rejected with MAMBA_ERR_ARG
  *    and a message stating both sizes; nothing is launched.  S follows from the shape and the SM
  *    count nSM of the device, and is at most max(1, seqlen / 256) (fp32) or seqlen / 512 (bf16):
  *      dstate <= 16: S = 1 unless batch * ceil(dim / 32) <= 2 * nSM; then
@@ -173,8 +180,8 @@ int mamba_state_step_ex(const mamba_scan_shape* s, int discretization, float* st
  *      dstate > 16:  S = 1 unless batch * ceil(dim / 8) < 5 * nSM; then
  *                    S = ceil(10 * nSM / (batch * ceil(dim / 8))).
  *    For example the million-token workload (batch 1, dim 1536, dstate 16) splits into at most
- *    14 segments on a 148-SM device, whose carries take at most 2.6 MB; batch 1, dim 32 (two
- *    segments per 8192 steps or more) takes 4 KB per segment.
+ *    14 segments on a 148-SM device, whose carries take at most 2.8 MB; batch 1, dim 32 takes
+ *    4 KB per segment.
  *  - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
  *    with that device current, then caches it under the unique id of the CUDA context that made
  *    the call; a call from another context, or after cudaDeviceReset, repeats the lookup.  Make

@@ -10,14 +10,13 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmambascan.so")
 SOURCES = ["mamba_scan.cu"]
-HEADERS = ["ptx.cuh", "common.cuh", "scan_fwd.cuh", "scan_fwd_cl.cuh", "scan_bwd.cuh", "state_step.cuh"]
+HEADERS = ["ptx.cuh", "common.cuh", "scan_fwd.cuh", "scan_fwd_cl.cuh", "scan_fix.cuh", "scan_bwd.cuh", "state_step.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
     "-Xcompiler", "-fPIC", "-shared",
     "--expt-relaxed-constexpr",
-    "--split-compile", "0",  # optimise the many kernel instantiations on all host threads
 ]
 
 

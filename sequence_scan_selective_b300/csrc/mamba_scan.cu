@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "scan_fwd.cuh"
 #include "scan_fwd_cl.cuh"
+#include "scan_fix.cuh"
 #include "scan_bwd.cuh"
 #include "state_step.cuh"
 
@@ -99,8 +100,11 @@ static int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 // Segments and CTAs for the channel-per-lane kernel.  A CTA runs one (segment, batch row) range of
 // at most wcap units, every warp on its own SM sub-partition, so a launch takes about
-// waves * segment length; a split adds the aggregate launch (about 3/4 of a segment's work, for
-// all but the last segment).  The segment count minimises that estimate.
+// waves * segment length; a split adds the fix-up launch, which walks each later segment until
+// the carried-in state has decayed (modelled as kFixSteps steps, at most the segment).  The
+// segment count minimises that estimate.
+constexpr long long kFixSteps = 4096;
+
 template <typename TIn, int NP, int LPC>
 static int plan_cl(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     constexpr int TC = Chunk<TIn>::TC;
@@ -145,7 +149,7 @@ static int plan_cl(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
             const long long k = kcta_of((long long)s->batch * ns);
             const long long waves = ((long long)s->batch * ns * k + nsm - 1) / nsm;
             double cost = (double)waves * segr;
-            if (ns > 1) cost += 0.75 * (double)(((long long)s->batch * (ns - 1) * k + nsm - 1) / nsm) * segr;
+            if (ns > 1) cost += (double)(segr < kFixSteps ? segr : kFixSteps);
             if (ns == 1 || cost < best_cost * 0.98) {
                 best_cost = cost;
                 best = ns;
@@ -310,25 +314,42 @@ static int launch_kernel(void (*kern)(const FwdArgs, const FwdMaps), AttrCache& 
 
 // Channel-per-lane kernel: data path and discretisation / convolution mode are template
 // parameters; softplus and the gate are runtime flags.
-template <typename TIn, int NP, int LPC, bool TMA, bool AGG, int MODE>
+template <typename TIn, int NP, int LPC, bool TMA, bool LOCAL, int MODE>
 static int launch_cl_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
     static AttrCache attr;
-    return launch_kernel(scan_fwd_cl_kernel<TIn, NP, LPC, TMA, AGG, MODE>, attr, a, maps, grid, smem_bytes, st);
+    return launch_kernel(scan_fwd_cl_kernel<TIn, NP, LPC, TMA, LOCAL, MODE>, attr, a, maps, grid, smem_bytes, st);
 }
 
-template <typename TIn, int NP, int LPC, bool AGG>
+template <typename TIn, int NP, int LPC, bool LOCAL>
 static int launch_cl(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, bool tma, int mode,
                      cudaStream_t st) {
     switch (mode) {
-        case 0: return tma ? launch_cl_one<TIn, NP, LPC, true, AGG, 0>(a, maps, grid, smem_bytes, st)
-                           : launch_cl_one<TIn, NP, LPC, false, AGG, 0>(a, maps, grid, smem_bytes, st);
-        case 1: return tma ? launch_cl_one<TIn, NP, LPC, true, AGG, 1>(a, maps, grid, smem_bytes, st)
-                           : launch_cl_one<TIn, NP, LPC, false, AGG, 1>(a, maps, grid, smem_bytes, st);
-        case 2: return tma ? launch_cl_one<TIn, NP, LPC, true, AGG, 2>(a, maps, grid, smem_bytes, st)
-                           : launch_cl_one<TIn, NP, LPC, false, AGG, 2>(a, maps, grid, smem_bytes, st);
-        default: return tma ? launch_cl_one<TIn, NP, LPC, true, AGG, 3>(a, maps, grid, smem_bytes, st)
-                            : launch_cl_one<TIn, NP, LPC, false, AGG, 3>(a, maps, grid, smem_bytes, st);
+        case 0: return tma ? launch_cl_one<TIn, NP, LPC, true, LOCAL, 0>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, LPC, false, LOCAL, 0>(a, maps, grid, smem_bytes, st);
+        case 1: return tma ? launch_cl_one<TIn, NP, LPC, true, LOCAL, 1>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, LPC, false, LOCAL, 1>(a, maps, grid, smem_bytes, st);
+        case 2: return tma ? launch_cl_one<TIn, NP, LPC, true, LOCAL, 2>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, LPC, false, LOCAL, 2>(a, maps, grid, smem_bytes, st);
+        default: return tma ? launch_cl_one<TIn, NP, LPC, true, LOCAL, 3>(a, maps, grid, smem_bytes, st)
+                            : launch_cl_one<TIn, NP, LPC, false, LOCAL, 3>(a, maps, grid, smem_bytes, st);
     }
+}
+
+// The second launch of a split time axis (channel-per-lane kernel): one warp per (segment > 0,
+// batch row, 32 channels).
+template <typename TIn, int NP>
+static int launch_fix(const FwdArgs& a, const FixMaps& maps, bool tma, cudaStream_t st) {
+    static AttrCache attr[2];
+    auto kern = tma ? scan_fix_kernel<TIn, NP, true> : scan_fix_kernel<TIn, NP, false>;
+    int rc = allow_smem(kern, attr[tma ? 1 : 0]);
+    if (rc) return rc;
+    const long long items = (long long)(a.nseg - 1) * a.batch * a.upr;
+    if (items > 0x7fffffffLL) return fail(MAMBA_ERR_ARG, "grid too large");
+    kern<<<(unsigned)items, 32, fix::Layout<NP>::SMEM, st>>>(a, maps);
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "split-scan fix-up kernel launch");
+    return MAMBA_OK;
 }
 
 template <FwdKernel KIND, typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE>
@@ -435,13 +456,21 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
         a.test_stall = 1;
     }
 
+    // Split time axis.  Channel-per-lane kernel: every segment runs at once (segment 0 from the
+    // initial state, the others from zero) and writes its carry; scan_fix_kernel then folds the
+    // carries and adds the carried-in part to the later segments' outputs.  scan_fwd_kernel: an
+    // aggregate launch writes the carries of all but the last segment, and the full launch folds
+    // them into each segment's initial state.
+    constexpr bool kLocal = KIND == FwdKernel::kChannelLane;
     bool owned = false;
     if (p.nseg > 1) {
         const size_t nstate = (size_t)s->batch * s->dim * s->dstate;
-        const size_t bytes = (size_t)(p.nseg - 1) * nstate * sizeof(float2);
-        // An initial state that shares memory with last_state is copied first: the last segment
-        // writes last_state while CTAs of earlier segments may still be reading the initial state.
-        const bool copy_h0 = a.h0 != nullptr && overlaps(a.h0, nstate * 4, a.last_state, nstate * 4);
+        const size_t bytes = (size_t)(kLocal ? p.nseg : p.nseg - 1) * nstate * sizeof(float2);
+        // scan_fwd_kernel: an initial state that shares memory with last_state is copied first
+        // (the last segment writes last_state while CTAs of earlier segments may still be reading
+        // the initial state).  The channel-per-lane split reads the initial state in its first
+        // launch and writes last_state in its second.
+        const bool copy_h0 = !kLocal && a.h0 != nullptr && overlaps(a.h0, nstate * 4, a.last_state, nstate * 4);
         const size_t total = bytes + (copy_h0 ? nstate * sizeof(float) : 0);
         if (copy_h0 && scratch != nullptr) return fail(MAMBA_ERR_ARG, "internal: initial state with fixed scratch");
         if (scratch != nullptr) {
@@ -463,18 +492,33 @@ static int fwd_run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gat
                 a.h0 = hcopy;
             }
         }
-        const unsigned g1 = (unsigned)((long long)s->batch * (p.nseg - 1) * p.kcta);
-        if constexpr (KIND == FwdKernel::kChannelLane)
-            rc = launch_cl<TIn, NP, LPC, true>(a, maps, g1, p.smem_bytes, tma_ok, mode, st);
-        else
+        const unsigned grid = (unsigned)((long long)s->batch * p.nseg * p.kcta);
+        if constexpr (kLocal) {
+            rc = launch_cl<TIn, NP, LPC, true>(a, maps, grid, p.smem_bytes, tma_ok, mode, st);
+            if (rc == MAMBA_OK) {
+                FixMaps fm;
+                memset(&fm, 0, sizeof fm);
+                if (tma_ok) {
+                    bool ok = encode_3d(&fm.d, a.delta, esize, L, s->dim, s->batch, TC, 32) &&
+                              encode_3d(&fm.z, a.z ? a.z : a.delta, esize, L, s->dim, s->batch, TC, 32);
+                    if (!ok) rc = fail(MAMBA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+                    fm.y = maps.y;
+                    fm.C = maps.C;
+                }
+                if (rc == MAMBA_OK) rc = launch_fix<TIn, NP>(a, fm, tma_ok, st);
+            }
+        } else {
+            const unsigned g1 = (unsigned)((long long)s->batch * (p.nseg - 1) * p.kcta);
             rc = launch_fwd<KIND, TIn, NP, true>(a, maps, g1, p.smem_bytes, tma_ok, softplus, gate, st);
-    }
-    if (rc == MAMBA_OK) {
-        const unsigned g2 = (unsigned)((long long)s->batch * p.nseg * p.kcta);
-        if constexpr (KIND == FwdKernel::kChannelLane)
-            rc = launch_cl<TIn, NP, LPC, false>(a, maps, g2, p.smem_bytes, tma_ok, mode, st);
+            if (rc == MAMBA_OK)
+                rc = launch_fwd<KIND, TIn, NP, false>(a, maps, grid, p.smem_bytes, tma_ok, softplus, gate, st);
+        }
+    } else {
+        const unsigned grid = (unsigned)((long long)s->batch * p.kcta);
+        if constexpr (kLocal)
+            rc = launch_cl<TIn, NP, LPC, false>(a, maps, grid, p.smem_bytes, tma_ok, mode, st);
         else
-            rc = launch_fwd<KIND, TIn, NP, false>(a, maps, g2, p.smem_bytes, tma_ok, softplus, gate, st);
+            rc = launch_fwd<KIND, TIn, NP, false>(a, maps, grid, p.smem_bytes, tma_ok, softplus, gate, st);
     }
     if (owned) {
         cudaError_t e = cudaFreeAsync(a.agg, st);

@@ -21,10 +21,12 @@
 //    forms keep the FP32 pipe and the MUFU pipe busy together.
 //  * u, delta, z arrive by TMA as [32 * warps, TC] tiles (128-byte swizzle); y leaves by TMA
 //    store from a per-warp staging tile in the same layout.
-//  * Few channels (long sequences): the time axis is split into segments exactly as in
-//    scan_fwd_kernel (an aggregate launch computes every segment's (prod Abar, h_end from zero);
-//    the full launch folds the carries of earlier segments into its initial state), regrouping
-//    the associative scan operator (guide section 3.3).
+//  * Few channels (long sequences): the time axis is split into segments that all run at once
+//    (LOCAL): segment 0 from the initial state, every later one from zero.  Each writes its
+//    outputs and its carry (prod Abar, h_end); scan_fix_kernel then adds to each later segment's
+//    outputs the part of the state carried in from before it, which decays from the segment's
+//    start on (the scan operator is associative and the recurrence linear in h: guide section
+//    3.3).
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
@@ -98,7 +100,7 @@ __device__ __forceinline__ void tile_store16<uint16_t>(unsigned char* tile, int 
 // convolution in front of the scan (guide section 3.5): the u tile then holds the block input x,
 // and the lane forms u[t] = act(conv_bias + sum_k conv_w[k] x[t-K+1+k]) itself, keeping the last
 // three inputs of its channel in registers from block to block.
-template <typename TIn, int NP, int LPC, bool TMA, bool AGG, int MODE>
+template <typename TIn, int NP, int LPC, bool TMA, bool LOCAL, int MODE>
 __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
     scan_fwd_cl_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps) {
     constexpr int TC = Chunk<TIn>::TC;
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
     constexpr int TILE = CPW * cl::kRowBytes;  // one warp's rows of one input tile
     constexpr bool ZOH = (MODE & 1) != 0;
     constexpr bool CONV = (MODE & 2) != 0;
-    const bool has_z = !AGG && a.z != nullptr;
+    const bool has_z = a.z != nullptr;
     const bool softplus = a.softplus != 0;
     static_assert(NP % (2 * LPC) == 0 && NP <= 16 && (LPC == 1 || LPC == 2), "shape");
 
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
     if (wid == W) {
         // ================================================================== producer warp
         const int mi = nunits == a.wlo ? 0 : 1;
-        const uint32_t tx = (uint32_t)(nunits * TILE * (has_z ? 3 : 2) + (AGG ? 1 : 2) * N * cl::kRowBytes);
+        const uint32_t tx = (uint32_t)(nunits * TILE * (has_z ? 3 : 2) + 2 * N * cl::kRowBytes);
         auto issue = [&](int k) {  // lane 0: TMA loads of chunk k into stage k % NS
             const int s = k % NS;
             unsigned char* st = smem + s * a.stage_bytes;
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
             tma_load_3d(st + W * TILE, &maps.d[mi], &full[s], t0, r0, b);
             if (has_z) tma_load_3d(st + 2 * W * TILE, &maps.z[mi], &full[s], t0, r0, b);
             tma_load_3d(st + a.bc_off, &maps.B, &full[s], t0, 0, b);
-            if (!AGG) tma_load_3d(st + a.bc_off + NP * cl::kRowBytes, &maps.C, &full[s], t0, 0, b);
+            tma_load_3d(st + a.bc_off + NP * cl::kRowBytes, &maps.C, &full[s], t0, 0, b);
         };
         // chunk k's B, C as (B_n, B_n+1, C_n, C_n+1) quads per step; lane handles steps lane + 32 i
         auto build_quads = [&](int k) {
@@ -182,17 +184,17 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
                         if (TMA) {
                             if constexpr (ES == 4) {
                                 bv[n] = *reinterpret_cast<const float*>(tB + swz128(n, t * 4));
-                                if (!AGG) cv[n] = *reinterpret_cast<const float*>(tC + swz128(n, t * 4));
+                                cv[n] = *reinterpret_cast<const float*>(tC + swz128(n, t * 4));
                             } else {
                                 bv[n] = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(tB + swz128(n, t * 2)));
-                                if (!AGG) cv[n] = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(tC + swz128(n, t * 2)));
+                                cv[n] = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(tC + swz128(n, t * 2)));
                             }
                         } else {
                             const long long tg = t_begin + (long long)k * TC + t;
                             if (tg < t_end) {
                                 const long long off = ((long long)b * N + n) * a.L + tg;
                                 bv[n] = In<TIn>::to_f32(static_cast<const TIn*>(a.B)[off]);
-                                if (!AGG) cv[n] = In<TIn>::to_f32(static_cast<const TIn*>(a.C)[off]);
+                                cv[n] = In<TIn>::to_f32(static_cast<const TIn*>(a.C)[off]);
                             }
                         }
                     }
@@ -247,12 +249,13 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
     const bool cvalid = dch < a.dim;
     const long long row = (long long)b * a.dim + (cvalid ? dch : 0);
     const float bias = (cvalid && a.bias != nullptr) ? a.bias[dch] : 0.f;
-    const float Dd = (!AGG && cvalid && a.D != nullptr) ? a.D[dch] : 0.f;
+    const float Dd = (cvalid && a.D != nullptr) ? a.D[dch] : 0.f;
     const int trow = wid * CPW + c;  // this lane's row in the CTA's u, delta, z tiles
 
     // the lane's states: pairs g * PL .. g * PL + PL - 1
     float2 A2[PL], h[PL], invA[ZOH ? PL : 1];
-    const float* h0 = (!AGG && cvalid && a.h0 != nullptr) ? a.h0 + row * N : nullptr;
+    // segment 0 starts from the initial state, later segments (LOCAL) from zero
+    const float* h0 = (seg == 0 && cvalid && a.h0 != nullptr) ? a.h0 + row * N : nullptr;
 #pragma unroll
     for (int p = 0; p < PL; ++p) {
         const int n0 = 2 * (g * PL + p), n1 = n0 + 1;
@@ -282,18 +285,6 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
                 xh[q] = a.conv_prev[row * (K - 1) + (K - 1) + pos];
         }
     }
-    if (!AGG && seg > 0 && cvalid) {
-        // fold the carries of segments 0 .. seg-1 in order: h <- prod Abar * h + h_end
-        for (int q = 0; q < seg; ++q) {
-            const float2* ag = a.agg + (((long long)q * a.batch + b) * a.dim + dch) * N;
-#pragma unroll
-            for (int p = 0; p < PL; ++p) {
-                const int n0 = 2 * (g * PL + p), n1 = n0 + 1;
-                if (n0 < N) { const float2 v = ag[n0]; h[p].x = fmaf(v.x, h[p].x, v.y); }
-                if (n1 < N) { const float2 v = ag[n1]; h[p].y = fmaf(v.x, h[p].y, v.y); }
-            }
-        }
-    }
 
     constexpr int YTILE = cl::Lanes<LPC>::YTILE;
     unsigned char* ystage = smem + a.scratch_off + wid * 2 * YTILE;
@@ -310,7 +301,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
         const unsigned char* st = smem + s * a.stage_bytes;
         const unsigned char* qbase = st + a.quad_off;
         unsigned char* ybuf = ystage + (k & 1) * YTILE;
-        if (TMA && !AGG && k >= 2) {  // the store issued from this buffer two chunks ago has read it
+        if (TMA && k >= 2) {  // the store issued from this buffer two chunks ago has read it
             if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
         }
@@ -368,11 +359,9 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
                 e.dt[j] = d2;
                 const float2 u2 = make_float2(uv[2 * j], uv[2 * j + 1]);
                 e.du[j] = fmul2(d2, u2);
-                if (!AGG) {
-                    e.skip[j] = fmul2(make_float2(Dd, Dd), u2);
-                    const float2 sg = silu2(make_float2(zv[2 * j], zv[2 * j + 1]));
-                    e.gate[j] = make_float2(has_z ? sg.x : 1.f, has_z ? sg.y : 1.f);
-                }
+                e.skip[j] = fmul2(make_float2(Dd, Dd), u2);
+                const float2 sg = silu2(make_float2(zv[2 * j], zv[2 * j + 1]));
+                e.gate[j] = make_float2(has_z ? sg.x : 1.f, has_z ? sg.y : 1.f);
             }
 #pragma unroll
             for (int j = 0; j < BLK; ++j) e.uv[j] = uv[j];
@@ -410,30 +399,28 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
                         const float2 bx = fmul2(make_float2(duq, duq), make_float2(w.x, w.y));
                         h[p] = ffma2(abar, h[p], bx);
                     }
-                    if (!AGG) ya = ffma2(make_float2(w.z, w.w), h[p], ya);
+                    ya = ffma2(make_float2(w.z, w.w), h[p], ya);
                 }
-                if (AGG) sumdt += dq;
+                if (LOCAL) sumdt += dq;
                 yv[j] = ya.x + ya.y;
-                if (LPC == 2 && !AGG) yv[j] += __shfl_xor_sync(0xffffffffu, yv[j], 16);
+                if (LPC == 2) yv[j] += __shfl_xor_sync(0xffffffffu, yv[j], 16);
             }
-            if (!AGG) {
-                float yo[BLK];
+            float yo[BLK];
 #pragma unroll
-                for (int j = 0; j < BLK / 2; ++j) {
-                    const float2 y2 = fmul2(fadd2(make_float2(yv[2 * j], yv[2 * j + 1]), skip[j]), gate[j]);
-                    yo[2 * j] = y2.x;
-                    yo[2 * j + 1] = y2.y;
-                }
-                if (TMA) {
-                    if (g == 0) cl::tile_store16<TIn>(ybuf, c, blk * 16, yo);
-                } else if (cvalid && g == 0) {
-                    TIn* gy = static_cast<TIn*>(a.y) + row * a.L;
-#pragma unroll
-                    for (int j = 0; j < BLK; ++j)
-                        if (to + j < t_end) store_out<TIn>(gy + to + j, yo[j]);
-                }
+            for (int j = 0; j < BLK / 2; ++j) {
+                const float2 y2 = fmul2(fadd2(make_float2(yv[2 * j], yv[2 * j + 1]), skip[j]), gate[j]);
+                yo[2 * j] = y2.x;
+                yo[2 * j + 1] = y2.y;
             }
-                };
+            if (TMA) {
+                if (g == 0) cl::tile_store16<TIn>(ybuf, c, blk * 16, yo);
+            } else if (cvalid && g == 0) {
+                TIn* gy = static_cast<TIn*>(a.y) + row * a.L;
+#pragma unroll
+                for (int j = 0; j < BLK; ++j)
+                    if (to + j < t_end) store_out<TIn>(gy + to + j, yo[j]);
+            }
+        };
 
 #pragma unroll 1
         for (int blk = 0; blk < TC / BLK; ++blk) {
@@ -443,7 +430,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
         }
         __syncwarp();
         mbar_arrive(&empty[s]);
-        if (TMA && !AGG) {
+        if (TMA) {
             // the warp's y tile of this chunk -> global (rows past dim and columns past L clipped)
             fence_proxy_async_smem();
             __syncwarp();
@@ -453,14 +440,15 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
             }
         }
     }
-    if (TMA && !AGG && lane == 0) bulk_wait_all<0>();  // stores complete before the CTA can exit
+    if (TMA && lane == 0) bulk_wait_all<0>();  // stores complete before the CTA can exit
     __syncwarp();
     if (!ok) {
         if (lane == 0) atomicExch(&g_status, 1);
         return;
     }
     if (!cvalid) return;
-    if (AGG) {
+    if (LOCAL) {
+        // this segment's carry: (prod Abar = 2^(A log2(e) sum Delta), end state from its own start)
         float2* ag = a.agg + (((long long)seg * a.batch + b) * a.dim + dch) * N;
 #pragma unroll
         for (int p = 0; p < PL; ++p) {
@@ -468,7 +456,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
             if (n0 < N) ag[n0] = make_float2(ex2_approx(A2[p].x * sumdt), h[p].x);
             if (n1 < N) ag[n1] = make_float2(ex2_approx(A2[p].y * sumdt), h[p].y);
         }
-    } else if (a.last_state != nullptr && seg == a.nseg - 1) {
+    } else if (a.last_state != nullptr) {
         float* ls = a.last_state + row * N;
 #pragma unroll
         for (int p = 0; p < PL; ++p) {

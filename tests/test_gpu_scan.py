@@ -182,6 +182,46 @@ def test_segment_count_invariance(ms, kernel):
         assert rel_err(st, outs[0][1]) <= 1e-5
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_split_without_decay(ms, kernel, dtype):
+    """States with A = 0 never forget: the state carried into a later segment reaches every one
+    of its outputs, so the channel-per-lane split must carry it through the whole segment (no
+    early stop), alongside decaying states in the same lanes."""
+    cfg = synth.CONFIGS["long"].replace(batch=1, dim=40, seqlen=6000, dtype=dtype, seed=26)
+    inp = synth.scan_inputs(cfg)
+    inp["A"] = inp["A"].copy()
+    inp["A"][:, :3] = 0.0
+    inp["A"][5, :] = 0.0  # one channel with no decay at all
+    y_ref, st_ref = oracle_scan_full(inp, dtype, True)
+    with _env(**_kenv(kernel, MAMBA_SCAN_NSEG="4")):
+        y, st = _run_gpu(ms, dev_inputs(inp, dtype))
+    assert rel_err(from_dev(y), y_ref) <= TOL[dtype]
+    assert rel_err(from_dev(st), st_ref) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_split_large_initial_state(ms, kernel):
+    """A large initial state dominates the early outputs of every segment it reaches; the split
+    must match the oracle there too (the carried-in part is dropped only once it has decayed far
+    below the outputs' resolution)."""
+    cfg = synth.CONFIGS["long"].replace(batch=2, dim=36, seqlen=5000, seed=27)
+    inp = synth.scan_inputs(cfg)
+    inp["A"] = inp["A"].copy()
+    inp["A"][:, ::2] *= 0.02  # slow decay: the carry reaches far into the following segments
+    h0 = (np.random.default_rng(27).standard_normal((cfg.batch, cfg.dim, cfg.dstate)) * 1e3).astype(np.float32)
+    y_ref, st_ref = oracle.scan(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                inp["delta_bias"], True, cfg.dtype, h0=h0.astype(np.float64))
+    d = dev_inputs(inp, cfg.dtype)
+    with _env(**_kenv(kernel, MAMBA_SCAN_NSEG="5")):
+        y, st = ms.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"], True,
+                                  h0=torch.from_numpy(h0).cuda())
+        torch.cuda.synchronize()
+        ms.device_status()
+    assert rel_err(from_dev(y), y_ref) <= TOL["f32"]
+    assert rel_err(from_dev(st), st_ref) <= TOL["f32"]
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_kernels_agree(ms, dtype):
     """Both forward kernels compute the same scan (to rounding) on a shape several CTAs wide."""

@@ -12,7 +12,9 @@ force, the scalar-state closed form, the one-step formula, the Delta -> 0 and De
 limits, linearity in the input, the decode step against the scan).
 ``tests/test_oracle_grad_pins.py`` pins the exact zero-order hold (against a numerical solution of
 the held-input ODE by scipy) and the gradients (against Richardson-extrapolated central
-differences of the forward, input by input).
+differences of the forward, input by input).  ``tests/test_oracle_conv_pins.py`` pins the causal
+convolution (against numpy's convolve) and its gradient ``causal_conv_bwd`` (against central
+differences of a numpy-convolve forward, and the full-convolution form of the input gradient).
 """
 from __future__ import annotations
 
@@ -268,3 +270,52 @@ def causal_conv(x, w, conv_bias=None, silu=True, dtype="f32", x_prev=None):
     u = causal_conv_rows(np.arange(bsz * dim), dim, np.asarray(x).reshape(bsz * dim, L), w, conv_bias, silu,
                          dtype, prev)
     return u.reshape(bsz, dim, L)
+
+
+def _as_f64(x, dtype):
+    """Storage values as float64: bf16 bit patterns widened exactly, fp32 / float64 as they are."""
+    if dtype == "bf16":
+        bits = np.asarray(x, dtype=np.uint16).astype(np.uint32) << 16
+        return bits.view(np.float32).astype(np.float64)
+    return np.asarray(x, dtype=np.float64)
+
+
+def causal_conv_bwd(x, w, du, conv_bias=None, silu=True, dtype="f32", x_prev=None):
+    """Gradients of the causal depthwise convolution ``causal_conv`` computes, for the loss
+    sum(du * u).  x [batch, dim, L] in storage dtype ("f32", "bf16", or "f64" for float64 values);
+    w [dim, K]; du [batch, dim, L] (float64); conv_bias [dim] or None; x_prev [batch, dim, K-1] (the
+    inputs before position 0, oldest first) or None (zeros).
+
+    The convolution in front of the SSM (visual guide, section 3.5) is
+        pre[t] = conv_bias + sum_{k<K} w[k] x[t-(K-1)+k],   u[t] = silu(pre[t]) (or pre[t]),
+    so by the chain rule, with s the logistic function and silu'(p) = s(p) (1 + p (1 - s(p))):
+        dpre[t] = du[t] silu'(pre[t])                   (du[t] without the activation)
+        dx[j]   = sum_k w[k] dpre[j + (K-1) - k]        (terms with the index inside [0, L))
+        dw[k]   = sum over batch and t of dpre[t] x[t-(K-1)+k]
+        dbias   = sum over batch and t of dpre[t]
+    and dx_prev the dx formula at the K-1 positions before 0.  Returns float64 arrays dx
+    [batch, dim, L], dw [dim, K], dconv_bias [dim], dx_prev [batch, dim, K-1]."""
+    xs = _as_f64(x, dtype)
+    bsz, dim, L = xs.shape
+    w = np.asarray(w, dtype=np.float64)
+    K = w.shape[1]
+    du = np.asarray(du, dtype=np.float64)
+    bias = np.zeros(dim) if conv_bias is None else np.asarray(conv_bias, dtype=np.float64)
+    prev = np.zeros((bsz, dim, K - 1)) if x_prev is None else np.asarray(x_prev, dtype=np.float64)
+    # xe[..., i] = x at position i - (K-1): the K-1 inputs before the sequence, then the sequence
+    xe = np.concatenate([prev, xs], axis=2)
+    pre = np.broadcast_to(bias[None, :, None], (bsz, dim, L)).copy()
+    for k in range(K):
+        pre += w[None, :, k, None] * xe[:, :, k:k + L]
+    if silu:
+        s = 1.0 / (1.0 + np.exp(-pre))
+        dpre = du * s * (1.0 + pre * (1.0 - s))
+    else:
+        dpre = du.copy()
+    dxe = np.zeros((bsz, dim, L + K - 1))
+    dw = np.zeros((dim, K))
+    for k in range(K):
+        dxe[:, :, k:k + L] += w[None, :, k, None] * dpre
+        dw[:, k] = np.sum(dpre * xe[:, :, k:k + L], axis=(0, 2))
+    return {"dx": dxe[:, :, K - 1:], "dw": dw, "dconv_bias": np.sum(dpre, axis=(0, 2)),
+            "dx_prev": dxe[:, :, :K - 1]}

@@ -208,7 +208,8 @@ static double softplus_grad(double x) { return 1.0 / (1.0 + exp(-x)); }
  * per channel, so dy_rows [nrows, seqlen] and dstate_rows [nrows, dstate] (NULL = 0) are the
  * gradients arriving at y and at last_state.
  *
- * Inputs as for oracle_scan_rows_ex.  Outputs, all fp64:
+ * Inputs as for oracle_scan_rows_ex (in_dtype ORACLE_F64 included: inputs already in double, such
+ * as this oracle's own convolution output).  Outputs, all fp64:
  *   per channel (overwritten): du_rows, ddelta_rows [nrows, seqlen]; dz_rows [nrows, seqlen]
  *     (only when z_rows is given; may be NULL); dh0_rows [nrows, dstate] (may be NULL);
  *   accumulated with += over the channels (the caller zeroes them): dA [dim, dstate],
@@ -228,7 +229,7 @@ int oracle_scan_bwd_rows(long long nrows, const int* row_b, const int* row_d, in
     if (nrows > 0 && (!row_b || !row_d || !u_rows || !delta_rows || !A || !B || !C || !dy_rows ||
                       !du_rows || !ddelta_rows || !dB || !dC))
         return -1;
-    if (in_dtype != ORACLE_F32 && in_dtype != ORACLE_BF16) return -1;
+    if (in_dtype != ORACLE_F32 && in_dtype != ORACLE_BF16 && in_dtype != ORACLE_F64) return -1;
     int failed = 0;
 #ifdef _OPENMP
     if (nthreads <= 0) nthreads = omp_get_max_threads();

@@ -17,6 +17,7 @@ from scipy.integrate import solve_ivp
 from scipy.special import expit
 
 import oracle
+import synth
 
 FD_RTOL = 1e-8
 
@@ -247,3 +248,26 @@ def test_bf16_storage_gradients_equal_widened_fp32():
     for k in a:
         if a[k] is not None:
             np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_bwd_f64_inputs_match_fp32():
+    """Gradient oracle with inputs given as doubles: on fp32-representable values it equals the fp32
+    run (single-threaded, so the sums over channels run in the same order), and an input perturbed
+    below fp32 resolution changes the result (the doubles are not rounded)."""
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=5, seqlen=30, seed=4)
+    inp = synth.scan_inputs(cfg)
+    g = synth.grad_inputs(cfg)
+    w = {k: inp[k].astype(np.float64) for k in ("u", "delta", "B", "C", "z")}
+    dy = g["dy"].astype(np.float64)
+    args = dict(h0=g["h0"], dlast_state=g["dlast"], nthreads=1)
+    r32 = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], dy, inp["D"], inp["z"],
+                          inp["delta_bias"], True, "f32", **args)
+    r64 = oracle.scan_bwd(w["u"], w["delta"], inp["A"], w["B"], w["C"], dy, inp["D"], w["z"],
+                          inp["delta_bias"], True, "f64", **args)
+    for k in ("du", "ddelta", "dz", "dA", "dB", "dC", "dD", "ddelta_bias", "dh0"):
+        assert np.array_equal(r32[k], r64[k]), k
+    u2 = w["u"].copy()
+    u2[0, 0, 0] += 1e-12
+    r2 = oracle.scan_bwd(u2, w["delta"], inp["A"], w["B"], w["C"], dy, inp["D"], w["z"], inp["delta_bias"], True,
+                         "f64", **args)
+    assert not np.array_equal(r2["dB"], r64["dB"])

@@ -116,13 +116,16 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-# the sources each profiled kernel (and the host code that plans its launches) is built from
+# the sources each profiled kernel and the host code that plans its launches are built from
 KERNEL_SOURCES = {
-    "scan_fwd": ("ptx.cuh", "common.cuh", "scan_fwd.cuh", "mamba_scan.cu"),
-    "scan_fwd_cl": ("ptx.cuh", "common.cuh", "scan_fwd.cuh", "scan_fwd_cl.cuh", "mamba_scan.cu"),
-    "state_step": ("ptx.cuh", "common.cuh", "state_step.cuh", "mamba_scan.cu"),
-    "scan_bwd": ("ptx.cuh", "common.cuh", "scan_bwd.cuh", "mamba_scan.cu"),
+    "scan_fwd": ("ptx.cuh", "common.cuh", "scan_fwd.cuh", "fwd_common.cuh", "fwd_warp.cuh", "fwd_warp_f32.cu",
+                 "fwd_warp_bf16.cu"),
+    "scan_fwd_cl": ("ptx.cuh", "common.cuh", "scan_fwd.cuh", "scan_fwd_cl.cuh", "scan_fix.cuh", "fwd_common.cuh",
+                    "fwd_lane.cuh", "fwd_lane_f32.cu", "fwd_lane_bf16.cu"),
+    "state_step": ("ptx.cuh", "common.cuh", "state_step.cuh", "step.cu"),
+    "scan_bwd": ("ptx.cuh", "common.cuh", "scan_bwd.cuh", "bwd.cu"),
 }
+KERNEL_SOURCES["scan_fix"] = KERNEL_SOURCES["scan_fwd_cl"]
 
 
 def source_hash(kernel: str = "scan_fwd") -> str:
@@ -854,11 +857,18 @@ def run_bwd(args, cfg, rank, world, local_rank):
         sets.append(st)
     out = None
     calls = []
-    for st in sets:
-        c, out = ms.prepare_scan_bwd(st["u"], st["delta"], params["A"], st["B"], st["C"], st["dy"],
-                                     params["D"], st["z"], params["delta_bias"], True, h0=st["h0"],
-                                     dlast_state=st["dlast"], out=out)
-        calls.append(c)
+    if args.conv:  # the block's backward pass: convolution recomputed, scan gradients, convolution gradients
+        cp = {k: to_torch(v, "f32", dev) for k, v in synth.conv_params(cfg, args.conv).items()}
+        for st in sets:
+            calls.append(lambda st=st: ms.mamba_scan_bwd_conv(
+                st["u"], cp["conv_w"], cp["conv_bias"], st["delta"], params["A"], st["B"], st["C"], st["dy"],
+                params["D"], st["z"], params["delta_bias"], True, h0=st["h0"], dlast_state=st["dlast"]))
+    else:
+        for st in sets:
+            c, out = ms.prepare_scan_bwd(st["u"], st["delta"], params["A"], st["B"], st["C"], st["dy"],
+                                         params["D"], st["z"], params["delta_bias"], True, h0=st["h0"],
+                                         dlast_state=st["dlast"], out=out)
+            calls.append(c)
     stream = torch.cuda.current_stream()
     W = max(args.warmup, 3)
     for i in range(W):
@@ -884,6 +894,8 @@ def run_bwd(args, cfg, rank, world, local_rank):
     elems_step = cfg.batch * cfg.dim * cfg.seqlen
     peaks, kind = measured_peaks()
     bb = bwd_bytes(cfg)
+    if args.conv:  # x read twice, u written and read back by the scan, du read: 4 more element passes
+        bb += 4 * cfg.batch * cfg.dim * cfg.seqlen * (2 if cfg.dtype == "bf16" else 4)
     achieved = bb / (avg_ms * 1e-3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     line = {
@@ -892,12 +904,18 @@ def run_bwd(args, cfg, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, recipe of the workload)",
         "config": {"workload": WORKLOADS[args.workload].replace("scan+decode", "backward pass"),
                    "batch": cfg.batch, "d_inner": cfg.dim, "d_state": cfg.dstate, "seq_len": cfg.seqlen,
-                   "storage": cfg.dtype, "step": "backward pass: gradients of u, delta, z, A, B, C, D, bias, h0",
+                   "storage": cfg.dtype,
+                   "step": (f"backward pass of the causal convolution (width {args.conv}) and the scan: gradients "
+                            "of x, conv weights and bias, delta, z, A, B, C, D, bias, h0" if args.conv else
+                            "backward pass: gradients of u, delta, z, A, B, C, D, bias, h0"),
                    "elements_per_step": elems_step, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2; two input sets alternate"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload, "scan_bwd"),
-                     "peak_source": f"{kind} hbm_gbs", "kernel": "scan_bwd_kernel", "algorithmic_bytes_per_launch": bb,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": None if args.conv else ncu_traffic(args.workload, "scan_bwd"),
+                     "peak_source": f"{kind} hbm_gbs",
+                     "kernel": "conv_fwd + scan_bwd + conv_bwd" if args.conv else "scan_bwd_kernel",
+                     "algorithmic_bytes_per_launch": bb,
                      "kernel_avg_us": round(avg_ms * 1e3, 2)},
         "clocks": clk.summary(),
         "gpu_launches": launches,

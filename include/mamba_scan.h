@@ -204,11 +204,13 @@ int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, const void*
  * this call recomputes them (visual guide section 3.4, "recomputation"): a forward sweep keeps
  * one state checkpoint per 8 positions (stream-ordered scratch, cudaMallocAsync on `stream`,
  * b * ceil(L/8) * d * 64 bytes, freed on the same stream), and a reverse sweep recomputes each
- * 8-position slot from its checkpoint and walks it backwards.
+ * 8-position slot from its checkpoint and walks it backwards.  States are handled in blocks of
+ * 16, one kernel launch each; for dstate > 16 the gradients of u, delta and z are summed over
+ * the blocks in fp32 scratch (another 2 or 3 * b * d * L * 4 bytes) and converted at the end.
  *
  *   discretization  MAMBA_DISC_SIMPLE or MAMBA_DISC_ZOH: the one the forward pass used.
  *   u .. h0         the forward inputs, as for mamba_scan_fwd_state (z, D, delta_bias, h0 may be
- *                   NULL with the same meaning).  dstate must be <= 16.
+ *                   NULL with the same meaning); any dstate up to MAMBA_MAX_DSTATE.
  *   dy              [b, d, L]  in_dtype: gradient of the loss with respect to y.
  *   dlast_state     [b, d, N]  fp32 or NULL (= 0): gradient with respect to last_state.
  * Outputs (written; none may overlap an input or another output):
@@ -229,6 +231,38 @@ int mamba_scan_bwd(const mamba_scan_shape* s, int discretization, const void* u,
                    const float* delta_bias, int softplus_flag, const float* h0, const void* dy,
                    const float* dlast_state, void* du, void* ddelta, void* dz, float* dA, float* dB,
                    float* dC, float* dD, float* ddelta_bias, float* dh0, void* stream);
+
+/*
+ * Gradients of the forward scan with the block's causal convolution in front of it
+ * (mamba_scan_fwd_conv) for the loss sum(dy * y) + sum(dlast_state * last_state): the backward pass
+ * of training the convolution and the selective SSM together (visual guide sections 3.4 and 3.5).
+ * Steps, all on `stream`: u = act(conv(x)) is recomputed into stream-ordered scratch
+ * (cudaMallocAsync, 2 * b * d * L * sizeof(in_dtype) bytes with du, freed on the same stream);
+ * the scan's backward pass (as mamba_scan_bwd) gives du; a convolution kernel takes du back
+ * through the activation and the taps.
+ *
+ *   discretization, x, conv_w, conv_bias, conv_k, conv_silu, conv_prev, delta .. h0:
+ *                   the forward inputs, as for mamba_scan_fwd_conv.
+ *   dy, dlast_state as for mamba_scan_bwd.
+ * Outputs (written; dx must not overlap an input or another output):
+ *   dx              [b, d, L]  in_dtype: gradient with respect to the convolution's input x.
+ *   ddelta, dz, dA, dB, dC, dD, ddelta_bias, dh0: as for mamba_scan_bwd.
+ *   dconv_w         [d, conv_k] fp32 or NULL, summed over batch and positions.
+ *   dconv_bias      [d] fp32 or NULL, summed over batch and positions (also when conv_bias is NULL).
+ *   dconv_prev      [b, d, conv_k - 1] fp32 or NULL: gradient with respect to the inputs before
+ *                   position 0 (conv_prev, or the zeros that stand for it when it is NULL); zeros
+ *                   when L == 0.
+ * With bf16 storage, u and du pass through bf16 scratch (the forward kept u in fp32 registers).
+ * The per-channel sums use atomics, so their rounding (not their value) can differ between runs.
+ * Errors: MAMBA_ERR_ARG, MAMBA_ERR_CUDA.
+ */
+int mamba_scan_bwd_conv(const mamba_scan_shape* s, int discretization, const void* x, const float* conv_w,
+                        const float* conv_bias, int conv_k, int conv_silu, const float* conv_prev,
+                        const void* delta, const float* A, const void* B, const void* C, const float* D,
+                        const void* z, const float* delta_bias, int softplus_flag, const float* h0,
+                        const void* dy, const float* dlast_state, void* dx, void* ddelta, void* dz, float* dA,
+                        float* dB, float* dC, float* dD, float* ddelta_bias, float* dconv_w, float* dconv_bias,
+                        float* dconv_prev, float* dh0, void* stream);
 
 /* Message describing the calling thread's most recent failure ("" if none). */
 const char* mamba_scan_last_error(void);

@@ -65,6 +65,8 @@ def _load() -> ctypes.CDLL:
     lib.mamba_state_step.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, I, P, P]
     lib.mamba_scan_bwd.restype = I
     lib.mamba_scan_bwd.argtypes = [ctypes.POINTER(Shape), I] + [P] * 8 + [I] + [P] * 13
+    lib.mamba_scan_bwd_conv.restype = I
+    lib.mamba_scan_bwd_conv.argtypes = [ctypes.POINTER(Shape), I, P, P, P, I, I, P] + [P] * 7 + [I] + [P] * 16
     lib.mamba_scan_last_error.restype = ctypes.c_char_p
     lib.mamba_scan_last_error.argtypes = []
     lib.mamba_scan_version.restype = I
@@ -80,7 +82,8 @@ _lib = _load()
 
 # symbols the header declares; the tests check that every one of them is exported
 EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_state", "mamba_scan_fwd_ex",
-            "mamba_scan_fwd_conv", "mamba_state_step", "mamba_state_step_ex", "mamba_scan_bwd", "mamba_scan_last_error", "mamba_scan_version", "mamba_scan_device_status",
+            "mamba_scan_fwd_conv", "mamba_state_step", "mamba_state_step_ex", "mamba_scan_bwd", "mamba_scan_bwd_conv",
+            "mamba_scan_last_error", "mamba_scan_version", "mamba_scan_device_status",
             "mamba_scan_launch_count")
 MAMBA_DISC_SIMPLE, MAMBA_DISC_ZOH = 0, 1
 _DISC = {"simple": MAMBA_DISC_SIMPLE, "zoh": MAMBA_DISC_ZOH}
@@ -354,6 +357,48 @@ def prepare_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, sof
     return PreparedCall(_lib.mamba_scan_bwd, args, keep), out
 
 
+def mamba_scan_bwd_conv(x, conv_w, conv_bias, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True,
+                        conv_silu=True, conv_prev=None, h0=None, dlast_state=None, disc="simple", stream=None):
+    """Gradients of mamba_scan_fwd_conv (the scan with the block's causal convolution in front) for
+    the loss sum(dy * y) + sum(dlast_state * last_state).  Inputs as for mamba_scan_fwd_conv plus dy
+    and dlast_state as for mamba_scan_bwd.  Returns the dict of mamba_scan_bwd with du replaced by
+    dx (input dtype) and three more float32 entries: dconv_w [d, K], dconv_bias [d] and dconv_prev
+    [b, d, K-1] (None when K == 1)."""
+    bsz, dim, L = x.shape
+    N = A.shape[1]
+    K = conv_w.shape[1]
+    dt = x.dtype
+    f32 = dict(device=x.device, dtype=torch.float32)
+    out = {"dx": torch.empty_like(x), "ddelta": torch.empty_like(x),
+           "dz": torch.empty_like(x) if z is not None else None,
+           "dA": torch.empty((dim, N), **f32), "dB": torch.empty((bsz, N, L), **f32),
+           "dC": torch.empty((bsz, N, L), **f32),
+           "dD": torch.empty((dim,), **f32) if D is not None else None,
+           "ddelta_bias": torch.empty((dim,), **f32) if delta_bias is not None else None,
+           "dconv_w": torch.empty((dim, K), **f32), "dconv_bias": torch.empty((dim,), **f32),
+           "dconv_prev": torch.empty((bsz, dim, K - 1), **f32) if K > 1 else None,
+           "dh0": torch.empty((bsz, dim, N), **f32) if h0 is not None else None}
+    shape = Shape(bsz, dim, N, L, _dtype_code(x))
+    _check(_lib.mamba_scan_bwd_conv(
+        ctypes.byref(shape), _DISC[disc], _ptr(x, (bsz, dim, L), dt, "x"),
+        _ptr(conv_w, (dim, K), torch.float32, "conv_w"), _ptr(conv_bias, (dim,), torch.float32, "conv_bias"),
+        int(K), int(bool(conv_silu)), _ptr(conv_prev, (bsz, dim, K - 1), torch.float32, "conv_prev"),
+        _ptr(delta, (bsz, dim, L), dt, "delta"), _ptr(A, (dim, N), torch.float32, "A"),
+        _ptr(B, (bsz, N, L), dt, "B"), _ptr(C, (bsz, N, L), dt, "C"), _ptr(D, (dim,), torch.float32, "D"),
+        _ptr(z, (bsz, dim, L), dt, "z"), _ptr(delta_bias, (dim,), torch.float32, "delta_bias"),
+        int(bool(softplus)), _ptr(h0, (bsz, dim, N), torch.float32, "h0"), _ptr(dy, (bsz, dim, L), dt, "dy"),
+        _ptr(dlast_state, (bsz, dim, N), torch.float32, "dlast_state"),
+        _ptr(out["dx"], (bsz, dim, L), dt, "dx"), _ptr(out["ddelta"], (bsz, dim, L), dt, "ddelta"),
+        _ptr(out["dz"], (bsz, dim, L), dt, "dz"), _ptr(out["dA"], (dim, N), torch.float32, "dA"),
+        _ptr(out["dB"], (bsz, N, L), torch.float32, "dB"), _ptr(out["dC"], (bsz, N, L), torch.float32, "dC"),
+        _ptr(out["dD"], (dim,), torch.float32, "dD"), _ptr(out["ddelta_bias"], (dim,), torch.float32, "ddelta_bias"),
+        _ptr(out["dconv_w"], (dim, K), torch.float32, "dconv_w"),
+        _ptr(out["dconv_bias"], (dim,), torch.float32, "dconv_bias"),
+        _ptr(out["dconv_prev"], (bsz, dim, K - 1), torch.float32, "dconv_prev"),
+        _ptr(out["dh0"], (bsz, dim, N), torch.float32, "dh0"), _stream(stream, x.device)))
+    return out
+
+
 class _HostPipeline:
     """Device staging buffers and streams of mamba_scan_fwd_pipelined for one shape (kept between
     calls, so that steady use allocates nothing)."""
@@ -458,14 +503,45 @@ class _SelectiveScan(torch.autograd.Function):
 
 def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, disc="simple"):
     """(y, last_state) of the scan, differentiable with respect to u, delta, A, B, C, D, z,
-    delta_bias and h0 (backward pass: mamba_scan_bwd, d_state <= 16).  Arguments as for
-    mamba_scan_fwd.  A d_state above 16 is refused here, before the forward pass, when a gradient
-    would be needed."""
-    ins = (u, delta, A, B, C, D, z, delta_bias, h0)
-    if torch.is_grad_enabled() and any(t is not None and t.requires_grad for t in ins) and A.shape[1] > 16:
-        raise ValueError(f"selective_scan: the backward pass supports d_state <= 16, got {A.shape[1]}; "
-                         "call mamba_scan_fwd for a forward pass without gradients")
+    delta_bias and h0 (backward pass: mamba_scan_bwd).  Arguments as for mamba_scan_fwd."""
     return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, h0, bool(softplus), disc)
+
+
+class _SelectiveScanConv(torch.autograd.Function):
+    """The scan with the block's causal convolution in front, as an autograd operation: forward
+    mamba_scan_fwd_conv, backward mamba_scan_bwd_conv (the convolution's output and the states are
+    recomputed; only the inputs are saved)."""
+
+    @staticmethod
+    def forward(ctx, x, conv_w, conv_bias, conv_prev, delta, A, B, C, D, z, delta_bias, h0, softplus, conv_silu,
+                disc):
+        y, last_state = mamba_scan_fwd_conv(x, conv_w, conv_bias, delta, A, B, C, D, z, delta_bias, softplus,
+                                            conv_silu=conv_silu, conv_prev=conv_prev, h0=h0, disc=disc)
+        ctx.save_for_backward(x, conv_w, conv_bias, conv_prev, delta, A, B, C, D, z, delta_bias, h0)
+        ctx.softplus, ctx.conv_silu, ctx.disc = softplus, conv_silu, disc
+        return y, last_state
+
+    @staticmethod
+    def backward(ctx, dy, dlast_state):
+        x, conv_w, conv_bias, conv_prev, delta, A, B, C, D, z, delta_bias, h0 = ctx.saved_tensors
+        dy = torch.zeros_like(x) if dy is None else dy.contiguous()
+        dlast_state = None if dlast_state is None else dlast_state.contiguous()
+        g = mamba_scan_bwd_conv(x, conv_w, conv_bias, delta, A, B, C, dy, D, z, delta_bias, ctx.softplus,
+                                conv_silu=ctx.conv_silu, conv_prev=conv_prev, h0=h0, dlast_state=dlast_state,
+                                disc=ctx.disc)
+        like = lambda t, ref: None if t is None or ref is None else t.to(ref.dtype)  # dB, dC come as fp32
+        return (g["dx"], g["dconv_w"], like(g["dconv_bias"], conv_bias), like(g["dconv_prev"], conv_prev),
+                g["ddelta"], g["dA"], like(g["dB"], B), like(g["dC"], C), g["dD"], g["dz"], g["ddelta_bias"],
+                g["dh0"], None, None, None)
+
+
+def selective_scan_conv(x, conv_w, conv_bias, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+                        conv_silu=True, conv_prev=None, h0=None, disc="simple"):
+    """(y, last_state) of the scan with the block's causal convolution in front, differentiable
+    with respect to x, conv_w, conv_bias, conv_prev, delta, A, B, C, D, z, delta_bias and h0
+    (backward pass: mamba_scan_bwd_conv).  Arguments as for mamba_scan_fwd_conv."""
+    return _SelectiveScanConv.apply(x, conv_w, conv_bias, conv_prev, delta, A, B, C, D, z, delta_bias, h0,
+                                    bool(softplus), bool(conv_silu), disc)
 
 
 def device_status(stream=None) -> None:

@@ -4,18 +4,24 @@ from __future__ import annotations
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmambascan.so")
-SOURCES = ["mamba_scan.cu"]
-HEADERS = ["ptx.cuh", "common.cuh", "scan_fwd.cuh", "scan_fwd_cl.cuh", "scan_fix.cuh", "scan_bwd.cuh", "state_step.cuh"]
+# One translation unit per kernel family (each becomes its own device module), compiled in
+# parallel and linked into one shared library.
+SOURCES = ["mamba_scan.cu", "fwd_lane_f32.cu", "fwd_lane_bf16.cu", "fwd_warp_f32.cu", "fwd_warp_bf16.cu", "bwd.cu",
+           "conv.cu", "step.cu"]
+HEADERS = ["host.cuh", "fwd_common.cuh", "fwd_lane.cuh", "fwd_warp.cuh", "ptx.cuh", "common.cuh", "scan_fwd.cuh", "scan_fwd_cl.cuh", "scan_fix.cuh",
+           "scan_bwd.cuh", "state_step.cuh", "conv.cuh"]
+OBJDIR = os.path.join(HERE, "_build")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
     "--expt-relaxed-constexpr",
 ]
 
@@ -40,13 +46,27 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     statically (nvcc's default), so the library only needs the driver at run time."""
     if not force and not stale():
         return LIB
+    os.makedirs(OBJDIR, exist_ok=True)
+    inc = ["-I", os.path.join(ROOT, "include"), "-I", CSRC]
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + f".{os.getpid()}.o")
+        cmd = [_nvcc(), *NVCC_FLAGS, *extra, *inc, "-c", os.path.join(CSRC, src), "-o", obj]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        subprocess.check_call(cmd)
+        return obj
+
+    with ThreadPoolExecutor(max_workers=len(SOURCES)) as pool:
+        objs = list(pool.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [_nvcc(), *NVCC_FLAGS, *extra, "-I", os.path.join(ROOT, "include"), "-I", CSRC,
-           *[os.path.join(CSRC, f) for f in SOURCES], "-o", tmp]
+    cmd = [_nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.check_call(cmd)
     os.replace(tmp, LIB)
+    for o in objs:
+        os.remove(o)
     return LIB
 
 

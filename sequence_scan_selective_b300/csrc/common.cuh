@@ -14,7 +14,9 @@ namespace mscan {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s bound on any wait inside a kernel
 
-__device__ int g_status;  // nonzero: some kernel abandoned a bounded wait
+// Nonzero: some kernel abandoned a bounded wait.  One copy per translation unit (each compiles to
+// its own module); the host reads every unit's copy.
+static __device__ int g_status;
 
 // ------------------------------------------------------------------------------ element access
 // Inputs are fp32 or bf16 (held as uint16_t bit patterns); arithmetic is always fp32.

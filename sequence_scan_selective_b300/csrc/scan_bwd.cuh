@@ -19,7 +19,10 @@
 // then ddelta = dDelta * sigmoid(delta + bias) (softplus) and dz = dy ypre silu'(z).
 //
 // Work layout: a CTA of 4 warps owns 32 channels of one batch row for the whole sequence; a warp
-// owns 8 channels, lane (c = lane % 8, g = lane / 8) holds states 4g..4g+3 of channel c (N <= 16).
+// owns 8 channels, lane (c = lane % 8, g = lane / 8) holds states nb+4g .. nb+4g+3 of channel c,
+// where nb is the first state of the launch's block of 16 (N > 16 runs one launch per block, in
+// order: the states are independent of one another, and the per-(channel, step) gradients, which
+// sum over all states, are accumulated in fp32 across the launches).
 // Tiles of 16 steps of u, delta, z, dy (per channel) and B, C (per batch row) are staged in shared
 // memory by cp.async, double-buffered.  The sums over channels (dB, dC) are reduced across the 8
 // channel lanes of a warp by a shuffle reduce-scatter, across the 4 warps in shared memory, and
@@ -59,6 +62,14 @@ struct BwdArgs {
     long long L;
     int ntile, nslot;
     int softplus;
+    // State block: this launch handles states nb .. nb + 15 (N > 16 takes ceil(N / 16) launches,
+    // in order).  Then the per-(channel, step) gradients, whose sums over states span all blocks,
+    // are added into fp32 accumulators acc_du, acc_dd, acc_dz [b, d, L] (the first block writes
+    // them); a final pass converts them.  With acc_du == null (N <= 16) they are stored directly.
+    int nb;
+    float* acc_du;
+    float* acc_dd;
+    float* acc_dz;
 };
 
 namespace bwd {
@@ -135,7 +146,7 @@ __device__ __forceinline__ float reduce_scatter3(float v0, float v1, float v2, i
 
 
 // Stage tile k (steps 32k .. 32k+31) of the CTA's channel rows (u, delta; z and dy when `full`) and
-// of B (and C when `full`) rows n < N.  Positions past L or past the last channel read as zero.
+// of B (and C when `full`) rows nb .. min(nb + 16, N) - 1 (the state block).  Positions past L or past the last channel read as zero.
 // VEC: 16-byte cp.async pieces (rows 16-byte aligned, L * sizeof(TIn) a multiple of 16), left in
 // flight; otherwise plain element loads, complete on return.
 template <typename TIn, bool VEC>
@@ -162,14 +173,15 @@ __device__ __forceinline__ void load_tile(uint8_t* st, const BwdArgs& a, int b, 
                            (ok ? ((long long)b * a.dim + d) * a.L + e0 : 0);
             cp_async16(st + choff(tens) + row * Lt::ROW + piece * 16, p, ok ? 16u : 0u);
         }
-        const int perb = a.dstate * Lt::CHUNKS;
+        const int nrow = min(kNS, a.dstate - a.nb);  // this block's states
+        const int perb = nrow * Lt::CHUNKS;
         for (int i = tid; i < nbc_t * perb; i += kThreads) {
             const int tens = i / perb, rem = i - tens * perb;
             const int n = rem / Lt::CHUNKS, piece = rem - n * Lt::CHUNKS;
             const long long e0 = t0 + piece * EPC;
             const bool ok = e0 < a.L;
             const TIn* p = static_cast<const TIn*>(tens ? a.C : a.B) +
-                           (ok ? ((long long)b * a.dstate + n) * a.L + e0 : 0);
+                           (ok ? ((long long)b * a.dstate + a.nb + n) * a.L + e0 : 0);
             cp_async16(st + (tens ? Lt::OFF_C : Lt::OFF_B) + n * Lt::ROW + piece * 16, p, ok ? 16u : 0u);
         }
         cp_async_commit();
@@ -185,13 +197,14 @@ __device__ __forceinline__ void load_tile(uint8_t* st, const BwdArgs& a, int b, 
             if (d < a.dim && e < a.L) v = static_cast<const TIn*>(chsrc(tens))[((long long)b * a.dim + d) * a.L + e];
             reinterpret_cast<TIn*>(st + choff(tens) + row * Lt::ROW)[t] = v;
         }
-        const int perb = a.dstate * kT;
+        const int nrow = min(kNS, a.dstate - a.nb);
+        const int perb = nrow * kT;
         for (int i = tid; i < nbc_t * perb; i += kThreads) {
             const int tens = i / perb, rem = i - tens * perb;
             const int n = rem / kT, t = rem - n * kT;
             const long long e = t0 + t;
             TIn v{};
-            if (e < a.L) v = static_cast<const TIn*>(tens ? a.C : a.B)[((long long)b * a.dstate + n) * a.L + e];
+            if (e < a.L) v = static_cast<const TIn*>(tens ? a.C : a.B)[((long long)b * a.dstate + a.nb + n) * a.L + e];
             reinterpret_cast<TIn*>(st + (tens ? Lt::OFF_C : Lt::OFF_B) + n * Lt::ROW)[t] = v;
         }
     }
@@ -265,7 +278,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     float* R = reinterpret_cast<float*>(smem + Lt::OFF_R) + warp * 3 * 8 * kPad;     // [k][c][t]
     float* part = reinterpret_cast<float*>(smem + Lt::OFF_PART) + warp * kT * kPartPitch;  // [t][col]
 
-    // B/C rows of states n >= N stay zero in both stages: their states never move
+    // B/C rows of states past N stay zero in both stages: their states never move
     for (int i = tid; i < 2 * 2 * kNS * Lt::ROW / 16; i += kThreads) {
         const int stg = i / (2 * kNS * Lt::ROW / 16), rem = i - stg * (2 * kNS * Lt::ROW / 16);
         reinterpret_cast<uint4*>(smem + stg * Lt::STAGE + Lt::OFF_B)[rem] = make_uint4(0, 0, 0, 0);
@@ -278,7 +291,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     auto el = [](float2* v, int j) -> float& { return (j & 1) ? v[j >> 1].y : v[j >> 1].x; };
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int n = 4 * g + j;
+        const int n = a.nb + 4 * g + j;  // state (this block's 4g + j)
         el(Aj, j) = (dvalid && n < N) ? a.A[(long long)d * N + n] : 0.f;
         el(A2, j) = el(Aj, j) * kLog2e;
         el(invA, j) = 1.f / el(Aj, j);  // hold only; infinite at A = 0, where the series branch is taken
@@ -289,13 +302,13 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
         return fabsf(X) < kZohSeriesLimit ? dt * zoh_phi(X) : (abar - 1.f) * el(invA, j);
     };
     const float bias_c = (dvalid && a.bias) ? a.bias[d] : 0.f;
-    const float D_c = (dvalid && a.D) ? a.D[d] : 0.f;
+    const float D_once = (dvalid && a.D && a.nb == 0) ? a.D[d] : 0.f;  // the skip term, first state block only
     const long long chrow = ((long long)b * a.dim + d) * a.L;  // start of the channel's rows
 
     float h0v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int n = 4 * g + j;
+        const int n = a.nb + 4 * g + j;  // state (this block's 4g + j)
         h0v[j] = (a.h0 && dvalid && n < N) ? a.h0[((long long)b * a.dim + d) * N + n] : 0.f;
     }
     float* ck = a.ckpt ? a.ckpt + (((long long)b * a.nslot) * a.dim + d) * kNS + 4 * g : nullptr;
@@ -402,7 +415,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     float2 mu[2], dAacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int n = 4 * g + j;
+        const int n = a.nb + 4 * g + j;  // state (this block's 4g + j)
         el(mu, j) = (a.dlast && dvalid && n < N) ? a.dlast[((long long)b * a.dim + d) * N + n] : 0.f;
     }
     float dD_acc = 0.f, dbias_acc = 0.f;
@@ -533,10 +546,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
                 const float sarg = dl[j] + bias_c;
                 const float gdt = a.softplus ? sdt * sigmoid_approx(sarg) : sdt;
                 o_dd[j] = gdt;
-                o_du[j] = fmaf(sub, ZOH ? 1.f : qq.x, qq.z * D_c);  // the hold's k already holds Delta
+                // the skip term D x belongs to no state: only the first state block adds it
+                o_du[j] = fmaf(sub, ZOH ? 1.f : qq.x, qq.z * D_once);  // the hold's k already holds Delta
                 if (gate) {
                     const float sg = sigmoid_approx(zz[j]);
-                    const float ypre = fmaf(D_c, qq.w, sch);
+                    const float ypre = fmaf(D_once, qq.w, sch);
                     o_dz[j] = dyv[j] * ypre * sg * fmaf(zz[j], 1.f - sg, 1.f);
                 }
                 if (ok) {
@@ -546,9 +560,20 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
             }
             if (dvalid) {
                 const long long tg0 = t0 + kSPL * g, off = chrow + tg0;
-                store_steps<TIn, VEC>(static_cast<TIn*>(a.du) + off, tg0, a.L, o_du);
-                store_steps<TIn, VEC>(static_cast<TIn*>(a.ddelta) + off, tg0, a.L, o_dd);
-                if (gate && a.dz) store_steps<TIn, VEC>(static_cast<TIn*>(a.dz) + off, tg0, a.L, o_dz);
+                if (a.acc_du != nullptr) {  // state blocks: add into the fp32 accumulators
+                    const bool first = a.nb == 0;
+#pragma unroll
+                    for (int j = 0; j < kSPL; ++j) {
+                        if (tg0 + j >= a.L) break;
+                        a.acc_du[off + j] = (first ? 0.f : a.acc_du[off + j]) + o_du[j];
+                        a.acc_dd[off + j] = (first ? 0.f : a.acc_dd[off + j]) + o_dd[j];
+                        if (gate && a.acc_dz) a.acc_dz[off + j] = (first ? 0.f : a.acc_dz[off + j]) + o_dz[j];
+                    }
+                } else {
+                    store_steps<TIn, VEC>(static_cast<TIn*>(a.du) + off, tg0, a.L, o_du);
+                    store_steps<TIn, VEC>(static_cast<TIn*>(a.ddelta) + off, tg0, a.L, o_dd);
+                    if (gate && a.dz) store_steps<TIn, VEC>(static_cast<TIn*>(a.dz) + off, tg0, a.L, o_dz);
+                }
             }
         }
         __syncthreads();
@@ -560,7 +585,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
             for (int rep = 0; rep < kT * 8 / kThreads; ++rep) {
                 const int gi = tid + rep * kThreads;  // 32 columns x kT/4 groups of 4 steps
                 const int colr = gi / (kT / 4), tq = gi % (kT / 4);
-                const int kind = colr >> 4, n = colr & 15;
+                const int kind = colr >> 4, n = a.nb + (colr & 15);
                 if (n < N) {
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -585,7 +610,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     // ---------------------------------------------------------------- per-channel results
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int n = 4 * g + j;
+        const int n = a.nb + 4 * g + j;  // state (this block's 4g + j)
         if (dvalid && n < N) {
             atomicAdd(a.dA + (long long)d * N + n, el(dAacc, j));
             if (a.dh0) a.dh0[((long long)b * a.dim + d) * N + n] = el(mu, j);
@@ -596,8 +621,19 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, 8);
     dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, 16);
     if (dvalid && g == 0) {
-        if (a.dD) atomicAdd(a.dD + d, dD_acc);
+        if (a.dD && a.nb == 0) atomicAdd(a.dD + d, dD_acc);
         if (a.dbias) atomicAdd(a.dbias + d, dbias_acc);
+    }
+}
+
+// fp32 accumulators of the state-block launches -> the per-(channel, step) gradients in the
+// storage type.
+template <typename TIn>
+__global__ void __launch_bounds__(256) bwd_finish_kernel(const BwdArgs a, long long n) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        store_out<TIn>(static_cast<TIn*>(a.du) + i, a.acc_du[i]);
+        store_out<TIn>(static_cast<TIn*>(a.ddelta) + i, a.acc_dd[i]);
+        if (a.acc_dz != nullptr) store_out<TIn>(static_cast<TIn*>(a.dz) + i, a.acc_dz[i]);
     }
 }
 

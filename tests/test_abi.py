@@ -125,7 +125,7 @@ def test_bwd_host_argument_checks(ms):
     d = P(256)  # never dereferenced: every case below fails validation first
     args = lambda s, disc=0, z=None, dz=None, A=d: (ctypes.byref(s), disc, d, d, A, d, d, None, z, None, 1, None, d,
                                                    None, d, d, dz, d, d, d, None, None, None, None)
-    assert lib.mamba_scan_bwd(*args(_shape(ms, dstate=17))) == -1
+    assert lib.mamba_scan_bwd(*args(_shape(ms, dstate=65))) == -1
     assert b"dstate" in lib.mamba_scan_last_error()
     assert lib.mamba_scan_bwd(*args(_shape(ms), disc=7)) == -1
     assert lib.mamba_scan_bwd(*args(_shape(ms), dz=d)) == -1
@@ -168,3 +168,20 @@ def test_bench_byte_counts():
     # A, D, bias read and their gradients written; h0, dlast read, dh0 written
     assert bench.bwd_bytes(cfg) == (7 * 4 * b * d * L + 4 * 4 * b * n * L + 2 * 4 * d * (n + 2)
                                     + 3 * 4 * b * d * n)
+
+
+def test_block_bwd_host_argument_checks(ms):
+    """mamba_scan_bwd_conv refuses a missing kernel, a width outside 1..4 and a bad shape before
+    touching the device."""
+    lib = ms.lib()
+    P = ctypes.c_void_p
+    d = P(256)  # never dereferenced: every case below fails validation first
+    args = lambda s, w=d, k=4: (ctypes.byref(s), 0, d, w, None, k, 1, None, d, d, d, d, None, None, None, 1, None,
+                                d, None, d, d, None, d, d, d, None, None, d, None, None, None, None)
+    assert lib.mamba_scan_bwd_conv(*args(_shape(ms), w=None)) == -1
+    assert b"conv_w" in lib.mamba_scan_last_error()
+    assert lib.mamba_scan_bwd_conv(*args(_shape(ms), k=5)) == -1
+    assert b"conv_k" in lib.mamba_scan_last_error()
+    assert lib.mamba_scan_bwd_conv(*args(_shape(ms), k=0)) == -1
+    assert lib.mamba_scan_bwd_conv(*args(_shape(ms, dstate=65))) == -1
+    assert lib.mamba_scan_bwd_conv(*args(_shape(ms, seqlen=-1))) == -1

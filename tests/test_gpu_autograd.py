@@ -57,14 +57,62 @@ def test_selective_scan_gradients_match_oracle(ms, dtype, with_h0):
         assert e <= TOL[dtype], f"{k}: rel err {e:.3e}"
 
 
-def test_selective_scan_refuses_wide_state_before_forward(ms):
-    x = torch.zeros((1, 4, 16), device="cuda", requires_grad=True)
-    A = -torch.ones((4, 32), device="cuda")
-    Bm = torch.zeros((1, 32, 16), device="cuda")
-    n0 = ms.launch_count()
-    with pytest.raises(ValueError, match="d_state <= 16"):
-        ms.selective_scan(x, torch.zeros_like(x), A, Bm, Bm.clone())
-    assert ms.launch_count() == n0
-    with torch.no_grad():  # no gradient wanted: the forward pass runs
-        y, _ = ms.selective_scan(x, torch.zeros_like(x), A, Bm, Bm.clone())
-    assert y.shape == x.shape
+@pytest.mark.parametrize("N", [32, 64])
+def test_selective_scan_wide_state(ms, N):
+    """d_state above 16 trains too: the backward pass takes the states in blocks of 16."""
+    cfg = synth.CONFIGS["m130"].replace(batch=1, dim=24, dstate=N, seqlen=120, seed=72 + N)
+    inp = synth.scan_inputs(cfg)
+    g = synth.grad_inputs(cfg)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+    t = {k: f32(inp[k]) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias")}
+    for v in t.values():
+        v.requires_grad_(True)
+    y, last = ms.selective_scan(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], True)
+    ((y * f32(g["dy"])).sum() + (last * f32(g["dlast"])).sum()).backward()
+    torch.cuda.synchronize()
+    ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], g["dy"].astype(np.float64),
+                          inp["D"], inp["z"], inp["delta_bias"], True, "f32", dlast_state=g["dlast"])
+    pairs = {"u": "du", "delta": "ddelta", "z": "dz", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "delta_bias": "ddelta_bias"}
+    for k, gk in pairs.items():
+        e = rel_err(from_dev(t[k].grad), ref[gk])
+        assert e <= TOL["f32"], f"{k}: rel err {e:.3e}"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_selective_scan_conv_gradients_match_oracle(ms, dtype):
+    """The fused block (causal convolution + scan) as an autograd operation, against the oracle
+    chain: oracle convolution (fp64 u), oracle scan gradients on that u, oracle convolution
+    gradient."""
+    K = 4
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=36, dstate=16, seqlen=300, dtype=dtype, seed=71)
+    inp = synth.scan_inputs(cfg)
+    g = synth.grad_inputs(cfg)
+    cp = synth.conv_params(cfg, K)
+    prev = synth.conv_prev(cfg, K)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+    t = {k: to_dev(inp[k], dtype) for k in ("u", "delta", "z", "B", "C")}
+    t.update({k: f32(inp[k]) for k in ("A", "D", "delta_bias")})
+    t.update(conv_w=f32(cp["conv_w"]), conv_bias=f32(cp["conv_bias"]), conv_prev=f32(prev), h0=f32(g["h0"]))
+    for v in t.values():
+        v.requires_grad_(True)
+    y, last = ms.selective_scan_conv(t["u"], t["conv_w"], t["conv_bias"], t["delta"], t["A"], t["B"], t["C"], t["D"],
+                                     t["z"], t["delta_bias"], True, conv_prev=t["conv_prev"], h0=t["h0"])
+    dy = to_dev(g["dy"], dtype)
+    ((y.float() * dy.float()).sum() + (last * f32(g["dlast"])).sum()).backward()
+    torch.cuda.synchronize()
+    ms.device_status()
+    w = lambda a: synth.widen(a, dtype)
+    u = oracle.causal_conv(inp["u"], cp["conv_w"], cp["conv_bias"], True, dtype, x_prev=prev)
+    ref = oracle.scan_bwd(u, w(inp["delta"]), inp["A"], w(inp["B"]), w(inp["C"]), w(g["dy"]), inp["D"], w(inp["z"]),
+                          inp["delta_bias"], True, "f64", h0=g["h0"], dlast_state=g["dlast"])
+    cg = oracle.causal_conv_bwd(inp["u"], cp["conv_w"], ref["du"], cp["conv_bias"], True, dtype, x_prev=prev)
+    ref.update(dx=cg["dx"], dconv_w=cg["dw"], dconv_bias=cg["dconv_bias"], dconv_prev=cg["dx_prev"])
+    pairs = {"u": "dx", "delta": "ddelta", "z": "dz", "A": "dA", "B": "dB", "C": "dC", "D": "dD",
+             "delta_bias": "ddelta_bias", "h0": "dh0", "conv_w": "dconv_w", "conv_bias": "dconv_bias",
+             "conv_prev": "dconv_prev"}
+    for k, gk in pairs.items():
+        assert t[k].grad is not None, k
+        assert t[k].grad.dtype == t[k].dtype and t[k].grad.shape == t[k].shape, k
+        e = rel_err(from_dev(t[k].grad), ref[gk])
+        assert e <= TOL[dtype], f"{k}: rel err {e:.3e}"

@@ -163,14 +163,33 @@ def test_bwd_empty_sequence(ms):
     assert torch.count_nonzero(out["dA"]) == 0 and torch.count_nonzero(out["dD"]) == 0
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [17, 24, 32, 48, 64])
+def test_bwd_wide_state(ms, dtype, N):
+    """N > 16 runs one launch per block of 16 states; the per-(channel, step) gradients, which sum
+    over all states, are accumulated across the launches in fp32."""
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=33, dstate=N, seqlen=150, dtype=dtype, seed=180 + N)
+    _check(ms, cfg)
+
+
+@pytest.mark.parametrize("disc", ["simple", "zoh"])
+def test_bwd_wide_state_optional_inputs(ms, disc):
+    cfg = synth.CONFIGS["m130"].replace(batch=1, dim=40, dstate=40, seqlen=77, seed=190)
+    inp = _inputs(cfg, drop=("z", "D"))
+    d = dev_inputs(inp, cfg.dtype)
+    f32 = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+    got = ms.mamba_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], to_dev(inp["dy"], cfg.dtype), None, None,
+                            d.get("delta_bias"), True, h0=f32(inp["h0"]), dlast_state=f32(inp["dlast"]), disc=disc)
+    torch.cuda.synchronize()
+    got = {k: (None if v is None else from_dev(v)) for k, v in got.items()}
+    ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], synth.widen(inp["dy"], cfg.dtype),
+                          None, None, inp.get("delta_bias"), True, cfg.dtype, h0=inp["h0"],
+                          dlast_state=inp["dlast"], disc=disc)
+    _compare(got, ref, cfg.dtype)
+
+
 def test_bwd_rejects_unsupported(ms):
-    cfg = synth.CONFIGS["m130"].replace(batch=1, dim=8, dstate=17, seqlen=16, seed=170)
-    inp = _inputs(cfg)
-    d = dev_inputs(inp, "f32")
-    dy = to_dev(inp["dy"], "f32")
-    with pytest.raises(ms.MambaScanError):
-        ms.mamba_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], dy, d["D"], d["z"], d["delta_bias"])
-    cfg = cfg.replace(dstate=16)
+    cfg = synth.CONFIGS["m130"].replace(batch=1, dim=8, dstate=16, seqlen=16, seed=170)
     inp = _inputs(cfg)
     d = dev_inputs(inp, "f32")
     with pytest.raises(ms.MambaScanError):  # a gradient output that aliases an input

@@ -14,8 +14,10 @@
 //      dx[j]   = sum_k w[k] dpre[j + (K-1) - k],
 //      dw[k]  += sum_t dpre[t] x[t-(K-1)+k],   dbias += sum_t dpre[t],
 //    and the gradient of the K-1 inputs before position 0 (dconv_prev).
-// A CTA owns kConvTile positions of one (batch row, channel); the sums over positions go to the
-// per-channel gradients with one atomic per tap per CTA.
+// A CTA owns kConvTile positions of one (batch row, channel): it stages that tile of x (with the
+// 3 inputs before it and, backward, 3 after) and of du once in shared memory with coalesced
+// loads, and every tap reads from there; the sums over positions go to the per-channel gradients
+// with one atomic per tap per CTA.
 #pragma once
 #include <stdint.h>
 
@@ -50,20 +52,28 @@ __device__ __forceinline__ float conv_x(const ConvArgs& a, long long row, long l
     return 0.f;
 }
 
-// pre[t]: the taps right-aligned in a 4-tap window, summed from the oldest input (the order of the
-// fused forward kernels).
-template <typename TIn>
-__device__ __forceinline__ float conv_pre(const ConvArgs& a, long long row, const float (&w4)[4], float cb,
-                                          long long t) {
-    float acc = cb;
+// dst[i] = x at position t0 - 3 + i for i < n (0 past L): every load of the thread is issued
+// before the first store, so that each thread keeps several loads in flight.
+template <typename TIn, int MAXN>
+__device__ __forceinline__ void stage_x(float* dst, const ConvArgs& a, long long row, long long t0, int n) {
+    constexpr int PER = (MAXN + kConvThreads - 1) / kConvThreads;
+    float v[PER];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-        if (q >= 4 - a.K) acc = fmaf(w4[q], conv_x<TIn>(a, row, t - 3 + q), acc);
-    return acc;
+    for (int r = 0; r < PER; ++r) {
+        const int i = (int)threadIdx.x + r * kConvThreads;
+        const long long p = t0 - 3 + i;
+        v[r] = (i < n && p < a.L) ? conv_x<TIn>(a, row, p) : 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < PER; ++r) {
+        const int i = (int)threadIdx.x + r * kConvThreads;
+        if (i < n) dst[i] = v[r];
+    }
 }
 
 template <typename TIn>
 __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a) {
+    __shared__ float xs[kConvTile + 3];  // x at t0 - 3 .. t0 + kConvTile - 1
     const long long row = (long long)blockIdx.x / a.ntile;  // b * dim + d
     const long long tile = (long long)blockIdx.x % a.ntile;
     const int d = (int)(row % a.dim);
@@ -73,17 +83,25 @@ __global__ void __launch_bounds__(kConvThreads) conv_fwd_kernel(const ConvArgs a
         if (q >= 4 - a.K) w4[q] = a.w[(long long)d * a.K + q - (4 - a.K)];
     const float cb = a.bias != nullptr ? a.bias[d] : 0.f;
     const long long t0 = tile * kConvTile;
+    stage_x<TIn, kConvTile + 3>(xs, a, row, t0, kConvTile + 3);
+    __syncthreads();
     for (int i = threadIdx.x; i < kConvTile; i += kConvThreads) {
         const long long t = t0 + i;
         if (t >= a.L) break;
-        const float p = conv_pre<TIn>(a, row, w4, cb, t);
+        // pre[t]: the taps right-aligned in a 4-tap window, summed from the oldest input (the
+        // order of the fused forward kernels); xs[i + q] is x[t - 3 + q]
+        float p = cb;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (q >= 4 - a.K) p = fmaf(w4[q], xs[i + q], p);
         store_out<TIn>(static_cast<TIn*>(a.u) + row * a.L + t, a.silu ? p * sigmoid_approx(p) : p);
     }
 }
 
 template <typename TIn>
 __global__ void __launch_bounds__(kConvThreads) conv_bwd_kernel(const ConvArgs a) {
-    __shared__ float dpre_s[kConvTile + 3];  // dpre at t0 .. t0 + kConvTile + K - 2
+    __shared__ float xs[kConvTile + 6];      // x at t0 - 3 .. t0 + kConvTile + 2
+    __shared__ float dpre_s[kConvTile + 3];  // dpre at t0 .. t0 + kConvTile + 2
     __shared__ float red[kConvThreads / 32][5];
     const long long row = (long long)blockIdx.x / a.ntile;
     const long long tile = (long long)blockIdx.x % a.ntile;
@@ -95,22 +113,32 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_kernel(const ConvArgs a
         if (q >= 4 - K) w4[q] = a.w[(long long)d * K + q - (4 - K)];
     const float cb = a.bias != nullptr ? a.bias[d] : 0.f;
     const long long t0 = tile * kConvTile;
-
-    // dpre over the tile and the K-1 positions after it (they reach the tile's last inputs)
-    for (int i = threadIdx.x; i < kConvTile + K - 1; i += kConvThreads) {
-        const long long t = t0 + i;
-        float g = 0.f;
-        if (t < a.L) {
-            const float p = conv_pre<TIn>(a, row, w4, cb, t);
-            const float gu = In<TIn>::to_f32(static_cast<const TIn*>(a.du)[row * a.L + t]);
-            if (a.silu) {
-                const float s = sigmoid_approx(p);
-                g = gu * s * fmaf(p, 1.f - s, 1.f);
-            } else {
-                g = gu;
-            }
+    const TIn* du = static_cast<const TIn*>(a.du) + row * a.L;
+    {
+        constexpr int PER = (kConvTile + 3 + kConvThreads - 1) / kConvThreads;
+        float g[PER];
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {  // du loads issued first, then the x tile's
+            const int i = (int)threadIdx.x + r * kConvThreads;
+            g[r] = (i < kConvTile + 3 && t0 + i < a.L) ? In<TIn>::to_f32(du[t0 + i]) : 0.f;
         }
-        dpre_s[i] = g;
+        stage_x<TIn, kConvTile + 6>(xs, a, row, t0, kConvTile + 6);
+#pragma unroll
+        for (int r = 0; r < PER; ++r) {
+            const int i = (int)threadIdx.x + r * kConvThreads;
+            if (i < kConvTile + 3) dpre_s[i] = g[r];
+        }
+    }
+    __syncthreads();
+    // dpre over the tile and the K-1 positions after it (they reach the tile's last inputs)
+    for (int i = threadIdx.x; i < kConvTile + 3; i += kConvThreads) {
+        if (!a.silu || t0 + i >= a.L) continue;  // identity activation: dpre = du (zero past L)
+        float p = cb;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (q >= 4 - K) p = fmaf(w4[q], xs[i + q], p);
+        const float sg = sigmoid_approx(p);
+        dpre_s[i] = dpre_s[i] * sg * fmaf(p, 1.f - sg, 1.f);
     }
     __syncthreads();
 
@@ -129,7 +157,7 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_kernel(const ConvArgs a
         sb += gp;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            if (q >= 4 - K) sw[q] = fmaf(gp, conv_x<TIn>(a, row, j - 3 + q), sw[q]);
+            if (q >= 4 - K) sw[q] = fmaf(gp, xs[i + q], sw[q]);  // x[j - 3 + q]
     }
     // inputs before position 0: the first tile's CTA
     if (tile == 0 && a.dprev != nullptr && threadIdx.x < K - 1) {

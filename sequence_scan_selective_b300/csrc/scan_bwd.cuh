@@ -74,6 +74,9 @@ struct BwdArgs {
 
 namespace bwd {
 
+// Hint: bring the line holding p into L2 (no register, no completion to wait for).
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kCh = kWarps * 8;  // channels per CTA
@@ -420,11 +423,22 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     }
     float dD_acc = 0.f, dbias_acc = 0.f;
     const int col = (c >> 2) * 16 + 4 * g + (c & 3);  // this lane's dC/dB column after the scatter
+    // The checkpoints of the next tile's slots are prefetched into L2 one tile ahead, so that
+    // each slot's recomputation starts from an L2 hit rather than waiting on HBM.
+    auto prefetch_ck = [&](int k) {
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+            const int gs = kSlots * k + s;
+            if (dvalid && gs >= 1 && gs < a.nslot) prefetch_l2(ck + gs * ckstride);
+        }
+    };
+    prefetch_ck(a.ntile - 1);
     if (VEC) load_tile<TIn, VEC>(smem + ((a.ntile - 1) & 1) * Lt::STAGE, a, b, d0, a.ntile - 1, true);
 #pragma unroll 1
     for (int k = a.ntile - 1; k >= 0; --k) {
         uint8_t* st = smem + (k & 1) * Lt::STAGE;
         const long long t0 = (long long)k * kT;
+        if (k > 0) prefetch_ck(k - 1);
         if (VEC) {
             if (k > 0) {
                 load_tile<TIn, VEC>(smem + ((k - 1) & 1) * Lt::STAGE, a, b, d0, k - 1, true);

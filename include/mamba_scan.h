@@ -205,8 +205,16 @@ int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, const void*
  * one state checkpoint per 8 positions (stream-ordered scratch, cudaMallocAsync on `stream`,
  * b * ceil(L/8) * d * 64 bytes, freed on the same stream), and a reverse sweep recomputes each
  * 8-position slot from its checkpoint and walks it backwards.  States are handled in blocks of
- * 16, one kernel launch each; for dstate > 16 the gradients of u, delta and z are summed over
- * the blocks in fp32 scratch (another 2 or 3 * b * d * L * 4 bytes) and converted at the end.
+ * 16, one kernel launch each.  When batch * ceil(d / 32) is at most 2 * nSM (few channels, e.g.
+ * long sequences), the time axis is also split into segments that run at once (visual guide
+ * section 3.3: the scan operator is associative, and both the state and its gradient are linear
+ * recurrences): a carry launch gives each segment's (prod Abar, own end state), the full launch
+ * runs every segment from its folded start state with no gradient arriving at its end, and a
+ * correction launch adds, from each segment's end backwards, what the gradient carried in from
+ * the later segments contributes, until it has decayed below 2^-40 of its size.  With several
+ * blocks or segments the gradients of u, delta and z are summed in fp32 (in the outputs for fp32
+ * storage; for bf16 in scratch of 2 or 3 * b * d * L * 4 bytes, converted at the end); segments
+ * add nseg * b * d * N * 12 bytes of scratch.
  *
  *   discretization  MAMBA_DISC_SIMPLE or MAMBA_DISC_ZOH: the one the forward pass used.
  *   u .. h0         the forward inputs, as for mamba_scan_fwd_state (z, D, delta_bias, h0 may be

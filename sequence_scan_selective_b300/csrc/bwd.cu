@@ -1,21 +1,32 @@
-// Backward pass: launch of scan_bwd_kernel.
+// Backward pass: launches of scan_bwd_kernel (per block of 16 states; with a split time axis, the
+// carry, full and correction launches) and of the final conversion of the fp32 accumulators.
 #include "host.cuh"
 #include "scan_bwd.cuh"
 
 namespace mscan {
 
-template <typename TIn, bool ZOH>
-static int bwd_launch(const BwdArgs& a, bool vec, cudaStream_t st) {
+template <typename TIn, bool ZOH, int MODE>
+static int bwd_launch(const BwdArgs& a, bool vec, unsigned nz, cudaStream_t st) {
     static AttrCache attr_vec, attr_scalar;
-    auto kern = vec ? scan_bwd_kernel<TIn, true, ZOH> : scan_bwd_kernel<TIn, false, ZOH>;
+    auto kern = vec ? scan_bwd_kernel<TIn, true, ZOH, MODE> : scan_bwd_kernel<TIn, false, ZOH, MODE>;
     int rc = allow_smem(kern, vec ? attr_vec : attr_scalar);
     if (rc) return rc;
-    const dim3 grid((unsigned)((a.dim + bwd::kCh - 1) / bwd::kCh), (unsigned)a.batch);
+    const dim3 grid((unsigned)((a.dim + bwd::kCh - 1) / bwd::kCh), (unsigned)a.batch, nz);
     kern<<<grid, bwd::kThreads, bwd::Layout<TIn>::BYTES, st>>>(a);
     count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "scan_bwd_kernel launch");
     return MAMBA_OK;
+}
+
+template <typename TIn, bool ZOH>
+static int bwd_block(const BwdArgs& a, bool vec, cudaStream_t st) {
+    const unsigned S = (unsigned)a.nseg;
+    int rc = MAMBA_OK;
+    if (S > 1) rc = bwd_launch<TIn, ZOH, bwd::kCarry>(a, vec, S, st);
+    if (rc == MAMBA_OK) rc = bwd_launch<TIn, ZOH, bwd::kFull>(a, vec, S, st);
+    if (rc == MAMBA_OK && S > 1) rc = bwd_launch<TIn, ZOH, bwd::kCorr>(a, vec, S - 1, st);
+    return rc;
 }
 
 template <typename TIn>
@@ -30,19 +41,20 @@ static int finish_launch(const BwdArgs& a, cudaStream_t st) {
     return MAMBA_OK;
 }
 
-// One launch per block of 16 states, in order; with more than one block the per-(channel, step)
-// gradients go through the fp32 accumulators in `a` and a final conversion.
+// One pass per block of 16 states, in order.  With more than one block or a split time axis the
+// per-(channel, step) gradients are summed in fp32 accumulators (for fp32 storage the outputs
+// themselves) and, for bf16 storage, converted at the end.
 int bwd_run(const BwdArgs& a_in, int in_dtype, bool zoh, bool vec, cudaStream_t st) {
     BwdArgs a = a_in;
     const bool bf = in_dtype == MAMBA_BF16;
     for (int nb = 0; nb < a.dstate; nb += bwd::kNS) {
         a.nb = nb;
-        int rc = bf ? (zoh ? bwd_launch<uint16_t, true>(a, vec, st) : bwd_launch<uint16_t, false>(a, vec, st))
-                    : (zoh ? bwd_launch<float, true>(a, vec, st) : bwd_launch<float, false>(a, vec, st));
+        int rc = bf ? (zoh ? bwd_block<uint16_t, true>(a, vec, st) : bwd_block<uint16_t, false>(a, vec, st))
+                    : (zoh ? bwd_block<float, true>(a, vec, st) : bwd_block<float, false>(a, vec, st));
         if (rc) return rc;
     }
-    if (a.acc_du == nullptr) return MAMBA_OK;
-    return bf ? finish_launch<uint16_t>(a, st) : finish_launch<float>(a, st);
+    if (a.acc_du == nullptr || !bf) return MAMBA_OK;
+    return finish_launch<uint16_t>(a, st);
 }
 
 }  // namespace mscan

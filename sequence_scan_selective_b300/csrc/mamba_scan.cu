@@ -403,14 +403,37 @@ static int scan_bwd_impl(const mamba_scan_shape* s, int discretization, const vo
     const bool vec = (L * (long long)es) % 16 == 0 && aligned16(u) && aligned16(delta) && aligned16(dy) &&
                      aligned16(B) && aligned16(C) && aligned16(du) && aligned16(ddelta) && aligned16(dB) &&
                      aligned16(dC) && (!z || aligned16(z)) && (!dz || aligned16(dz));
-    // scratch: the state checkpoints of one block of 16 states (reused by the blocks in turn) and,
-    // for N > 16, fp32 accumulators of du, ddelta (and dz) across the blocks
+    // Split of the time axis, when the CTAs (batch x ceil(dim / 32)) fill at most half of four per
+    // SM: segments of at least kBwdMinSegTiles tiles, about four CTAs per SM.  MAMBA_SCAN_BWD_NSEG
+    // forces a count (tests).
+    constexpr long long kBwdMinSegTiles = 512;
+    const long long nsm = sm_count();
+    const long long ctas = (long long)s->batch * ((s->dim + bwd::kCh - 1) / bwd::kCh);
+    long long S = 1;
+    const int want = env_int("MAMBA_SCAN_BWD_NSEG", 0);
+    if (want > 0) {
+        S = want < a.ntile ? want : a.ntile;
+    } else if (ctas * 2 <= 4 * nsm) {
+        S = 4 * nsm / ctas;
+        const long long smax = a.ntile / kBwdMinSegTiles;
+        if (S > smax) S = smax;
+    }
+    if (S > 4096) S = 4096;
+    if (S < 1) S = 1;
+    a.seg_tiles = (int)((a.ntile + S - 1) / S);
+    a.nseg = (a.ntile + a.seg_tiles - 1) / a.seg_tiles;
+    // scratch: the state checkpoints of one block of 16 states (reused by the blocks in turn);
+    // with several blocks or segments, fp32 accumulators of du, ddelta (and dz) (for fp32
+    // storage the outputs themselves); with segments, their carries and local start gradients
     const size_t nck = a.nslot > 1 ? (size_t)s->batch * a.nslot * s->dim * bwd::kNS * sizeof(float) : 0;
-    const size_t nacc = N > bwd::kNS ? (size_t)chans * L * sizeof(float) : 0;
+    const bool accumulate = N > bwd::kNS || a.nseg > 1;
+    const size_t nacc = accumulate && s->in_dtype == MAMBA_BF16 ? (size_t)chans * L * sizeof(float) : 0;
     const int nacc_t = dz ? 3 : 2;
+    const size_t nstate = (size_t)chans * N;
+    const size_t nseg_b = a.nseg > 1 ? (size_t)a.nseg * nstate * (sizeof(float2) + sizeof(float)) : 0;
     char* scratch = nullptr;
-    if (nck + nacc * nacc_t > 0) {
-        e = cudaMallocAsync(reinterpret_cast<void**>(&scratch), nck + nacc * nacc_t, st);
+    if (nck + nacc * nacc_t + nseg_b > 0) {
+        e = cudaMallocAsync(reinterpret_cast<void**>(&scratch), nck + nacc * nacc_t + nseg_b, st);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(state checkpoints)");
     }
     a.ckpt = nck ? reinterpret_cast<float*>(scratch) : nullptr;
@@ -418,6 +441,14 @@ static int scan_bwd_impl(const mamba_scan_shape* s, int discretization, const vo
         a.acc_du = reinterpret_cast<float*>(scratch + nck);
         a.acc_dd = reinterpret_cast<float*>(scratch + nck + nacc);
         a.acc_dz = dz ? reinterpret_cast<float*>(scratch + nck + 2 * nacc) : nullptr;
+    } else if (accumulate) {  // fp32 storage: accumulate in the outputs
+        a.acc_du = static_cast<float*>(du);
+        a.acc_dd = static_cast<float*>(ddelta);
+        a.acc_dz = static_cast<float*>(dz);
+    }
+    if (nseg_b) {
+        a.carry = reinterpret_cast<float2*>(scratch + nck + nacc * nacc_t);
+        a.mu_local = reinterpret_cast<float*>(scratch + nck + nacc * nacc_t + (size_t)a.nseg * nstate * sizeof(float2));
     }
     const bool zoh = discretization == MAMBA_DISC_ZOH;
     rc = bwd_run(a, s->in_dtype, zoh, vec, st);

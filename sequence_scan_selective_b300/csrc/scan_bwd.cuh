@@ -70,6 +70,13 @@ struct BwdArgs {
     float* acc_du;
     float* acc_dd;
     float* acc_dz;
+    // Split time axis: segment blockIdx.z covers tiles [z * seg_tiles, (z + 1) * seg_tiles).
+    // carry [nseg][b][d][N]: (prod Abar over the segment, end state from the segment's own start:
+    // the initial state for segment 0, zero for the others); mu_local [nseg][b][d][N]: dL/dh at
+    // the segment's start from its own reverse walk (no gradient carried in from later segments).
+    int nseg, seg_tiles;
+    float2* carry;
+    float* mu_local;
 };
 
 namespace bwd {
@@ -88,6 +95,16 @@ constexpr int kNS = 16;          // state capacity (lanes per channel x 4)
 constexpr int kPad = kT + 1;     // padded row (floats) of the per-channel sums r[k][c][t]
 constexpr int kPartPitch = 33;   // padded row (floats) of the dB/dC partials part[t][32 columns]
 constexpr int kBcqPitch = 36;    // floats per step in the B/C step buffer (padded)
+constexpr float kDropBelow = 9.094947017729282e-13f;  // 2^-40
+
+// Launch modes of scan_bwd_kernel.
+//  kFull:  forward sweep (checkpoints) + reverse walk of the segment, from the state carried into
+//          it; gradient at the segment's end: dlast for the last segment, else zero.
+//  kCarry: forward sweep of the segment from its own start only, writing its carry.
+//  kCorr:  reverse walk of a segment from its end with mu = the gradient carried in from the later
+//          segments and no output gradient (dy = 0), adding what that gradient contributes; it stops
+//          once mu has decayed below 2^-40 of its size at the segment's end.
+constexpr int kFull = 0, kCarry = 1, kCorr = 2;
 
 template <typename TIn>
 struct Layout {
@@ -261,7 +278,7 @@ __device__ __forceinline__ void store_steps(TIn* p, long long tg0, long long L, 
 
 }  // namespace bwd
 
-template <typename TIn, bool VEC, bool ZOH>
+template <typename TIn, bool VEC, bool ZOH, int MODE>
 __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArgs a) {
     using namespace bwd;
     using Lt = bwd::Layout<TIn>;
@@ -269,6 +286,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = lane & 7, g = lane >> 3;  // channel lane and state group (also step group)
     const int b = blockIdx.y;
+    const int seg = blockIdx.z;                           // segment of the time axis
+    const int k_begin = seg * a.seg_tiles;                // its tiles
+    const int k_end = min(a.ntile, k_begin + a.seg_tiles);
     const int d0 = blockIdx.x * kCh;
     const int row = warp * 8 + c;  // the lane's channel within the CTA
     const int d = d0 + row;
@@ -308,11 +328,24 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     const float D_once = (dvalid && a.D && a.nb == 0) ? a.D[d] : 0.f;  // the skip term, first state block only
     const long long chrow = ((long long)b * a.dim + d) * a.L;  // start of the channel's rows
 
+    // state before the segment: the initial state (segment 0); in a full launch of a later
+    // segment, segment 0's end state folded with the carries of segments 1 .. seg-1; from zero in
+    // a carry launch
+    const long long cstride = (long long)a.batch * a.dim * N;  // one segment's carries
     float h0v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int n = a.nb + 4 * g + j;  // state (this block's 4g + j)
-        h0v[j] = (a.h0 && dvalid && n < N) ? a.h0[((long long)b * a.dim + d) * N + n] : 0.f;
+        const bool sv = dvalid && n < N;
+        float hv = 0.f;
+        if (seg == 0) {
+            hv = (a.h0 && sv) ? a.h0[((long long)b * a.dim + d) * N + n] : 0.f;
+        } else if (MODE == kFull && sv) {
+            const float2* cr = a.carry + ((long long)b * a.dim + d) * N + n;
+            hv = cr[0].y;
+            for (int q2 = 1; q2 < seg; ++q2) hv = fmaf(cr[q2 * cstride].x, hv, cr[q2 * cstride].y);
+        }
+        h0v[j] = hv;
     }
     float* ck = a.ckpt ? a.ckpt + (((long long)b * a.nslot) * a.dim + d) * kNS + 4 * g : nullptr;
     const long long ckstride = (long long)a.dim * kNS;  // floats between consecutive slots
@@ -379,13 +412,14 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     };
 
     // ---------------------------------------------------------------- forward sweep: checkpoints
-    if (a.nslot > 1) {
+    if (MODE == kCarry || (MODE == kFull && a.nslot > 1)) {
         float2 h[2] = {make_float2(h0v[0], h0v[1]), make_float2(h0v[2], h0v[3])};
-        if (VEC) load_tile<TIn, VEC>(smem, a, b, d0, 0, false);
-        for (int k = 0; k < a.ntile; ++k) {
+        float sumdt = 0.f;  // carry launch: sum of Delta over the segment
+        if (VEC) load_tile<TIn, VEC>(smem + (k_begin & 1) * Lt::STAGE, a, b, d0, k_begin, false);
+        for (int k = k_begin; k < k_end; ++k) {
             uint8_t* st = smem + (k & 1) * Lt::STAGE;
             if (VEC) {
-                if (k + 1 < a.ntile) {
+                if (k + 1 < k_end) {
                     load_tile<TIn, VEC>(smem + ((k + 1) & 1) * Lt::STAGE, a, b, d0, k + 1, false);
                     cp_async_wait<1>();
                 } else {
@@ -402,25 +436,58 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
             for (int s = 0; s < kSlots; ++s) {
                 const int gs = kSlots * k + s;
                 if (gs >= a.nslot) break;
-                if (gs >= 1 && dvalid) *reinterpret_cast<float4*>(ck + gs * ckstride) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+                if (MODE == kFull && gs >= 1 && dvalid)
+                    *reinterpret_cast<float4*>(ck + gs * ckstride) = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
 #pragma unroll
                 for (int i = 0; i < bwd::kSlot; ++i) {
                     const int t = s * bwd::kSlot + i;
                     const float4 qq = q[t * 8 + c];
                     const float4 bq = *reinterpret_cast<const float4*>(bcq + t * kBcqPitch + 4 * g);
                     advance(h, qq, bq);
+                    if (MODE == kCarry) sumdt += qq.x;
                 }
             }
             __syncthreads();
         }
+        if constexpr (MODE == kCarry) {
+            // (prod Abar = 2^(A log2(e) sum Delta), end state from the segment's own start)
+            if (dvalid) {
+                float2* cw = a.carry + (long long)seg * cstride + ((long long)b * a.dim + d) * N;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int n = a.nb + 4 * g + j;
+                    if (n < N) cw[n] = make_float2(ex2_approx(el(A2, j) * sumdt), el(h, j));
+                }
+            }
+            return;
+        }
     }
     // ---------------------------------------------------------------- reverse sweep
+    // mu = dL/dh at the segment's end: dlast for the last segment; in a full launch of an earlier
+    // segment zero (its own part only); in a correction launch the gradient carried in from the
+    // later segments, folded back from the last one (whose own walk started from dlast, so that its
+    // mu_local is already its whole start gradient): mu_end(s) = mu_start(s+1) with
+    // mu_start(S-1) = mu_local(S-1) and mu_start(q) = mu_local(q) + P(q) mu_start(q+1)
     float2 mu[2], dAacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float thr = 0.f;  // correction launch: stop once every |mu| is at most this
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int n = a.nb + 4 * g + j;  // state (this block's 4g + j)
-        el(mu, j) = (a.dlast && dvalid && n < N) ? a.dlast[((long long)b * a.dim + d) * N + n] : 0.f;
+        const bool sv = dvalid && n < N;
+        const long long sn = ((long long)b * a.dim + d) * N + n;
+        float m = (a.dlast && sv) ? a.dlast[sn] : 0.f;
+        if (MODE == kFull && seg != a.nseg - 1) m = 0.f;
+        if (MODE == kCorr && sv) {
+            m = a.mu_local[(a.nseg - 1) * cstride + sn];
+            for (int q2 = a.nseg - 2; q2 > seg; --q2) m = fmaf(a.carry[q2 * cstride + sn].x, m, a.mu_local[q2 * cstride + sn]);
+            // gradient at the initial state: segment 0's own part plus what reaches it through
+            // the whole of segment 0
+            if (seg == 0 && a.dh0) a.dh0[sn] = fmaf(a.carry[sn].x, m, a.mu_local[sn]);
+        }
+        el(mu, j) = m;
+        thr = fmaxf(thr, fabsf(m));
     }
+    thr = thr <= 3.4028234663852886e38f ? thr * kDropBelow : 0.f;  // (an infinite or NaN gradient is never dropped)
     float dD_acc = 0.f, dbias_acc = 0.f;
     const int col = (c >> 2) * 16 + 4 * g + (c & 3);  // this lane's dC/dB column after the scatter
     // The checkpoints of the next tile's slots are prefetched into L2 one tile ahead, so that
@@ -432,15 +499,15 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
             if (dvalid && gs >= 1 && gs < a.nslot) prefetch_l2(ck + gs * ckstride);
         }
     };
-    prefetch_ck(a.ntile - 1);
-    if (VEC) load_tile<TIn, VEC>(smem + ((a.ntile - 1) & 1) * Lt::STAGE, a, b, d0, a.ntile - 1, true);
+    prefetch_ck(k_end - 1);
+    if (VEC) load_tile<TIn, VEC>(smem + ((k_end - 1) & 1) * Lt::STAGE, a, b, d0, k_end - 1, true);
 #pragma unroll 1
-    for (int k = a.ntile - 1; k >= 0; --k) {
+    for (int k = k_end - 1; k >= k_begin; --k) {
         uint8_t* st = smem + (k & 1) * Lt::STAGE;
         const long long t0 = (long long)k * kT;
-        if (k > 0) prefetch_ck(k - 1);
+        if (k > k_begin) prefetch_ck(k - 1);
         if (VEC) {
-            if (k > 0) {
+            if (k > k_begin) {
                 load_tile<TIn, VEC>(smem + ((k - 1) & 1) * Lt::STAGE, a, b, d0, k - 1, true);
                 cp_async_wait<1>();
             } else {
@@ -451,7 +518,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
         }
         __syncthreads();
         transpose_bc(st);
-        phase_a(st, k, true);
+        phase_a(st, k, MODE != kCorr);  // a correction sees no output gradient: e = 0
         __syncthreads();
 
 #pragma unroll 1
@@ -574,14 +641,15 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
             }
             if (dvalid) {
                 const long long tg0 = t0 + kSPL * g, off = chrow + tg0;
-                if (a.acc_du != nullptr) {  // state blocks: add into the fp32 accumulators
-                    const bool first = a.nb == 0;
+                if (a.acc_du != nullptr) {  // state blocks or segments: add into the fp32 accumulators
+                    const bool first = MODE == kFull && a.nb == 0;
 #pragma unroll
                     for (int j = 0; j < kSPL; ++j) {
                         if (tg0 + j >= a.L) break;
                         a.acc_du[off + j] = (first ? 0.f : a.acc_du[off + j]) + o_du[j];
                         a.acc_dd[off + j] = (first ? 0.f : a.acc_dd[off + j]) + o_dd[j];
-                        if (gate && a.acc_dz) a.acc_dz[off + j] = (first ? 0.f : a.acc_dz[off + j]) + o_dz[j];
+                        if (MODE == kFull && gate && a.acc_dz)
+                            a.acc_dz[off + j] = (first ? 0.f : a.acc_dz[off + j]) + o_dz[j];
                     }
                 } else {
                     store_steps<TIn, VEC>(static_cast<TIn*>(a.du) + off, tg0, a.L, o_du);
@@ -600,7 +668,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
                 const int gi = tid + rep * kThreads;  // 32 columns x kT/4 groups of 4 steps
                 const int colr = gi / (kT / 4), tq = gi % (kT / 4);
                 const int kind = colr >> 4, n = a.nb + (colr & 15);
-                if (n < N) {
+                if (n < N && (MODE != kCorr || kind == 1)) {  // a correction changes dB only
                     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w)
@@ -618,7 +686,19 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
                 }
             }
         }
-        __syncthreads();
+        if constexpr (MODE == kCorr) {
+            // stop once the carried-in gradient has decayed in every lane of the CTA (the copies
+            // of the next tile are still in flight: let them land first)
+            bool small = true;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) small = small && fabsf(el(mu, j)) <= thr;
+            if (__syncthreads_and(small)) {
+                if (VEC) cp_async_wait<0>();
+                break;
+            }
+        } else {
+            __syncthreads();
+        }
     }
 
     // ---------------------------------------------------------------- per-channel results
@@ -627,7 +707,12 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
         const int n = a.nb + 4 * g + j;  // state (this block's 4g + j)
         if (dvalid && n < N) {
             atomicAdd(a.dA + (long long)d * N + n, el(dAacc, j));
-            if (a.dh0) a.dh0[((long long)b * a.dim + d) * N + n] = el(mu, j);
+            // gradient at the segment's start: the initial state's gradient when the time axis
+            // is not split; with a split, this segment's own part (the correction launch of
+            // segment 0 combines them)
+            const long long sn = ((long long)b * a.dim + d) * N + n;
+            if (MODE == kFull && a.nseg > 1) a.mu_local[(long long)seg * cstride + sn] = el(mu, j);
+            else if (MODE == kFull && a.dh0) a.dh0[sn] = el(mu, j);
         }
     }
     dD_acc += __shfl_xor_sync(0xffffffffu, dD_acc, 8);
@@ -635,7 +720,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, 8);
     dbias_acc += __shfl_xor_sync(0xffffffffu, dbias_acc, 16);
     if (dvalid && g == 0) {
-        if (a.dD && a.nb == 0) atomicAdd(a.dD + d, dD_acc);
+        if (MODE == kFull && a.dD && a.nb == 0) atomicAdd(a.dD + d, dD_acc);
         if (a.dbias) atomicAdd(a.dbias + d, dbias_acc);
     }
 }

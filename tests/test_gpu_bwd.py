@@ -188,6 +188,82 @@ def test_bwd_wide_state_optional_inputs(ms, disc):
     _compare(got, ref, cfg.dtype)
 
 
+class _env:
+    def __init__(self, **kv):
+        self.kv, self.old = kv, {}
+
+    def __enter__(self):
+        import os
+        for k, v in self.kv.items():
+            self.old[k] = os.environ.get(k)
+            os.environ[k] = v
+
+    def __exit__(self, *exc):
+        import os
+        for k, v in self.old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("nseg", [2, 5])
+def test_bwd_split_time_axis(ms, dtype, nseg):
+    """The time axis split into segments (carry launch, full launch per segment, correction
+    launch from each segment's end) gives the oracle's gradients."""
+    cfg = synth.CONFIGS["long"].replace(batch=2, dim=40, seqlen=6000, dtype=dtype, seed=200 + nseg)
+    with _env(MAMBA_SCAN_BWD_NSEG=str(nseg)):
+        _check(ms, cfg)
+
+
+@pytest.mark.parametrize("disc", ["simple", "zoh"])
+def test_bwd_split_options(ms, disc):
+    """Split time axis with the hold, without z and D, and with 24 states (two state blocks)."""
+    cfg = synth.CONFIGS["long"].replace(batch=1, dim=33, dstate=24, seqlen=3001, seed=210)
+    inp = _inputs(cfg, drop=("z", "D"))
+    d = dev_inputs(inp, cfg.dtype)
+    f32 = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+    with _env(MAMBA_SCAN_BWD_NSEG="4"):
+        got = ms.mamba_scan_bwd(d["u"], d["delta"], d["A"], d["B"], d["C"], to_dev(inp["dy"], cfg.dtype), None,
+                                None, d.get("delta_bias"), True, h0=f32(inp["h0"]), dlast_state=f32(inp["dlast"]),
+                                disc=disc)
+        torch.cuda.synchronize()
+    got = {k: (None if v is None else from_dev(v)) for k, v in got.items()}
+    ref = oracle.scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], synth.widen(inp["dy"], cfg.dtype),
+                          None, None, inp.get("delta_bias"), True, cfg.dtype, h0=inp["h0"],
+                          dlast_state=inp["dlast"], disc=disc)
+    _compare(got, ref, cfg.dtype)
+
+
+def test_bwd_split_without_decay(ms):
+    """States with A = 0 never forget: the gradient carried into a segment reaches all of it, so
+    the correction launch walks the whole segment."""
+    cfg = synth.CONFIGS["long"].replace(batch=1, dim=24, seqlen=4000, seed=220)
+    inp = _inputs(cfg)
+    inp["A"] = inp["A"].copy()
+    inp["A"][:, :2] = 0.0
+    inp["A"][3, :] = 0.0
+    got = None
+    with _env(MAMBA_SCAN_BWD_NSEG="3"):
+        got = _gpu(ms, inp, cfg.dtype)
+    ref = _oracle(inp, cfg.dtype)
+    _compare(got, ref, cfg.dtype)
+
+
+def test_bwd_segment_count_invariance(ms):
+    cfg = synth.CONFIGS["long"].replace(batch=1, dim=32, seqlen=8192, seed=230)
+    inp = _inputs(cfg)
+    outs = []
+    for nseg in ("1", "4", "16"):
+        with _env(MAMBA_SCAN_BWD_NSEG=nseg):
+            outs.append(_gpu(ms, inp, cfg.dtype))
+    for o in outs[1:]:
+        for k in GRADS:
+            if o.get(k) is not None:
+                assert rel_err(o[k], outs[0][k]) <= 1e-5, k
+
+
 def test_bwd_rejects_unsupported(ms):
     cfg = synth.CONFIGS["m130"].replace(batch=1, dim=8, dstate=16, seqlen=16, seed=170)
     inp = _inputs(cfg)
@@ -199,3 +275,15 @@ def test_bwd_rejects_unsupported(ms):
                                                         "dB": torch.empty_like(d["B"]),
                                                         "dC": torch.empty_like(d["C"]), "dD": None,
                                                         "ddelta_bias": None, "dh0": None})
+
+
+def test_bwd_million_steps_library_plan(ms):
+    """2^20 steps on few channels, with the library's own split of the time axis (no forced
+    count: here 128 segments on a 148-SM device), against the oracle's gradients of every tensor."""
+    cfg = synth.CONFIGS["long"].replace(batch=1, dim=64, seed=240)
+    inp = _inputs(cfg)
+    n0 = ms.launch_count()
+    got = _gpu(ms, inp, cfg.dtype)
+    assert ms.launch_count() - n0 >= 3  # carry, full and correction launches
+    ref = _oracle(inp, cfg.dtype)
+    _compare(got, ref, cfg.dtype)

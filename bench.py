@@ -556,8 +556,36 @@ def run_e2e(args, cfg, inp, dec, params, dev, world, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_tot = float(t[0])
     elems = cfg.batch * cfg.dim * (cfg.seqlen + 1) * K * world
+    # context: the same bytes moved by plain copies alone (host -> device and device -> host on two
+    # streams at once), the floor the host link sets for this step
+    src_h = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    dst_d = torch.empty(h2d, dtype=torch.uint8, device=dev)
+    src_d = torch.empty(d2h, dtype=torch.uint8, device=dev)
+    dst_h = torch.empty(d2h, dtype=torch.uint8).pin_memory()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    cur = torch.cuda.current_stream(dev)
+
+    def copies():
+        s_in.wait_stream(cur)
+        s_out.wait_stream(cur)
+        with torch.cuda.stream(s_in):
+            dst_d.copy_(src_h, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            dst_h.copy_(src_d, non_blocking=True)
+        cur.wait_stream(s_in)
+        cur.wait_stream(s_out)
+
+    copies()
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(K):
+        copies()
+    b.record()
+    torch.cuda.synchronize()
+    link_ms = a.elapsed_time(b) / K
     return {"value": elems / (ms_tot * 1e-3), "unit": "elements/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": ms_tot / K}
+            "d2h_bytes_per_step": int(d2h), "steps": K, "ms_per_step": ms_tot / K,
+            "copies_alone_ms_per_step": round(link_ms, 3), "copies_alone_fraction": round(link_ms / (ms_tot / K), 3)}
 
 
 # ------------------------------------------------------------------------------------ CPU oracle

@@ -20,17 +20,17 @@ namespace mscan {
 // segment count minimises that estimate.
 constexpr long long kFixSteps = 4096;
 
-template <typename TIn, int NP, int LPC>
+template <typename TIn, int NP>
 static int plan_cl(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     constexpr int TC = Chunk<TIn>::TC;
-    constexpr int CPW = cl::Lanes<LPC>::CPW;
+    constexpr int CPW = cl::Lanes::CPW;
     constexpr int TILE = CPW * cl::kRowBytes;
-    constexpr int YTILE = cl::Lanes<LPC>::YTILE;
+    constexpr int YTILE = cl::Lanes::YTILE;
     const long long L = s->seqlen;
     p.upr = (s->dim + CPW - 1) / CPW;
     auto stage_of = [&](int w) { return round_up(3 * w * TILE + 2 * NP * cl::kRowBytes + TC * cl::Quads<NP>::PITCH, 1024); };
     auto smem_of = [&](int w, int ns) { return ns * stage_of(w) + w * 2 * YTILE + (3 * ns + 1) * 8 + 1024; };
-    int wcap = cl::Lanes<LPC>::MAX_WARPS;
+    int wcap = cl::Lanes::MAX_WARPS;
     while (wcap > 1 && smem_of(wcap, 2) > kSmemLimit) --wcap;
     const int wforce = env_int("MAMBA_SCAN_WMAX", 0);
     if (wforce > wcap) return fail(MAMBA_ERR_ARG, "MAMBA_SCAN_WMAX above %d", wcap);
@@ -113,24 +113,24 @@ static int launch_kernel(void (*kern)(const FwdArgs, const FwdMaps), AttrCache& 
 
 // Channel-per-lane kernel: data path and discretisation / convolution mode are template
 // parameters; softplus and the gate are runtime flags.
-template <typename TIn, int NP, int LPC, bool TMA, bool LOCAL, int MODE>
+template <typename TIn, int NP, bool TMA, bool LOCAL, int MODE>
 static int launch_cl_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
     static AttrCache attr;
-    return launch_kernel(scan_fwd_cl_kernel<TIn, NP, LPC, TMA, LOCAL, MODE>, attr, a, maps, grid, smem_bytes, st);
+    return launch_kernel(scan_fwd_cl_kernel<TIn, NP, TMA, LOCAL, MODE>, attr, a, maps, grid, smem_bytes, st);
 }
 
-template <typename TIn, int NP, int LPC, bool LOCAL>
+template <typename TIn, int NP, bool LOCAL>
 static int launch_cl(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, bool tma, int mode,
                      cudaStream_t st) {
     switch (mode) {
-        case 0: return tma ? launch_cl_one<TIn, NP, LPC, true, LOCAL, 0>(a, maps, grid, smem_bytes, st)
-                           : launch_cl_one<TIn, NP, LPC, false, LOCAL, 0>(a, maps, grid, smem_bytes, st);
-        case 1: return tma ? launch_cl_one<TIn, NP, LPC, true, LOCAL, 1>(a, maps, grid, smem_bytes, st)
-                           : launch_cl_one<TIn, NP, LPC, false, LOCAL, 1>(a, maps, grid, smem_bytes, st);
-        case 2: return tma ? launch_cl_one<TIn, NP, LPC, true, LOCAL, 2>(a, maps, grid, smem_bytes, st)
-                           : launch_cl_one<TIn, NP, LPC, false, LOCAL, 2>(a, maps, grid, smem_bytes, st);
-        default: return tma ? launch_cl_one<TIn, NP, LPC, true, LOCAL, 3>(a, maps, grid, smem_bytes, st)
-                            : launch_cl_one<TIn, NP, LPC, false, LOCAL, 3>(a, maps, grid, smem_bytes, st);
+        case 0: return tma ? launch_cl_one<TIn, NP, true, LOCAL, 0>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, false, LOCAL, 0>(a, maps, grid, smem_bytes, st);
+        case 1: return tma ? launch_cl_one<TIn, NP, true, LOCAL, 1>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, false, LOCAL, 1>(a, maps, grid, smem_bytes, st);
+        case 2: return tma ? launch_cl_one<TIn, NP, true, LOCAL, 2>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, false, LOCAL, 2>(a, maps, grid, smem_bytes, st);
+        default: return tma ? launch_cl_one<TIn, NP, true, LOCAL, 3>(a, maps, grid, smem_bytes, st)
+                            : launch_cl_one<TIn, NP, false, LOCAL, 3>(a, maps, grid, smem_bytes, st);
     }
 }
 
@@ -158,11 +158,11 @@ static int launch_fix(const FwdArgs& a, const FixMaps& maps, bool tma, cudaStrea
 template <typename TIn, int NP>
 static int run(const mamba_scan_shape* s, FwdArgs a, bool softplus, float2* scratch, size_t cap, cudaStream_t st) {
     constexpr int TC = Chunk<TIn>::TC;
-    constexpr int CPW = cl::Lanes<1>::CPW;
+    constexpr int CPW = cl::Lanes::CPW;
     const int esize = (int)sizeof(TIn);
     const long long L = s->seqlen;
     FwdPlan p;
-    int rc = plan_cl<TIn, NP, 1>(s, sm_count(), p);
+    int rc = plan_cl<TIn, NP>(s, sm_count(), p);
     if (rc) return rc;
     const bool tma = fwd_tma_ok(a, L, esize);
     FwdMaps maps;
@@ -178,14 +178,14 @@ static int run(const mamba_scan_shape* s, FwdArgs a, bool softplus, float2* scra
     const int mode = (a.zoh ? 1 : 0) | (a.conv_w != nullptr ? 2 : 0);
     if (p.nseg == 1) {
         const unsigned grid = (unsigned)((long long)s->batch * p.kcta);
-        return launch_cl<TIn, NP, 1, false>(a, maps, grid, p.smem_bytes, tma, mode, st);
+        return launch_cl<TIn, NP, false>(a, maps, grid, p.smem_bytes, tma, mode, st);
     }
     const size_t nstate = (size_t)s->batch * s->dim * s->dstate;
     bool owned = false;
     rc = carries_get((size_t)p.nseg * nstate * sizeof(float2), 0, scratch, cap, p.nseg, st, &a.agg, &owned);
     if (rc) return rc;
     const unsigned grid = (unsigned)((long long)s->batch * p.nseg * p.kcta);
-    rc = launch_cl<TIn, NP, 1, true>(a, maps, grid, p.smem_bytes, tma, mode, st);
+    rc = launch_cl<TIn, NP, true>(a, maps, grid, p.smem_bytes, tma, mode, st);
     if (rc == MAMBA_OK) {
         FixMaps fm;
         memset(&fm, 0, sizeof fm);

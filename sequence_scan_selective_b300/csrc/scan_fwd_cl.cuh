@@ -8,10 +8,7 @@
 // B300 SM's pipes:
 //  * Lane = channel.  A lane owns every state of its channel, so the per-element work (softplus
 //    step size, Delta x, D x, silu gate) is done once, by the lane that needs it, and the readout
-//    C.h is summed in registers: no exchange between lanes at all.  When the channels give fewer
-//    than two warps per SM sub-partition, a channel's states can be split over two lanes instead
-//    (LPC = 2), which doubles the warps at the cost of duplicated per-element work and one
-//    shuffle per step.
+//    C.h is summed in registers: no exchange between lanes at all.
 //  * B and C are the same for every channel of a batch row, so all 32 lanes of a warp read the
 //    same (B_n, B_n+1, C_n, C_n+1) quad at each step: a broadcast 16-byte shared-memory load,
 //    which the SM serves at about one per clock.  The producer warp builds the quads once per
@@ -39,14 +36,11 @@ namespace cl {
 
 constexpr int kRowBytes = 128;     // bytes per tile row (one chunk of one channel)
 
-// LPC lanes share one channel (LPC = 1: all NP states in one lane; LPC = 2: NP / 2 states in each
-// of lanes c and c + 16, which both do the channel's per-element work and add their readout
-// partials with one shuffle per step).  A CTA holds up to 4 * LPC consumer warps: one (LPC = 1) or
-// two (LPC = 2) per SM sub-partition.
-template <int LPC>
+// A work unit is 32 channels of one batch row, one per lane of a consumer warp; a CTA holds up
+// to 4 consumer warps, one per SM sub-partition.
 struct Lanes {
-    static constexpr int CPW = 32 / LPC;                 // channels per warp (work unit)
-    static constexpr int MAX_WARPS = 4 * LPC;            // consumer warps per CTA
+    static constexpr int CPW = 32;                       // channels per warp (work unit)
+    static constexpr int MAX_WARPS = 4;                  // consumer warps per CTA
     static constexpr int YTILE = CPW * kRowBytes;        // one warp's y staging tile
 };
 
@@ -100,22 +94,22 @@ __device__ __forceinline__ void tile_store16<uint16_t>(unsigned char* tile, int 
 // convolution in front of the scan (guide section 3.5): the u tile then holds the block input x,
 // and the lane forms u[t] = act(conv_bias + sum_k conv_w[k] x[t-K+1+k]) itself, keeping the last
 // three inputs of its channel in registers from block to block.
-template <typename TIn, int NP, int LPC, bool TMA, bool LOCAL, int MODE>
-__global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
+template <typename TIn, int NP, bool TMA, bool LOCAL, int MODE>
+__global__ void __launch_bounds__(32 * (cl::Lanes::MAX_WARPS + 1), 1)
     scan_fwd_cl_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps) {
     constexpr int TC = Chunk<TIn>::TC;
     constexpr int ES = (int)sizeof(TIn);
     constexpr int BLK = 16 / ES;  // steps per 16-byte tile read
     constexpr int NPAIR = NP / 2;
     constexpr int QPITCH = cl::Quads<NP>::PITCH;
-    constexpr int CPW = cl::Lanes<LPC>::CPW;
-    constexpr int PL = NPAIR / LPC;            // state pairs per lane
+    constexpr int CPW = cl::Lanes::CPW;
+    constexpr int PL = NPAIR;                  // state pairs per lane
     constexpr int TILE = CPW * cl::kRowBytes;  // one warp's rows of one input tile
     constexpr bool ZOH = (MODE & 1) != 0;
     constexpr bool CONV = (MODE & 2) != 0;
     const bool has_z = a.z != nullptr;
     const bool softplus = a.softplus != 0;
-    static_assert(NP % (2 * LPC) == 0 && NP <= 16 && (LPC == 1 || LPC == 2), "shape");
+    static_assert(NP % 2 == 0 && NP <= 16, "shape");
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -244,7 +238,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
     if (wid >= nunits) return;
 
     // ====================================================================== consumer warps
-    const int c = lane % CPW, g = lane / CPW;  // channel within the unit, state group
+    const int c = lane;  // channel within the unit
     const int dch = (u0 + wid) * CPW + c;
     const bool cvalid = dch < a.dim;
     const long long row = (long long)b * a.dim + (cvalid ? dch : 0);
@@ -252,13 +246,13 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
     const float Dd = (cvalid && a.D != nullptr) ? a.D[dch] : 0.f;
     const int trow = wid * CPW + c;  // this lane's row in the CTA's u, delta, z tiles
 
-    // the lane's states: pairs g * PL .. g * PL + PL - 1
+    // the lane's states, as pairs (2p, 2p + 1)
     float2 A2[PL], h[PL], invA[ZOH ? PL : 1];
     // segment 0 starts from the initial state, later segments (LOCAL) from zero
     const float* h0 = (seg == 0 && cvalid && a.h0 != nullptr) ? a.h0 + row * N : nullptr;
 #pragma unroll
     for (int p = 0; p < PL; ++p) {
-        const int n0 = 2 * (g * PL + p), n1 = n0 + 1;
+        const int n0 = 2 * p, n1 = n0 + 1;
         const float a0 = (cvalid && n0 < N) ? a.A[(long long)dch * N + n0] : 0.f;
         const float a1 = (cvalid && n1 < N) ? a.A[(long long)dch * N + n1] : 0.f;
         A2[p] = make_float2(a0 * kLog2e, a1 * kLog2e);
@@ -286,7 +280,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
         }
     }
 
-    constexpr int YTILE = cl::Lanes<LPC>::YTILE;
+    constexpr int YTILE = cl::Lanes::YTILE;
     unsigned char* ystage = smem + a.scratch_off + wid * 2 * YTILE;
     float sumdt = 0.f;
     bool ok = true;
@@ -380,7 +374,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
                 const float dq = (j & 1) ? dt[j / 2].y : dt[j / 2].x;
                 const float duq = (j & 1) ? du[j / 2].y : du[j / 2].x;
                 const float uq = uv[j];
-                const float4* qrow = reinterpret_cast<const float4*>(qbase + (blk * BLK + j) * QPITCH) + g * PL;
+                const float4* qrow = reinterpret_cast<const float4*>(qbase + (blk * BLK + j) * QPITCH);
                 float2 ya = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int p = 0; p < PL; ++p) {
@@ -403,7 +397,6 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
                 }
                 if (LOCAL) sumdt += dq;
                 yv[j] = ya.x + ya.y;
-                if (LPC == 2) yv[j] += __shfl_xor_sync(0xffffffffu, yv[j], 16);
             }
             float yo[BLK];
 #pragma unroll
@@ -413,8 +406,8 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
                 yo[2 * j + 1] = y2.y;
             }
             if (TMA) {
-                if (g == 0) cl::tile_store16<TIn>(ybuf, c, blk * 16, yo);
-            } else if (cvalid && g == 0) {
+                cl::tile_store16<TIn>(ybuf, c, blk * 16, yo);
+            } else if (cvalid) {
                 TIn* gy = static_cast<TIn*>(a.y) + row * a.L;
 #pragma unroll
                 for (int j = 0; j < BLK; ++j)
@@ -452,7 +445,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
         float2* ag = a.agg + (((long long)seg * a.batch + b) * a.dim + dch) * N;
 #pragma unroll
         for (int p = 0; p < PL; ++p) {
-            const int n0 = 2 * (g * PL + p), n1 = n0 + 1;
+            const int n0 = 2 * p, n1 = n0 + 1;
             if (n0 < N) ag[n0] = make_float2(ex2_approx(A2[p].x * sumdt), h[p].x);
             if (n1 < N) ag[n1] = make_float2(ex2_approx(A2[p].y * sumdt), h[p].y);
         }
@@ -460,7 +453,7 @@ __global__ void __launch_bounds__(32 * (cl::Lanes<LPC>::MAX_WARPS + 1), 1)
         float* ls = a.last_state + row * N;
 #pragma unroll
         for (int p = 0; p < PL; ++p) {
-            const int n0 = 2 * (g * PL + p), n1 = n0 + 1;
+            const int n0 = 2 * p, n1 = n0 + 1;
             if (n0 < N) ls[n0] = h[p].x;
             if (n1 < N) ls[n1] = h[p].y;
         }

@@ -108,6 +108,25 @@ def bwd_bytes(cfg) -> int:
     return b * d * L * 7 * s + b * n * L * (2 * s + 2 * 4) + 2 * d * (n + 2) * 4 + 3 * b * d * n * 4
 
 
+# FP32 arithmetic floor of the scan: per state-update the recurrence needs 4 FP32 lane operations
+# (Delta A, (Delta u) B, Abar h + ..., C.h accumulation; an FMA counts once) and one exp2.  The
+# FP32 pipe does 128 lane operations per clock per SM (32 exp2 per clock per SM on the MUFU pipe,
+# measured, so both pipes give the same floor); B300: 148 SMs at 2032 MHz at most.
+ALU_OPS_PER_STATE_UPDATE = 4
+ALU_PEAK_TOPS = 128 * 148 * 2.032e9 / 1e12
+
+
+def alu_context(cfg, kernel_ms):
+    """The forward scan's FP32 arithmetic against the FP32 pipe's peak (context beside the HBM
+    roofline: for these shapes the arithmetic floor lies above the HBM floor)."""
+    ops = ALU_OPS_PER_STATE_UPDATE * cfg.batch * cfg.dim * cfg.seqlen * cfg.dstate
+    achieved = ops / (kernel_ms * 1e-3) / 1e12
+    return {"achieved": round(achieved, 2), "peak": round(ALU_PEAK_TOPS, 2), "unit": "Top/s",
+            "frac": round(achieved / ALU_PEAK_TOPS, 4), "ops_per_launch": ops,
+            "peak_source": "derived: 128 FP32 lanes/clk/SM x 148 SMs x 2032 MHz",
+            "floor_us": round(ops / (ALU_PEAK_TOPS * 1e12) * 1e6, 1)}
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -406,6 +425,7 @@ def run_ours(args, cfg, rank, world, local_rank):
                    "scan_kernel": kname,
                    "l2": "inputs larger than L2; two input sets alternate"},
         "roofline": roofline,
+        "alu_context": alu_context(cfg, scan_avg_ms),
         "clocks": clk.summary(),
         "gpu_launches": launches,
         "e2e": e2e,

@@ -112,3 +112,35 @@ def test_noalloc_rejects_scratch_overflow(ms):
             ms.mamba_scan_fwd_noalloc(x, x.clone(), A, Bm, Bm.clone())
     finally:
         os.environ.pop("MAMBA_SCAN_NSEG", None)
+
+
+def _header_bound_bytes(batch, dim, N, L, dtype, nsm):
+    """The scratch bound include/mamba_scan.h states for a shape: S segments at most, times the
+    bytes of one segment's carries (S of them for N <= 16, S - 1 above)."""
+    tc = 32 if dtype == "f32" else 64
+    smax_len = max(1, L // (8 * tc))
+    if N <= 16:
+        units = batch * -(-dim // 32)
+        S = 1 if units * 2 > 4 * nsm else min(-(-4 * nsm // units) + 1, smax_len)
+        nseg_carries = S
+    else:
+        units = batch * -(-dim // 8)
+        S = 1 if units >= 5 * nsm else min(-(-10 * nsm // units), smax_len)
+        nseg_carries = S - 1
+    return 0 if S <= 1 else nseg_carries * batch * dim * N * 8
+
+
+@pytest.mark.parametrize("dim,L", [(32, 8192), (64, 65536), (256, 16384), (1536, 32768)])
+def test_noalloc_shapes_within_the_stated_bound(ms, dim, L):
+    """Shapes whose stated bound fits the fixed scratch are accepted and match the regular entry
+    point (the bound is what a caller can compute from the shape and the SM count)."""
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    bound = _header_bound_bytes(1, dim, 16, L, "f32", nsm)
+    assert bound <= 4 << 20, bound
+    cfg = synth.CONFIGS["long"].replace(batch=1, dim=dim, seqlen=L, seed=50 + dim)
+    d = dev_inputs(synth.scan_inputs(cfg), "f32")
+    y_ref, st_ref = ms.mamba_scan_fwd(*_args(d))
+    y, st = ms.mamba_scan_fwd_noalloc(*_args(d))
+    torch.cuda.synchronize()
+    assert rel_err(from_dev(y), from_dev(y_ref)) <= TOL["f32"]
+    assert rel_err(from_dev(st), from_dev(st_ref)) <= TOL["f32"]

@@ -939,6 +939,9 @@ def run_bwd(args, cfg, rank, world, local_rank):
     launches = ms.launch_count() - n0
     total_ms = t_start.elapsed_time(t_end)
     total_ms, avg_ms, launches = aggregate_ranks(dist, dev, total_ms, total_ms / K, launches)
+    train = None
+    if not args.conv and cfg.dstate <= 16:
+        train = train_step_times(ms, sets, params, out, stream, W, K)
     elems_step = cfg.batch * cfg.dim * cfg.seqlen
     peaks, kind = measured_peaks()
     bb = bwd_bytes(cfg)
@@ -969,9 +972,74 @@ def run_bwd(args, cfg, rank, world, local_rank):
         "gpu_launches": launches,
         "e2e": None,
     }
+    if train is not None:
+        line["train_step"] = train
     if dist:
         dist.destroy_process_group()
     return line
+
+
+def train_step_times(ms, sets, params, out, stream, W, K):
+    """Forward + backward of one training step, two ways: the forward scan and a backward pass that
+    recomputes its checkpoints in a forward sweep, or the training forward pass (which writes the
+    checkpoints) and a backward pass that starts from them.  Each leg device-timed alone over K
+    launches, the input sets alternating as in the backward line."""
+    import torch
+
+    ys = [torch.empty_like(st["u"]) for st in sets]
+    lss = [torch.empty_like(st["h0"]) for st in sets]
+    cks = [torch.empty((st["u"].shape[0], (st["u"].shape[2] + 7) // 8, st["u"].shape[1], 16),
+                       device=st["u"].device, dtype=torch.float32) for st in sets]
+    got = [None, None]
+
+    def fwd(i):
+        st = sets[i]
+        ms.mamba_scan_fwd(st["u"], st["delta"], params["A"], st["B"], st["C"], params["D"], st["z"],
+                          params["delta_bias"], True, y=ys[i], last_state=lss[i], h0=st["h0"])
+
+    def fwd_train(i):
+        st = sets[i]
+        _, _, got[i] = ms.mamba_scan_fwd_train(st["u"], st["delta"], params["A"], st["B"], st["C"], params["D"],
+                                               st["z"], params["delta_bias"], True, h0=st["h0"], y=ys[i],
+                                               last_state=lss[i], ckpt=cks[i])
+
+    for i in range(2):
+        fwd_train(i)
+    torch.cuda.synchronize()
+    if got[0] is None:  # the planner split the forward pass: no checkpoints for this shape
+        return {"checkpoints": "not kept (the forward pass splits the sequence for this shape)"}
+    bwd_ck = []
+    for i, st in enumerate(sets):
+        c, _ = ms.prepare_scan_bwd(st["u"], st["delta"], params["A"], st["B"], st["C"], st["dy"], params["D"],
+                                   st["z"], params["delta_bias"], True, h0=st["h0"], dlast_state=st["dlast"],
+                                   out=out, ckpt=cks[i])
+        bwd_ck.append(c)
+    bwd_plain = []
+    for st in sets:
+        c, _ = ms.prepare_scan_bwd(st["u"], st["delta"], params["A"], st["B"], st["C"], st["dy"], params["D"],
+                                   st["z"], params["delta_bias"], True, h0=st["h0"], dlast_state=st["dlast"],
+                                   out=out)
+        bwd_plain.append(c)
+
+    def timed(fn):
+        for i in range(W):
+            fn(i % 2)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(K):
+            fn(i % 2)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / K * 1e3
+
+    us = {"fwd": timed(fwd), "bwd": timed(lambda i: bwd_plain[i]()),
+          "fwd_train": timed(fwd_train), "bwd_from_checkpoints": timed(lambda i: bwd_ck[i]())}
+    plain, ck = us["fwd"] + us["bwd"], us["fwd_train"] + us["bwd_from_checkpoints"]
+    return {"us": {k: round(v, 2) for k, v in us.items()},
+            "recompute_us": round(plain, 2), "checkpoints_us": round(ck, 2), "speedup": round(plain / ck, 4),
+            "note": "forward + backward of one step; checkpoints: the training forward pass writes the state "
+                    "before every 8-step slot and the backward pass skips its forward sweep"}
 
 
 def main():

@@ -198,6 +198,39 @@ int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, const void*
                            void* stream);
 
 /*
+ * Forward pass of training: mamba_scan_fwd_ex that also writes the state before every 8-position
+ * slot.  The hardware-aware algorithm keeps no state for the backward pass and recomputes them
+ * there (visual guide section 3.4, "recomputation"); mamba_scan_bwd does so with a forward sweep
+ * that writes exactly these one-in-eight states before its reverse sweep.  Writing them here
+ * instead (8 bytes per channel and step, while the forward kernel is bound by arithmetic, not
+ * HBM) lets mamba_scan_bwd_ckpt skip that sweep.
+ *   ckpt          [b, ceil(L/8), d, 16] fp32, 16-byte aligned, written for slots 1.. (slot 0 is
+ *                 h0); states past N are written as zero.  Must not overlap any input or output.
+ *                 dstate must be <= 16.
+ *   ckpt_written  set to 1 when ckpt was written, 0 when it was not: a sequence the library splits
+ *                 along L (few channels, long sequences) gets no checkpoints, and
+ *                 mamba_scan_bwd_ckpt then makes its own.
+ * Everything else as for mamba_scan_fwd_ex (no fused convolution).  Errors: as mamba_scan_fwd_ex.
+ */
+int mamba_scan_fwd_train(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
+                         const float* A, const void* B, const void* C, const float* D, const void* z,
+                         const float* delta_bias, int softplus_flag, const float* h0, void* y, float* last_state,
+                         float* ckpt, int* ckpt_written, void* stream);
+
+/*
+ * mamba_scan_bwd with the checkpoints of mamba_scan_fwd_train (same inputs, h0 and
+ * discretization): when ckpt is non-NULL and the backward pass runs unsplit with dstate <= 16, it
+ * skips its forward sweep and recomputes every slot from ckpt; otherwise ckpt is ignored.  ckpt
+ * (16-byte aligned; MAMBA_ERR_ARG otherwise) must not overlap a gradient output.  Everything else
+ * as for mamba_scan_bwd.
+ */
+int mamba_scan_bwd_ckpt(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
+                        const float* A, const void* B, const void* C, const float* D, const void* z,
+                        const float* delta_bias, int softplus_flag, const float* h0, const void* dy,
+                        const float* dlast_state, const float* ckpt, void* du, void* ddelta, void* dz, float* dA,
+                        float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0, void* stream);
+
+/*
  * Gradients of the forward scan (mamba_scan_fwd_state) for the loss
  *   sum(dy * y) + sum(dlast_state * last_state),
  * i.e. the backward pass of training.  The expanded states are not stored by the forward pass;

@@ -65,6 +65,10 @@ def _load() -> ctypes.CDLL:
     lib.mamba_state_step.argtypes = [ctypes.POINTER(Shape), P, P, P, P, P, P, P, P, P, I, P, P]
     lib.mamba_scan_bwd.restype = I
     lib.mamba_scan_bwd.argtypes = [ctypes.POINTER(Shape), I] + [P] * 8 + [I] + [P] * 13
+    lib.mamba_scan_fwd_train.restype = I
+    lib.mamba_scan_fwd_train.argtypes = [ctypes.POINTER(Shape), I] + [P] * 8 + [I] + [P] * 6
+    lib.mamba_scan_bwd_ckpt.restype = I
+    lib.mamba_scan_bwd_ckpt.argtypes = [ctypes.POINTER(Shape), I] + [P] * 8 + [I] + [P] * 14
     lib.mamba_scan_bwd_conv.restype = I
     lib.mamba_scan_bwd_conv.argtypes = [ctypes.POINTER(Shape), I, P, P, P, I, I, P] + [P] * 7 + [I] + [P] * 16
     lib.mamba_scan_last_error.restype = ctypes.c_char_p
@@ -83,6 +87,7 @@ _lib = _load()
 # symbols the header declares; the tests check that every one of them is exported
 EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_state", "mamba_scan_fwd_ex",
             "mamba_scan_fwd_conv", "mamba_state_step", "mamba_state_step_ex", "mamba_scan_bwd", "mamba_scan_bwd_conv",
+            "mamba_scan_fwd_train", "mamba_scan_bwd_ckpt",
             "mamba_scan_last_error", "mamba_scan_version", "mamba_scan_device_status",
             "mamba_scan_launch_count")
 MAMBA_DISC_SIMPLE, MAMBA_DISC_ZOH = 0, 1
@@ -249,6 +254,25 @@ def _scan(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want
     return y, last_state
 
 
+def mamba_scan_fwd_train(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, disc="simple",
+                         y=None, last_state=None, ckpt=None, stream=None):
+    """Forward pass of training (d_state <= 16): mamba_scan_fwd that also writes the state before
+    every 8-position slot, ckpt [b, ceil(L/8), d, 16] float32, for mamba_scan_bwd(..., ckpt=...).
+    Returns (y, last_state, ckpt), with ckpt None when the library split the sequence along L and
+    kept no checkpoints."""
+    bsz, dim, L = u.shape
+    N = A.shape[1]
+    if ckpt is None:
+        ckpt = torch.empty((bsz, (L + 7) // 8, dim, 16), device=u.device, dtype=torch.float32)
+    args, _shape, y, last_state = _scan_args(_lib.mamba_scan_fwd_ex, u, delta, A, B, C, D, z, delta_bias, softplus,
+                                             y, last_state, True, stream, h0, disc)
+    written = ctypes.c_int(0)
+    args = args[:-1] + (_ptr(ckpt, (bsz, (L + 7) // 8, dim, 16), torch.float32, "ckpt"), ctypes.byref(written),
+                        args[-1])
+    _check(_lib.mamba_scan_fwd_train(*args))
+    return y, last_state, (ckpt if written.value else None)
+
+
 def prepare_scan_fwd(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, y=None,
                      last_state=None, want_state=True, stream=None, noalloc=False, disc="simple"):
     """mamba_scan_fwd (or mamba_scan_fwd_noalloc; mamba_scan_fwd_ex for disc="zoh") with its
@@ -336,25 +360,37 @@ def _bwd_args(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0, dlast_state
 
 
 def mamba_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True, h0=None,
-                   dlast_state=None, disc="simple", stream=None, out=None):
+                   dlast_state=None, disc="simple", stream=None, out=None, ckpt=None):
     """Gradients of mamba_scan_fwd for the loss sum(dy * y) + sum(dlast_state * last_state).
-    Inputs as for mamba_scan_fwd plus dy [b, d, L] (input dtype) and dlast_state [b, d, N] float32.
+    Inputs as for mamba_scan_fwd plus dy [b, d, L] (input dtype) and dlast_state [b, d, N] float32;
+    ckpt: the checkpoints of mamba_scan_fwd_train on the same inputs, or None.
     Returns a dict: du, ddelta, dz [b, d, L] (input dtype; dz None without z), dA [d, N],
     dB, dC [b, N, L], dD, ddelta_bias [d] (None when D / delta_bias is None), dh0 [b, d, N]
     (None without h0), all float32 except du, ddelta, dz.  ``out`` may supply that dict."""
     args, _shape, out = _bwd_args(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0, dlast_state, disc,
                                   stream, out)
-    _check(_lib.mamba_scan_bwd(*args))
+    if ckpt is None:
+        _check(_lib.mamba_scan_bwd(*args))
+    else:
+        bsz, dim, L = u.shape
+        # mamba_scan_bwd_ckpt takes ckpt right after dlast_state (argument 14)
+        args = args[:14] + (_ptr(ckpt, (bsz, (L + 7) // 8, dim, 16), torch.float32, "ckpt"),) + args[14:]
+        _check(_lib.mamba_scan_bwd_ckpt(*args))
     return out
 
 
 def prepare_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True, h0=None,
-                     dlast_state=None, disc="simple", stream=None, out=None):
-    """mamba_scan_bwd with its arguments checked once.  Returns (call, out)."""
+                     dlast_state=None, disc="simple", stream=None, out=None, ckpt=None):
+    """mamba_scan_bwd (mamba_scan_bwd_ckpt with ckpt) with its arguments checked once.  Returns
+    (call, out)."""
     args, shape, out = _bwd_args(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0, dlast_state, disc,
                                  stream, out)
-    keep = (shape, u, delta, A, B, C, dy, D, z, delta_bias, h0, dlast_state, out)
-    return PreparedCall(_lib.mamba_scan_bwd, args, keep), out
+    keep = (shape, u, delta, A, B, C, dy, D, z, delta_bias, h0, dlast_state, out, ckpt)
+    if ckpt is None:
+        return PreparedCall(_lib.mamba_scan_bwd, args, keep), out
+    bsz, dim, L = u.shape
+    args = args[:14] + (_ptr(ckpt, (bsz, (L + 7) // 8, dim, 16), torch.float32, "ckpt"),) + args[14:]
+    return PreparedCall(_lib.mamba_scan_bwd_ckpt, args, keep), out
 
 
 def mamba_scan_bwd_conv(x, conv_w, conv_bias, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True,
@@ -478,24 +514,28 @@ def mamba_scan_fwd_pipelined(u, delta, A, B, C, D=None, z=None, delta_bias=None,
 
 
 class _SelectiveScan(torch.autograd.Function):
-    """The scan as an autograd operation: the forward pass is mamba_scan_fwd (or its _state / _ex
-    forms), the backward pass mamba_scan_bwd, which recomputes the states instead of keeping them
-    (only the inputs are saved)."""
+    """The scan as an autograd operation: the forward pass is mamba_scan_fwd_train (d_state <= 16:
+    it also keeps the state before every 8-position slot) or mamba_scan_fwd, the backward pass
+    mamba_scan_bwd, which recomputes the states between those checkpoints."""
 
     @staticmethod
     def forward(ctx, u, delta, A, B, C, D, z, delta_bias, h0, softplus, disc):
-        y, last_state = mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0, disc=disc)
-        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias, h0)
+        ckpt = None
+        if A.shape[1] <= 16 and u.shape[2] > 0:  # keep the checkpoints the backward pass would recompute
+            y, last_state, ckpt = mamba_scan_fwd_train(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0, disc=disc)
+        else:
+            y, last_state = mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0, disc=disc)
+        ctx.save_for_backward(u, delta, A, B, C, D, z, delta_bias, h0, ckpt)
         ctx.softplus, ctx.disc = softplus, disc
         return y, last_state
 
     @staticmethod
     def backward(ctx, dy, dlast_state):
-        u, delta, A, B, C, D, z, delta_bias, h0 = ctx.saved_tensors
+        u, delta, A, B, C, D, z, delta_bias, h0, ckpt = ctx.saved_tensors
         dy = torch.zeros_like(u) if dy is None else dy.contiguous()
         dlast_state = None if dlast_state is None else dlast_state.contiguous()
         g = mamba_scan_bwd(u, delta, A, B, C, dy, D, z, delta_bias, ctx.softplus, h0=h0, dlast_state=dlast_state,
-                           disc=ctx.disc)
+                           disc=ctx.disc, ckpt=ckpt)
         like = lambda t, ref: None if t is None else t.to(ref.dtype)  # dB, dC come as fp32
         return (g["du"], g["ddelta"], g["dA"], like(g["dB"], B), like(g["dC"], C), g["dD"], g["dz"],
                 g["ddelta_bias"], g["dh0"], None, None)

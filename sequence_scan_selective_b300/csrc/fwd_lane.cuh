@@ -129,8 +129,18 @@ static int launch_cl(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int s
                            : launch_cl_one<TIn, NP, false, LOCAL, 1>(a, maps, grid, smem_bytes, st);
         case 2: return tma ? launch_cl_one<TIn, NP, true, LOCAL, 2>(a, maps, grid, smem_bytes, st)
                            : launch_cl_one<TIn, NP, false, LOCAL, 2>(a, maps, grid, smem_bytes, st);
-        default: return tma ? launch_cl_one<TIn, NP, true, LOCAL, 3>(a, maps, grid, smem_bytes, st)
-                            : launch_cl_one<TIn, NP, false, LOCAL, 3>(a, maps, grid, smem_bytes, st);
+        case 3: return tma ? launch_cl_one<TIn, NP, true, LOCAL, 3>(a, maps, grid, smem_bytes, st)
+                           : launch_cl_one<TIn, NP, false, LOCAL, 3>(a, maps, grid, smem_bytes, st);
+        default:
+            if constexpr (!LOCAL) {  // modes 4, 5: forward pass of training (checkpoints), no convolution
+                if (mode == 4)
+                    return tma ? launch_cl_one<TIn, NP, true, false, 4>(a, maps, grid, smem_bytes, st)
+                               : launch_cl_one<TIn, NP, false, false, 4>(a, maps, grid, smem_bytes, st);
+                if (mode == 5)
+                    return tma ? launch_cl_one<TIn, NP, true, false, 5>(a, maps, grid, smem_bytes, st)
+                               : launch_cl_one<TIn, NP, false, false, 5>(a, maps, grid, smem_bytes, st);
+            }
+            return fail(MAMBA_ERR_ARG, "internal: forward mode %d", mode);
     }
 }
 
@@ -175,7 +185,11 @@ static int run(const mamba_scan_shape* s, FwdArgs a, bool softplus, float2* scra
         a.wait_ns = 1000000ull;
         a.test_stall = 1;
     }
-    const int mode = (a.zoh ? 1 : 0) | (a.conv_w != nullptr ? 2 : 0);
+    // checkpoints for the backward pass: only with an unsplit time axis and no fused convolution
+    const bool ckpt = a.ckpt != nullptr && p.nseg == 1 && a.conv_w == nullptr;
+    if (a.ck_written) *a.ck_written = ckpt ? 1 : 0;
+    if (!ckpt) a.ckpt = nullptr;
+    const int mode = (a.zoh ? 1 : 0) | (a.conv_w != nullptr ? 2 : 0) | (ckpt ? 4 : 0);
     if (p.nseg == 1) {
         const unsigned grid = (unsigned)((long long)s->batch * p.kcta);
         return launch_cl<TIn, NP, false>(a, maps, grid, p.smem_bytes, tma, mode, st);

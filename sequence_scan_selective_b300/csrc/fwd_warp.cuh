@@ -83,10 +83,10 @@ static int plan_warp(const mamba_scan_shape* s, int nsm, FwdPlan& p) {
     return MAMBA_OK;
 }
 
-template <typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE>
+template <typename TIn, int NP, bool TMA, bool AGG, bool SP, bool GATE, bool CKPT = false>
 static int launch_fwd_one(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int smem_bytes, cudaStream_t st) {
     static AttrCache attr;
-    auto kern = scan_fwd_kernel<TIn, NP, 4, TMA, AGG, SP, GATE>;
+    auto kern = scan_fwd_kernel<TIn, NP, 4, TMA, AGG, SP, GATE, CKPT>;
     int rc = allow_smem(kern, attr);
     if (rc) return rc;
     kern<<<grid, 32 * (a.wmax + 1), smem_bytes, st>>>(a, maps);
@@ -106,6 +106,20 @@ static int launch_fwd(const FwdArgs& a, const FwdMaps& maps, unsigned grid, int 
         return sp ? launch_fwd_one<TIn, NP, false, true, true, false>(a, maps, grid, smem_bytes, st)
                   : launch_fwd_one<TIn, NP, false, true, false, false>(a, maps, grid, smem_bytes, st);
     } else {
+        if constexpr (NP == 16) {
+            if (a.ckpt != nullptr) {  // forward pass of training: also the state checkpoints
+                if (tma) {
+                    if (sp) return gate ? launch_fwd_one<TIn, NP, true, false, true, true, true>(a, maps, grid, smem_bytes, st)
+                                        : launch_fwd_one<TIn, NP, true, false, true, false, true>(a, maps, grid, smem_bytes, st);
+                    return gate ? launch_fwd_one<TIn, NP, true, false, false, true, true>(a, maps, grid, smem_bytes, st)
+                                : launch_fwd_one<TIn, NP, true, false, false, false, true>(a, maps, grid, smem_bytes, st);
+                }
+                if (sp) return gate ? launch_fwd_one<TIn, NP, false, false, true, true, true>(a, maps, grid, smem_bytes, st)
+                                    : launch_fwd_one<TIn, NP, false, false, true, false, true>(a, maps, grid, smem_bytes, st);
+                return gate ? launch_fwd_one<TIn, NP, false, false, false, true, true>(a, maps, grid, smem_bytes, st)
+                            : launch_fwd_one<TIn, NP, false, false, false, false, true>(a, maps, grid, smem_bytes, st);
+            }
+        }
         if (tma) {
             if (sp) return gate ? launch_fwd_one<TIn, NP, true, false, true, true>(a, maps, grid, smem_bytes, st)
                                 : launch_fwd_one<TIn, NP, true, false, true, false>(a, maps, grid, smem_bytes, st);
@@ -138,9 +152,12 @@ static int run(const mamba_scan_shape* s, FwdArgs a, bool softplus, bool gate, f
     if (tma && !fwd_maps(maps, a, s, p, esize, TC, kUnitCh, false)) return fail(MAMBA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     fwd_apply_plan(a, p, softplus);
     if (p.nseg == 1) {
+        if (a.ck_written) *a.ck_written = (a.ckpt != nullptr && NP == 16) ? 1 : 0;
         const unsigned grid = (unsigned)((long long)s->batch * p.kcta);
         return launch_fwd<TIn, NP, false>(a, maps, grid, p.smem_bytes, tma, softplus, gate, st);
     }
+    a.ckpt = nullptr;  // checkpoints are written only with an unsplit time axis
+    if (a.ck_written) *a.ck_written = 0;
     const size_t nstate = (size_t)s->batch * s->dim * s->dstate;
     const size_t bytes = (size_t)(p.nseg - 1) * nstate * sizeof(float2);
     const bool copy_h0 = a.h0 != nullptr && overlaps(a.h0, nstate * 4, a.last_state, nstate * 4);

@@ -172,10 +172,16 @@ struct ConvSpec {
     int silu = 0;
 };
 
+struct CkptSpec {
+    float* ckpt = nullptr;     // forward pass of training: state checkpoints, or NULL
+    int* written = nullptr;    // set to 1 when they were written
+};
+
 static int scan_fwd_impl(const mamba_scan_shape* s, const void* u, const void* delta, const float* A, const void* B,
                          const void* C, const float* D, const void* z, const float* delta_bias, int softplus_flag,
                          const float* h0, void* y, float* last_state, float2* scratch, size_t scratch_cap,
-                         void* stream, int discretization = MAMBA_DISC_SIMPLE, ConvSpec conv = ConvSpec()) {
+                         void* stream, int discretization = MAMBA_DISC_SIMPLE, ConvSpec conv = ConvSpec(),
+                         CkptSpec ck = CkptSpec()) {
     t_err.clear();
     int rc = check_shape(s, true);
     if (rc) return rc;
@@ -214,7 +220,36 @@ static int scan_fwd_impl(const mamba_scan_shape* s, const void* u, const void* d
     a.zoh = discretization == MAMBA_DISC_ZOH;
     a.conv_w = conv.w; a.conv_bias = conv.bias; a.conv_prev = conv.prev;
     a.conv_k = conv.k; a.conv_silu = conv.silu;
+    a.ckpt = ck.ckpt;
+    a.ck_nslot = (int)((s->seqlen + 7) / 8);
+    a.ck_written = ck.written;
     return fwd_dispatch(s, a, softplus_flag != 0, z != nullptr, scratch, scratch_cap, st);
+}
+
+extern "C" int mamba_scan_fwd_train(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
+                                    const float* A, const void* B, const void* C, const float* D, const void* z,
+                                    const float* delta_bias, int softplus_flag, const float* h0, void* y,
+                                    float* last_state, float* ckpt, int* ckpt_written, void* stream) {
+    t_err.clear();
+    int rc = check_shape(s, true);
+    if (rc) return rc;
+    if (!ckpt || !ckpt_written) return fail(MAMBA_ERR_ARG, "ckpt and ckpt_written are required");
+    *ckpt_written = 0;
+    if (!aligned16(ckpt)) return fail(MAMBA_ERR_ARG, "ckpt must be 16-byte aligned");
+    if (s->dstate > 16) return fail(MAMBA_ERR_ARG, "checkpoints are kept for dstate <= 16");
+    const long long chans = (long long)s->batch * s->dim;
+    const size_t es = s->in_dtype == MAMBA_F32 ? 4 : 2;
+    const size_t nx = (size_t)chans * s->seqlen * es, nbc = (size_t)s->batch * s->dstate * s->seqlen * es;
+    const size_t nck = (size_t)chans * ((s->seqlen + 7) / 8) * 16 * sizeof(float);
+    if (overlaps(ckpt, nck, u, nx) || overlaps(ckpt, nck, delta, nx) || overlaps(ckpt, nck, z, nx) ||
+        overlaps(ckpt, nck, y, nx) || overlaps(ckpt, nck, B, nbc) || overlaps(ckpt, nck, C, nbc) ||
+        overlaps(ckpt, nck, last_state, (size_t)chans * s->dstate * 4) || overlaps(ckpt, nck, h0, (size_t)chans * s->dstate * 4))
+        return fail(MAMBA_ERR_ARG, "ckpt overlaps an input or an output");
+    CkptSpec ck;
+    ck.ckpt = ckpt;
+    ck.written = ckpt_written;
+    return scan_fwd_impl(s, u, delta, A, B, C, D, z, delta_bias, softplus_flag, h0, y, last_state, nullptr, 0, stream,
+                         discretization, ConvSpec(), ck);
 }
 
 extern "C" int mamba_scan_fwd(const mamba_scan_shape* s, const void* u, const void* delta, const float* A,
@@ -349,7 +384,7 @@ static int scan_bwd_impl(const mamba_scan_shape* s, int discretization, const vo
                          const float* A, const void* B, const void* C, const float* D, const void* z,
                          const float* delta_bias, int softplus_flag, const float* h0, const void* dy,
                          const float* dlast_state, void* du, void* ddelta, void* dz, float* dA, float* dB, float* dC,
-                         float* dD, float* ddelta_bias, float* dh0, void* stream) {
+                         float* dD, float* ddelta_bias, float* dh0, void* stream, const float* ckpt_in = nullptr) {
     int rc = check_shape(s, true);
     if (rc) return rc;
     if (discretization != MAMBA_DISC_SIMPLE && discretization != MAMBA_DISC_ZOH)
@@ -425,7 +460,10 @@ static int scan_bwd_impl(const mamba_scan_shape* s, int discretization, const vo
     // scratch: the state checkpoints of one block of 16 states (reused by the blocks in turn);
     // with several blocks or segments, fp32 accumulators of du, ddelta (and dz) (for fp32
     // storage the outputs themselves); with segments, their carries and local start gradients
-    const size_t nck = a.nslot > 1 ? (size_t)s->batch * a.nslot * s->dim * bwd::kNS * sizeof(float) : 0;
+    // checkpoints from the forward pass of training replace the forward sweep (unsplit, N <= 16)
+    const bool use_ck = ckpt_in != nullptr && a.nseg == 1 && N <= bwd::kNS && a.nslot > 1;
+    a.ck_given = use_ck ? 1 : 0;
+    const size_t nck = (a.nslot > 1 && !use_ck) ? (size_t)s->batch * a.nslot * s->dim * bwd::kNS * sizeof(float) : 0;
     const bool accumulate = N > bwd::kNS || a.nseg > 1;
     const size_t nacc = accumulate && s->in_dtype == MAMBA_BF16 ? (size_t)chans * L * sizeof(float) : 0;
     const int nacc_t = dz ? 3 : 2;
@@ -436,7 +474,7 @@ static int scan_bwd_impl(const mamba_scan_shape* s, int discretization, const vo
         e = cudaMallocAsync(reinterpret_cast<void**>(&scratch), nck + nacc * nacc_t + nseg_b, st);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(state checkpoints)");
     }
-    a.ckpt = nck ? reinterpret_cast<float*>(scratch) : nullptr;
+    a.ckpt = use_ck ? const_cast<float*>(ckpt_in) : nck ? reinterpret_cast<float*>(scratch) : nullptr;
     if (nacc) {
         a.acc_du = reinterpret_cast<float*>(scratch + nck);
         a.acc_dd = reinterpret_cast<float*>(scratch + nck + nacc);
@@ -467,6 +505,27 @@ extern "C" int mamba_scan_bwd(const mamba_scan_shape* s, int discretization, con
     t_err.clear();
     return scan_bwd_impl(s, discretization, u, delta, A, B, C, D, z, delta_bias, softplus_flag, h0, dy, dlast_state,
                          du, ddelta, dz, dA, dB, dC, dD, ddelta_bias, dh0, stream);
+}
+
+extern "C" int mamba_scan_bwd_ckpt(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
+                                   const float* A, const void* B, const void* C, const float* D, const void* z,
+                                   const float* delta_bias, int softplus_flag, const float* h0, const void* dy,
+                                   const float* dlast_state, const float* ckpt, void* du, void* ddelta, void* dz,
+                                   float* dA, float* dB, float* dC, float* dD, float* ddelta_bias, float* dh0,
+                                   void* stream) {
+    t_err.clear();
+    if (ckpt && !aligned16(ckpt)) return fail(MAMBA_ERR_ARG, "ckpt must be 16-byte aligned");
+    if (s && ckpt && s->seqlen > 0) {
+        const long long chans = (long long)s->batch * s->dim;
+        const size_t es = s->in_dtype == MAMBA_F32 ? 4 : 2;
+        const size_t nx = (size_t)chans * s->seqlen * es, nbc4 = (size_t)s->batch * s->dstate * s->seqlen * 4;
+        const size_t nck = (size_t)chans * ((s->seqlen + 7) / 8) * 16 * sizeof(float);
+        if (overlaps(ckpt, nck, du, nx) || overlaps(ckpt, nck, ddelta, nx) || overlaps(ckpt, nck, dz, nx) ||
+            overlaps(ckpt, nck, dB, nbc4) || overlaps(ckpt, nck, dC, nbc4))
+            return fail(MAMBA_ERR_ARG, "ckpt overlaps a gradient output");
+    }
+    return scan_bwd_impl(s, discretization, u, delta, A, B, C, D, z, delta_bias, softplus_flag, h0, dy, dlast_state,
+                         du, ddelta, dz, dA, dB, dC, dD, ddelta_bias, dh0, stream, ckpt);
 }
 
 extern "C" int mamba_scan_bwd_conv(const mamba_scan_shape* s, int discretization, const void* x, const float* conv_w,

@@ -77,6 +77,9 @@ struct BwdArgs {
     int nseg, seg_tiles;
     float2* carry;
     float* mu_local;
+    // nonzero: ckpt holds the forward pass's checkpoints already (unsplit, N <= 16), so the full
+    // launch skips its forward sweep
+    int ck_given;
 };
 
 namespace bwd {
@@ -412,7 +415,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
     };
 
     // ---------------------------------------------------------------- forward sweep: checkpoints
-    if (MODE == kCarry || (MODE == kFull && a.nslot > 1)) {
+    if (MODE == kCarry || (MODE == kFull && a.nslot > 1 && !a.ck_given)) {
         float2 h[2] = {make_float2(h0v[0], h0v[1]), make_float2(h0v[2], h0v[3])};
         float sumdt = 0.f;  // carry launch: sum of Delta over the segment
         if (VEC) load_tile<TIn, VEC>(smem + (k_begin & 1) * Lt::STAGE, a, b, d0, k_begin, false);

@@ -107,6 +107,12 @@ struct FwdArgs {
     // arrives on, so every bounded wait of the launch runs out and the status word is set.
     int test_stall;
     int softplus;  // channel-per-lane kernel: Delta = softplus(delta + bias) (else delta + bias)
+    // Forward pass of training (unsplit time axis only): the state before every 8-step slot
+    // s >= 1, ckpt [batch][ck_nslot][dim][16] fp32 (states past N written as zero), the layout
+    // the backward pass recomputes from; NULL: not written.
+    float* ckpt;
+    int ck_nslot;      // ceil(L / 8)
+    int* ck_written;   // host side: set to 1 when the launch wrote the checkpoints, else 0
 };
 
 // u, delta, z maps: [0] box of wlo units' rows, [1] of (wlo+1) units' rows; B, C: box [N, TC].
@@ -149,7 +155,7 @@ __device__ __forceinline__ void store4<uint16_t>(uint16_t* p, const float* v) {
     *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
 }
 
-template <typename TIn, int NP, int LPC, bool TMA, bool AGG, bool SOFTPLUS, bool GATE>
+template <typename TIn, int NP, int LPC, bool TMA, bool AGG, bool SOFTPLUS, bool GATE, bool CKPT = false>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     scan_fwd_kernel(const FwdArgs a, const __grid_constant__ FwdMaps maps) {
     using LY = Layout<LPC>;
@@ -300,6 +306,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     const bool zoh = a.zoh != 0;
     float2 A2[G / 2], invA[G / 2];
     float2 h[G / 2];
+    static_assert(!CKPT || (G == 4 && kSlot == 16 && !AGG), "checkpoints: N <= 16 (four states per lane), unsplit");
     const float* h0 = (!AGG && cvalid && a.h0 != nullptr) ? a.h0 + row * N : nullptr;
 #pragma unroll
     for (int p = 0; p < G / 2; ++p) {
@@ -462,6 +469,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         }
     };
 
+    // Forward pass of training: the lane's G states after step tt - 1 of the sequence, i.e. the
+    // state before 8-step slot tt / 8, into the checkpoints (G = 4: one 16-byte store)
+    auto store_ckpt = [&](long long tt) {
+        const long long sl8 = tt / 8;
+        if (cvalid && sl8 < a.ck_nslot)
+            *reinterpret_cast<float4*>(a.ckpt + ((b * (long long)a.ck_nslot + sl8) * a.dim + dch) * 16 + g * G) =
+                make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+    };
+
     // Phase B of slot i: advance the lane's G states through the slot's 16 steps; yp[t] is the
     // lane's share of C.h at step t.
     auto phase_b = [&](int i, float* yp) {
@@ -486,6 +502,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 if (!AGG) ya = p == 0 ? fmul2(make_float2(w.z, w.w), h[p]) : ffma2(make_float2(w.z, w.w), h[p], ya);
             }
             if (!AGG) yp[t] = ya.x + ya.y;
+            if constexpr (CKPT) {
+                if (t == 7 || t == kSlot - 1) store_ckpt(t_begin + (long long)i * kSlot + t + 1);
+            }
         }
     };
 
@@ -519,6 +538,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 if (!AGG) ya = p == 0 ? fmul2(make_float2(w.z, w.w), h[p]) : ffma2(make_float2(w.z, w.w), h[p], ya);
             }
             if (!AGG) yp[t] = ya.x + ya.y;
+            if constexpr (CKPT) {
+                if (t == 7 || t == kSlot - 1) store_ckpt(t_begin + (long long)i * kSlot + t + 1);
+            }
         }
     };
 

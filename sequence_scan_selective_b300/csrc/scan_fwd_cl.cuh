@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(32 * (cl::Lanes::MAX_WARPS + 1), 1)
     constexpr int TILE = CPW * cl::kRowBytes;  // one warp's rows of one input tile
     constexpr bool ZOH = (MODE & 1) != 0;
     constexpr bool CONV = (MODE & 2) != 0;
+    constexpr bool CKPT = (MODE & 4) != 0;  // forward pass of training: state checkpoints
+    static_assert(!CKPT || (!LOCAL && !CONV), "checkpoints: unsplit time axis, no fused convolution");
     const bool has_z = a.z != nullptr;
     const bool softplus = a.softplus != 0;
     static_assert(NP % 2 == 0 && NP <= 16, "shape");
@@ -420,6 +422,22 @@ __global__ void __launch_bounds__(32 * (cl::Lanes::MAX_WARPS + 1), 1)
             Elem e;
             elem(blk, e);
             recur(blk, e);
+            if constexpr (CKPT) {
+                // after every 8 steps: the state before the next 8-step slot, all 16 positions
+                // (those past NP as zero), in the backward pass's checkpoint layout
+                const long long tt = tc0 + (long long)(blk + 1) * BLK;
+                const long long sl8 = tt / 8;
+                if ((((blk + 1) * BLK) % 8) == 0 && cvalid && sl8 < a.ck_nslot) {
+                    float4* dst = reinterpret_cast<float4*>(a.ckpt + ((b * (long long)a.ck_nslot + sl8) * a.dim + dch) * 16);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        constexpr int last = PL - 1;
+                        const int p0 = 2 * q4 < last ? 2 * q4 : last, p1 = 2 * q4 + 1 < last ? 2 * q4 + 1 : last;
+                        dst[q4] = 2 * q4 + 1 < PL ? make_float4(h[p0].x, h[p0].y, h[p1].x, h[p1].y)
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+            }
         }
         __syncwarp();
         mbar_arrive(&empty[s]);

@@ -185,3 +185,27 @@ def test_block_bwd_host_argument_checks(ms):
     assert lib.mamba_scan_bwd_conv(*args(_shape(ms), k=0)) == -1
     assert lib.mamba_scan_bwd_conv(*args(_shape(ms, dstate=65))) == -1
     assert lib.mamba_scan_bwd_conv(*args(_shape(ms, seqlen=-1))) == -1
+
+
+def test_train_checkpoint_host_argument_checks(ms):
+    lib = ms.lib()
+    P = ctypes.c_void_p
+    d = P(256)  # never dereferenced: every case below fails validation first
+    written = ctypes.c_int(7)
+    fwd = lambda s, ck, y=P(1 << 40): lib.mamba_scan_fwd_train(ctypes.byref(s), 0, d, d, d, d, d, None, None, None,
+                                                               1, None, y, None, ck, ctypes.byref(written), None)
+    assert fwd(_shape(ms), None) == -1
+    assert b"ckpt" in lib.mamba_scan_last_error() and written.value == 7  # no output pointer: nothing written
+    assert fwd(_shape(ms, dstate=17), P(1 << 41)) == -1
+    assert b"dstate" in lib.mamba_scan_last_error() and written.value == 0
+    assert fwd(_shape(ms), P((1 << 41) + 4)) == -1
+    assert b"aligned" in lib.mamba_scan_last_error()
+    assert fwd(_shape(ms), P(1 << 41), y=P((1 << 41) + 64)) == -1  # ckpt overlapping y
+    assert b"overlap" in lib.mamba_scan_last_error()
+    bwd = lambda s, ck, du=d: lib.mamba_scan_bwd_ckpt(ctypes.byref(s), 0, d, d, d, d, d, None, None, None, 1, None,
+                                                      d, None, ck, du, d, None, d, d, d, None, None, None, None)
+    assert bwd(_shape(ms), P((1 << 41) + 8)) == -1
+    assert b"aligned" in lib.mamba_scan_last_error()
+    assert bwd(_shape(ms), P(1 << 41), du=P((1 << 41) + 32)) == -1
+    assert b"overlap" in lib.mamba_scan_last_error()
+    assert bwd(_shape(ms, dstate=65), P(1 << 41)) == -1

@@ -21,8 +21,14 @@ def ms_fake(monkeypatch):
                             h0=None if h0 is None else n(h0).astype(np.float64), disc=disc)
         return torch.from_numpy(y.astype(np.float32)), torch.from_numpy(st.astype(np.float32))
 
+    def fwd_train(*args, **kw):  # the training forward pass: also a checkpoint tensor for the backward pass
+        y, st = fwd(*args, **kw)
+        calls["ckpt"] = torch.zeros(1)
+        return y, st, calls["ckpt"]
+
     def bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus=True, h0=None, dlast_state=None,
-            disc="simple", **_):
+            disc="simple", ckpt=None, **_):
+        calls["bwd_ckpt"] = ckpt
         n = lambda t: None if t is None else t.detach().numpy()
         g = oracle.scan_bwd(n(u), n(delta), n(A), n(B), n(C), n(dy).astype(np.float64), n(D), n(z), n(delta_bias),
                             softplus, "f32", h0=None if h0 is None else n(h0).astype(np.float64),
@@ -39,6 +45,7 @@ def ms_fake(monkeypatch):
         return out
 
     monkeypatch.setattr(ms, "mamba_scan_fwd", fwd)
+    monkeypatch.setattr(ms, "mamba_scan_fwd_train", fwd_train)
     monkeypatch.setattr(ms, "mamba_scan_bwd", bwd)
     return ms, calls
 
@@ -67,3 +74,5 @@ def test_gradients_reach_their_inputs(ms_fake, drop):
         assert t[k].grad is not None, k
         assert t[k].grad.dtype == t[k].dtype and t[k].grad.shape == t[k].shape, k
         assert torch.equal(t[k].grad, g[gk]), k
+    # d_state <= 16: the training forward pass's checkpoints reach the backward pass
+    assert calls["bwd_ckpt"] is calls["ckpt"]

@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--settle-ms", type=float, default=300.0,
+                    help="after the warm-up steps, further untimed steps until this much device time has "
+                         "passed, so that the timed region does not measure the clocks' ramp from idle")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="b14")
     ap.add_argument("--no-long", action="store_true",
@@ -323,6 +326,25 @@ DEC_KEYS = ("x", "delta", "z", "B", "C")
 
 
 # ------------------------------------------------------------------------------------ our arm
+def settle_clocks(run, stream, min_ms: float):
+    """Untimed iterations after the warm-up steps until `min_ms` of device time has passed: a GPU
+    that was idle raises its clocks over its first milliseconds of work, so a timed region of a few
+    milliseconds that starts right after a handful of warm-up steps measures part of that ramp.
+    run(i) enqueues iteration i.  Returns {"steps": n, "device_ms": t}."""
+    import torch
+    n, spent = 0, 0.0
+    while spent < min_ms and n < 1000000:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(8):
+            run(n)
+            n += 1
+        b.record(stream)
+        b.synchronize()
+        spent += a.elapsed_time(b)
+    return {"steps": n, "device_ms": round(spent, 1)}
+
+
 def run_ours(args, cfg, rank, world, local_rank):
     import torch
     import sequence_scan_selective_b300 as ms
@@ -370,6 +392,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     W = max(args.warmup, 3)
     for i in range(W):
         step(i)
+    settle = settle_clocks(lambda i: step(W + i), stream, args.settle_ms)
     torch.cuda.synchronize()
     ms.device_status()
 
@@ -414,7 +437,8 @@ def run_ours(args, cfg, rank, world, local_rank):
                 "algorithmic_bytes_per_launch": sb, "kernel_avg_us": round(scan_avg_ms * 1e3, 2)}
     line = {
         "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "clock_settle": settle, "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded, recipe of the workload)",
         "config": {"workload": WORKLOADS[args.workload], "batch": cfg.batch, "d_inner": cfg.dim,
                    "d_state": cfg.dstate, "seq_len": cfg.seqlen, "storage": cfg.dtype,
@@ -787,6 +811,7 @@ def run_decode(args, cfg, rank, world, local_rank):
     W = max(args.warmup, 3)
     for i in range(W):
         calls[i % S]()
+    settle = settle_clocks(lambda i: calls[(W + i) % S](), stream, args.settle_ms)
     torch.cuda.synchronize()
     K = args.steps
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -854,7 +879,8 @@ def run_decode(args, cfg, rank, world, local_rank):
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     line = {
         "metric": METRIC, "value": whole_job_rate(elems_step, K, world, total_ms), "unit": "elements/s",
-        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "n_gpus": world, "steps": K, "warmup": W, "clock_settle": settle, "ms_per_step": total_ms / K,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, recipe of the workload)",
         "config": {"workload": WORKLOADS["decode"], "batch": cfg.batch, "d_inner": cfg.dim, "d_state": cfg.dstate,
                    "storage": cfg.dtype, "step": "one decode step (state update in place), fresh inputs per step",
@@ -921,6 +947,7 @@ def run_bwd(args, cfg, rank, world, local_rank):
     W = max(args.warmup, 3)
     for i in range(W):
         calls[i % 2]()
+    settle = settle_clocks(lambda i: calls[(W + i) % 2](), stream, args.settle_ms)
     torch.cuda.synchronize()
     K = args.steps
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -951,7 +978,8 @@ def run_bwd(args, cfg, rank, world, local_rank):
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     line = {
         "metric": METRIC, "value": whole_job_rate(elems_step, K, world, total_ms), "unit": "elements/s",
-        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "n_gpus": world, "steps": K, "warmup": W, "clock_settle": settle, "ms_per_step": total_ms / K,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, recipe of the workload)",
         "config": {"workload": WORKLOADS[args.workload].replace("scan+decode", "backward pass"),
                    "batch": cfg.batch, "d_inner": cfg.dim, "d_state": cfg.dstate, "seq_len": cfg.seqlen,

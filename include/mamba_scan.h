@@ -28,6 +28,8 @@
 #ifndef MAMBA_SCAN_H
 #define MAMBA_SCAN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -209,13 +211,24 @@ int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, const void*
  *                 dstate must be <= 16.
  *   ckpt_written  set to 1 when ckpt was written, 0 when it was not: a sequence the library splits
  *                 along L (few channels, long sequences) gets no checkpoints, and
- *                 mamba_scan_bwd_ckpt then makes its own.
+ *                 mamba_scan_bwd_ckpt then makes its own.  mamba_scan_fwd_train_ckpt_bytes
+ *                 tells beforehand (0 bytes: none).
  * Everything else as for mamba_scan_fwd_ex (no fused convolution).  Errors: as mamba_scan_fwd_ex.
  */
 int mamba_scan_fwd_train(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
                          const float* A, const void* B, const void* C, const float* D, const void* z,
                          const float* delta_bias, int softplus_flag, const float* h0, void* y, float* last_state,
                          float* ckpt, int* ckpt_written, void* stream);
+
+/*
+ * Size in bytes of the checkpoints that mamba_scan_fwd_train writes for shape s on the current
+ * device: b * ceil(L/8) * d * 16 * 4, or 0 when it would write none (dstate > 16, L = 0, or a
+ * sequence the library splits along L).  Host-side only: no allocation and no launch.  The
+ * answer holds while the device and the MAMBA_SCAN_* environment variables stay the same.
+ *   bytes   written.
+ * Errors: MAMBA_ERR_ARG (NULL pointer, bad shape).
+ */
+int mamba_scan_fwd_train_ckpt_bytes(const mamba_scan_shape* s, size_t* bytes);
 
 /*
  * mamba_scan_bwd with the checkpoints of mamba_scan_fwd_train (same inputs, h0 and

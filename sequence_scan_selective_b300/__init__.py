@@ -17,6 +17,7 @@ Entry points (names as in include/mamba_scan.h):
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -67,6 +68,8 @@ def _load() -> ctypes.CDLL:
     lib.mamba_scan_bwd.argtypes = [ctypes.POINTER(Shape), I] + [P] * 8 + [I] + [P] * 13
     lib.mamba_scan_fwd_train.restype = I
     lib.mamba_scan_fwd_train.argtypes = [ctypes.POINTER(Shape), I] + [P] * 8 + [I] + [P] * 6
+    lib.mamba_scan_fwd_train_ckpt_bytes.restype = I
+    lib.mamba_scan_fwd_train_ckpt_bytes.argtypes = [ctypes.POINTER(Shape), ctypes.POINTER(ctypes.c_size_t)]
     lib.mamba_scan_bwd_ckpt.restype = I
     lib.mamba_scan_bwd_ckpt.argtypes = [ctypes.POINTER(Shape), I] + [P] * 8 + [I] + [P] * 14
     lib.mamba_scan_bwd_conv.restype = I
@@ -87,7 +90,7 @@ _lib = _load()
 # symbols the header declares; the tests check that every one of them is exported
 EXPORTED = ("mamba_scan_fwd", "mamba_scan_fwd_noalloc", "mamba_scan_fwd_state", "mamba_scan_fwd_ex",
             "mamba_scan_fwd_conv", "mamba_state_step", "mamba_state_step_ex", "mamba_scan_bwd", "mamba_scan_bwd_conv",
-            "mamba_scan_fwd_train", "mamba_scan_bwd_ckpt",
+            "mamba_scan_fwd_train", "mamba_scan_bwd_ckpt", "mamba_scan_fwd_train_ckpt_bytes",
             "mamba_scan_last_error", "mamba_scan_version", "mamba_scan_device_status",
             "mamba_scan_launch_count")
 MAMBA_DISC_SIMPLE, MAMBA_DISC_ZOH = 0, 1
@@ -254,15 +257,30 @@ def _scan(fn, u, delta, A, B, C, D, z, delta_bias, softplus, y, last_state, want
     return y, last_state
 
 
+def train_checkpoint_bytes(u, A) -> int:
+    """Bytes of the checkpoints mamba_scan_fwd_train keeps for u [b, d, L] and A [d, N] on the
+    current device: 8 per (batch row, channel, step), or 0 when it keeps none."""
+    bsz, dim, L = u.shape
+    nbytes = ctypes.c_size_t(0)
+    with (torch.cuda.device(u.device) if u.is_cuda else contextlib.nullcontext()):
+        _check(_lib.mamba_scan_fwd_train_ckpt_bytes(ctypes.byref(Shape(bsz, dim, A.shape[1], L, _dtype_code(u))),
+                                                    ctypes.byref(nbytes)))
+    return nbytes.value
+
+
 def mamba_scan_fwd_train(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, disc="simple",
                          y=None, last_state=None, ckpt=None, stream=None):
     """Forward pass of training (d_state <= 16): mamba_scan_fwd that also writes the state before
     every 8-position slot, ckpt [b, ceil(L/8), d, 16] float32, for mamba_scan_bwd(..., ckpt=...).
-    Returns (y, last_state, ckpt), with ckpt None when the library split the sequence along L and
-    kept no checkpoints."""
+    Returns (y, last_state, ckpt), with ckpt None when the library splits the sequence along L and
+    keeps no checkpoints (then no buffer is allocated for them)."""
     bsz, dim, L = u.shape
     N = A.shape[1]
     if ckpt is None:
+        if train_checkpoint_bytes(u, A) == 0:
+            y, last_state = _scan(_lib.mamba_scan_fwd_ex, u, delta, A, B, C, D, z, delta_bias, softplus, y,
+                                  last_state, True, stream, h0, disc)
+            return y, last_state, None
         ckpt = torch.empty((bsz, (L + 7) // 8, dim, 16), device=u.device, dtype=torch.float32)
     args, _shape, y, last_state = _scan_args(_lib.mamba_scan_fwd_ex, u, delta, A, B, C, D, z, delta_bias, softplus,
                                              y, last_state, True, stream, h0, disc)
@@ -519,9 +537,9 @@ class _SelectiveScan(torch.autograd.Function):
     mamba_scan_bwd, which recomputes the states between those checkpoints."""
 
     @staticmethod
-    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, h0, softplus, disc):
+    def forward(ctx, u, delta, A, B, C, D, z, delta_bias, h0, softplus, disc, checkpoints):
         ckpt = None
-        if A.shape[1] <= 16 and u.shape[2] > 0:  # keep the checkpoints the backward pass would recompute
+        if checkpoints and A.shape[1] <= 16 and u.shape[2] > 0:  # keep what the backward pass would recompute
             y, last_state, ckpt = mamba_scan_fwd_train(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0, disc=disc)
         else:
             y, last_state = mamba_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus, h0=h0, disc=disc)
@@ -538,13 +556,17 @@ class _SelectiveScan(torch.autograd.Function):
                            disc=ctx.disc, ckpt=ckpt)
         like = lambda t, ref: None if t is None else t.to(ref.dtype)  # dB, dC come as fp32
         return (g["du"], g["ddelta"], g["dA"], like(g["dB"], B), like(g["dC"], C), g["dD"], g["dz"],
-                g["ddelta_bias"], g["dh0"], None, None)
+                g["ddelta_bias"], g["dh0"], None, None, None)
 
 
-def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, disc="simple"):
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True, h0=None, disc="simple",
+                   checkpoints=True):
     """(y, last_state) of the scan, differentiable with respect to u, delta, A, B, C, D, z,
-    delta_bias and h0 (backward pass: mamba_scan_bwd).  Arguments as for mamba_scan_fwd."""
-    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, h0, bool(softplus), disc)
+    delta_bias and h0 (backward pass: mamba_scan_bwd).  Arguments as for mamba_scan_fwd.
+    checkpoints: for d_state <= 16, the forward pass keeps the state before every 8-step slot for
+    the backward pass (8 bytes per batch row, channel and step, held until the backward pass);
+    False recomputes them there instead (slower step, no extra memory)."""
+    return _SelectiveScan.apply(u, delta, A, B, C, D, z, delta_bias, h0, bool(softplus), disc, bool(checkpoints))
 
 
 class _SelectiveScanConv(torch.autograd.Function):

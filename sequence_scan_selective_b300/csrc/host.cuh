@@ -87,6 +87,12 @@ int fwd_lane_run_t(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, f
 template <typename TIn>
 int fwd_warp_run_t(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, bool gate, float2* scratch,
                    size_t cap, cudaStream_t st);
+// Segments of the time axis that the forward planner of each kernel picks for a shape (negative:
+// an error code).  Host-only: no launch, no allocation.
+template <typename TIn>
+int fwd_lane_nseg_t(const mamba_scan_shape* s);
+template <typename TIn>
+int fwd_warp_nseg_t(const mamba_scan_shape* s);
 template <typename TIn>
 int fwd_lane_status_t(bool clear);
 template <typename TIn>

@@ -130,16 +130,23 @@ static bool prefer_lane_kernel(const mamba_scan_shape* s, int nsm) {
 
 // The channel-per-lane kernel for N <= 16 where it fills the GPU (prefer_lane_kernel),
 // scan_fwd_kernel otherwise.  MAMBA_SCAN_KERNEL=warp or =lane forces one (tests, benchmarks).
-static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, bool gate, float2* scratch,
-                        size_t scratch_cap, cudaStream_t st) {
+static int choose_lane_kernel(const mamba_scan_shape* s, bool* use_lane) {
     const char* force = getenv("MAMBA_SCAN_KERNEL");
     const bool lane_ok = s->dstate <= 16;
-    bool use_lane = lane_ok && prefer_lane_kernel(s, sm_count());
-    if (force && strcmp(force, "warp") == 0) use_lane = false;
+    *use_lane = lane_ok && prefer_lane_kernel(s, sm_count());
+    if (force && strcmp(force, "warp") == 0) *use_lane = false;
     if (force && strcmp(force, "lane") == 0) {
         if (!lane_ok) return fail(MAMBA_ERR_ARG, "MAMBA_SCAN_KERNEL=lane: the channel-per-lane kernel takes N <= 16");
-        use_lane = true;
+        *use_lane = true;
     }
+    return MAMBA_OK;
+}
+
+static int fwd_dispatch(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, bool gate, float2* scratch,
+                        size_t scratch_cap, cudaStream_t st) {
+    bool use_lane = false;
+    const int rc = choose_lane_kernel(s, &use_lane);
+    if (rc) return rc;
     const bool bf = s->in_dtype == MAMBA_BF16;
     if (use_lane)
         return bf ? fwd_lane_run_t<uint16_t>(s, a, softplus, scratch, scratch_cap, st)
@@ -224,6 +231,24 @@ static int scan_fwd_impl(const mamba_scan_shape* s, const void* u, const void* d
     a.ck_nslot = (int)((s->seqlen + 7) / 8);
     a.ck_written = ck.written;
     return fwd_dispatch(s, a, softplus_flag != 0, z != nullptr, scratch, scratch_cap, st);
+}
+
+extern "C" int mamba_scan_fwd_train_ckpt_bytes(const mamba_scan_shape* s, size_t* bytes) {
+    t_err.clear();
+    if (!bytes) return fail(MAMBA_ERR_ARG, "bytes is NULL");
+    *bytes = 0;
+    int rc = check_shape(s, true);
+    if (rc) return rc;
+    if (s->dstate > 16 || s->seqlen == 0) return MAMBA_OK;
+    bool lane = false;
+    rc = choose_lane_kernel(s, &lane);
+    if (rc) return rc;
+    const bool bf = s->in_dtype == MAMBA_BF16;
+    const int nseg = lane ? (bf ? fwd_lane_nseg_t<uint16_t>(s) : fwd_lane_nseg_t<float>(s))
+                          : (bf ? fwd_warp_nseg_t<uint16_t>(s) : fwd_warp_nseg_t<float>(s));
+    if (nseg < 0) return nseg;
+    if (nseg == 1) *bytes = (size_t)s->batch * (size_t)((s->seqlen + 7) / 8) * s->dim * 16 * sizeof(float);
+    return MAMBA_OK;
 }
 
 extern "C" int mamba_scan_fwd_train(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,

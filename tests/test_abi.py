@@ -209,3 +209,21 @@ def test_train_checkpoint_host_argument_checks(ms):
     assert bwd(_shape(ms), P(1 << 41), du=P((1 << 41) + 32)) == -1
     assert b"overlap" in lib.mamba_scan_last_error()
     assert bwd(_shape(ms, dstate=65), P(1 << 41)) == -1
+
+
+def test_train_checkpoint_bytes_host_query(ms, monkeypatch):
+    """The size query runs the forward planners on the host (148 SMs when no device answers):
+    checkpoints for the layer shapes, none for the million-token shape (split along L), none for
+    N > 16 or L = 0."""
+    lib = ms.lib()
+    q = lambda **kw: (lambda n: (lib.mamba_scan_fwd_train_ckpt_bytes(ctypes.byref(_shape(ms, **kw)),
+                                                                     ctypes.byref(n)), n.value))(ctypes.c_size_t(9))
+    assert lib.mamba_scan_fwd_train_ckpt_bytes(ctypes.byref(_shape(ms)), None) == -1
+    assert q(batch=4, dim=4096, dstate=16, seqlen=2048, in_dtype=1) == (0, 4 * 256 * 4096 * 64)
+    assert q(batch=8, dim=1536, dstate=16, seqlen=2048) == (0, 8 * 256 * 1536 * 64)
+    assert q(batch=1, dim=1536, dstate=16, seqlen=1 << 20) == (0, 0)
+    assert q(batch=2, dim=64, dstate=17, seqlen=100) == (0, 0)
+    assert q(batch=2, dim=64, dstate=16, seqlen=0) == (0, 0)
+    assert q(batch=2, dim=64, dstate=16, seqlen=-1)[0] == -1
+    monkeypatch.setenv("MAMBA_SCAN_NSEG", "1")  # read by the planners at every call
+    assert q(batch=1, dim=1536, dstate=16, seqlen=1 << 20) == (0, 1536 * (1 << 17) * 64)

@@ -125,9 +125,40 @@ def test_train_split_forward_keeps_no_checkpoints(ms, kernel):
     cfg = synth.CONFIGS["m130"].replace(batch=1, dim=32, dstate=16, seqlen=4096, seed=330)
     inp = _inputs(cfg)
     with _env(MAMBA_SCAN_KERNEL=kernel, MAMBA_SCAN_NSEG="3"):
-        _d, _h0, (y0, st0), (y, st, ck) = _train(ms, inp, cfg.dtype, "simple")
-    assert ck is None
-    assert torch.equal(y, y0) and torch.equal(st, st0)
+        d, h0, (y0, st0), (y, st, ck) = _train(ms, inp, cfg.dtype, "simple")
+        assert ms.train_checkpoint_bytes(d["u"], d["A"]) == 0
+        assert ck is None
+        assert torch.equal(y, y0) and torch.equal(st, st0)
+        # with a buffer given, the library itself reports that it wrote nothing
+        buf = torch.full((1, 512, 32, 16), 7.0, device="cuda")
+        y2, st2, ck2 = ms.mamba_scan_fwd_train(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                               d["delta_bias"], True, h0=h0, ckpt=buf)
+        torch.cuda.synchronize()
+        assert ck2 is None and torch.equal(y2, y0) and torch.equal(st2, st0)
+        assert bool(torch.all(buf == 7.0)), "a split forward pass wrote checkpoints"
+
+
+@pytest.mark.parametrize("kernel", ["lane", "warp"])
+@pytest.mark.parametrize("nseg", ["1", "2", ""])
+def test_train_checkpoint_bytes_matches_what_is_written(ms, kernel, nseg):
+    """The size query and the forward pass agree on whether checkpoints are kept, with the
+    library's own plan ("") and forced segment counts."""
+    cfg = synth.CONFIGS["m130"].replace(batch=1, dim=64, dstate=16, seqlen=4096, seed=360)
+    inp = _inputs(cfg)
+    d = dev_inputs(inp, cfg.dtype)
+    env = {"MAMBA_SCAN_KERNEL": kernel}
+    if nseg:
+        env["MAMBA_SCAN_NSEG"] = nseg
+    with _env(**env):
+        nbytes = ms.train_checkpoint_bytes(d["u"], d["A"])
+        buf = torch.empty((1, 512, 64, 16), device="cuda")
+        _y, _st, ck = ms.mamba_scan_fwd_train(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                              d["delta_bias"], True, ckpt=buf)
+        torch.cuda.synchronize()
+    assert (ck is not None) == (nbytes > 0)
+    assert nbytes in (0, buf.numel() * 4)
+    if nseg == "1":
+        assert nbytes == buf.numel() * 4
 
 
 def test_train_checkpoints_ignored_by_a_split_backward(ms):
@@ -139,12 +170,21 @@ def test_train_checkpoints_ignored_by_a_split_backward(ms):
         _bwd_check(ms, inp, d, h0, cfg.dtype, "simple", ck)
 
 
-def test_train_wide_state_is_refused(ms):
+def test_train_wide_state_keeps_no_checkpoints(ms):
+    """N > 16: the binding runs the plain forward pass and returns no checkpoints; the library
+    itself refuses a checkpoint buffer for that shape."""
     cfg = synth.CONFIGS["m130"].replace(batch=1, dim=8, dstate=17, seqlen=16, seed=350)
     inp = _inputs(cfg)
     d = dev_inputs(inp, cfg.dtype)
+    assert ms.train_checkpoint_bytes(d["u"], d["A"]) == 0
+    y, st, ck = ms.mamba_scan_fwd_train(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                        d["delta_bias"])
+    y0, st0 = ms.mamba_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"])
+    torch.cuda.synchronize()
+    assert ck is None and torch.equal(y, y0) and torch.equal(st, st0)
     with pytest.raises(RuntimeError, match="dstate"):
-        ms.mamba_scan_fwd_train(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"])
+        ms.mamba_scan_fwd_train(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["delta_bias"],
+                                ckpt=torch.empty((1, 2, 8, 16), device="cuda"))
 
 
 def test_train_full_size_sampled(ms):

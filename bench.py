@@ -950,6 +950,8 @@ def run_bwd(args, cfg, rank, world, local_rank):
     settle = settle_clocks(lambda i: calls[(W + i) % 2](), stream, args.settle_ms)
     torch.cuda.synchronize()
     K = args.steps
+    # events around each call as well: the kernel time excludes any gap the host leaves between calls
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
@@ -959,13 +961,16 @@ def run_bwd(args, cfg, rank, world, local_rank):
         clk.mark(True)
         t_start.record(stream)
         for i in range(K):
+            evs[i][0].record(stream)
             calls[i % 2]()
+            evs[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         clk.mark(False)
     launches = ms.launch_count() - n0
     total_ms = t_start.elapsed_time(t_end)
-    total_ms, avg_ms, launches = aggregate_ranks(dist, dev, total_ms, total_ms / K, launches)
+    call_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    total_ms, avg_ms, launches = aggregate_ranks(dist, dev, total_ms, call_ms, launches)
     train = None
     if not args.conv and cfg.dstate <= 16:
         train = train_step_times(ms, sets, params, out, stream, W, K)

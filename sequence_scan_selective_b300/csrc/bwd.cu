@@ -5,13 +5,27 @@
 
 namespace mscan {
 
+// Register budget of the launch: 3 CTAs per SM (the reverse walk keeps each step's Abar) when
+// the grid fits in one wave of 3 per SM and the simplified discretisation is used, else 4.
+// MAMBA_SCAN_BWD_MINB=3 or =4 forces one (tests).
+static int bwd_minb(long long ctas) {
+    const int force = env_int("MAMBA_SCAN_BWD_MINB", 0);
+    if (force == 3 || force == 4) return force;
+    return ctas <= 3LL * sm_count() ? 3 : 4;
+}
+
 template <typename TIn, bool ZOH, int MODE>
 static int bwd_launch(const BwdArgs& a, bool vec, unsigned nz, cudaStream_t st) {
-    static AttrCache attr_vec, attr_scalar;
-    auto kern = vec ? scan_bwd_kernel<TIn, true, ZOH, MODE> : scan_bwd_kernel<TIn, false, ZOH, MODE>;
-    int rc = allow_smem(kern, vec ? attr_vec : attr_scalar);
-    if (rc) return rc;
+    static AttrCache attr[2][2];
     const dim3 grid((unsigned)((a.dim + bwd::kCh - 1) / bwd::kCh), (unsigned)a.batch, nz);
+    auto kern = vec ? scan_bwd_kernel<TIn, true, ZOH, MODE, 4> : scan_bwd_kernel<TIn, false, ZOH, MODE, 4>;
+    bool three = false;
+    if constexpr (!ZOH && MODE != bwd::kCarry) {
+        three = bwd_minb((long long)grid.x * grid.y * grid.z) == 3;
+        if (three) kern = vec ? scan_bwd_kernel<TIn, true, ZOH, MODE, 3> : scan_bwd_kernel<TIn, false, ZOH, MODE, 3>;
+    }
+    int rc = allow_smem(kern, attr[vec ? 1 : 0][three ? 1 : 0]);
+    if (rc) return rc;
     kern<<<grid, bwd::kThreads, bwd::Layout<TIn>::BYTES, st>>>(a);
     count_launch();
     cudaError_t e = cudaGetLastError();

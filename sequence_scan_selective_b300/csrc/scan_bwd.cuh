@@ -281,9 +281,14 @@ __device__ __forceinline__ void store_steps(TIn* p, long long tg0, long long L, 
 
 }  // namespace bwd
 
-template <typename TIn, bool VEC, bool ZOH, int MODE>
-__global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArgs a) {
+// MINB: CTAs per SM the register budget is cut for (4: 128 registers a thread; 3: 168).  With 3,
+// the simplified discretisation keeps each step's Abar from the slot's recomputation for the
+// reverse walk instead of computing it again (2 ex2 and a packed multiply per state pair and step
+// fewer, 32 more registers); it suits grids of at most 3 CTAs per SM.
+template <typename TIn, bool VEC, bool ZOH, int MODE, int MINB = 4>
+__global__ void __launch_bounds__(bwd::kThreads, MINB) scan_bwd_kernel(const BwdArgs a) {
     using namespace bwd;
+    constexpr bool KEEP = MINB < 4 && !ZOH && MODE != kCarry;
     using Lt = bwd::Layout<TIn>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -398,13 +403,15 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
         }
     };
 
-    // one step of the lane's 4 states: h <- Abar h + Bbar x (packed pairs for the simplified B)
-    auto advance = [&](float2 (&h)[2], const float4& qq, const float4& bq) {
+    // one step of the lane's 4 states: h <- Abar h + Bbar x (packed pairs for the simplified B);
+    // abar_out, when given, receives the step's Abar pairs
+    auto advance = [&](float2 (&h)[2], const float4& qq, const float4& bq, float2* abar_out = nullptr) {
         const float2 bp[2] = {make_float2(bq.x, bq.y), make_float2(bq.z, bq.w)};
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
             const float2 X = fmul2(make_float2(qq.x, qq.x), A2[p]);
             const float2 ab = make_float2(ex2_approx(X.x), ex2_approx(X.y));
+            if (abar_out != nullptr) abar_out[p] = ab;
             if constexpr (!ZOH) {
                 h[p] = ffma2(ab, h[p], fmul2(make_float2(qq.y, qq.y), bp[p]));
             } else {
@@ -537,12 +544,14 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
                 h[0] = make_float2(v.x, v.y);
                 h[1] = make_float2(v.z, v.w);
             }
-            // recompute the slot's states
+            // recompute the slot's states (and, KEEP, their Abar)
             float2 hist[bwd::kSlot][2];
+            float2 abk[KEEP ? bwd::kSlot : 1][2];
 #pragma unroll
             for (int i = 0; i < bwd::kSlot; ++i) {
                 const int t = s * bwd::kSlot + i;
-                advance(h, q[t * 8 + c], *reinterpret_cast<const float4*>(bcq + t * kBcqPitch + 4 * g));
+                advance(h, q[t * 8 + c], *reinterpret_cast<const float4*>(bcq + t * kBcqPitch + 4 * g),
+                        KEEP ? abk[KEEP ? i : 0] : nullptr);
                 hist[i][0] = h[0];
                 hist[i][1] = h[1];
             }
@@ -568,8 +577,13 @@ __global__ void __launch_bounds__(bwd::kThreads, 4) scan_bwd_kernel(const BwdArg
 #pragma unroll
                     for (int p = 0; p < 2; ++p) {
                         const float2 ht = hist[i][p];
-                        const float2 X = fmul2(dq, A2[p]);
-                        const float2 ab = make_float2(ex2_approx(X.x), ex2_approx(X.y));
+                        float2 ab;
+                        if constexpr (KEEP) {
+                            ab = abk[i][p];
+                        } else {
+                            const float2 X = fmul2(dq, A2[p]);
+                            ab = make_float2(ex2_approx(X.x), ex2_approx(X.y));
+                        }
                         const float2 lam = ffma2(eq, cp[p], mu[p]);
                         sch2 = ffma2(cp[p], ht, sch2);
                         const float2 vc = fmul2(eq, ht);

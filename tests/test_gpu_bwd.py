@@ -287,3 +287,24 @@ def test_bwd_million_steps_library_plan(ms):
     assert ms.launch_count() - n0 >= 3  # carry, full and correction launches
     ref = _oracle(inp, cfg.dtype)
     _compare(got, ref, cfg.dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("nseg,N", [("1", 16), ("3", 16), ("1", 24)])
+def test_bwd_register_budgets_agree(ms, dtype, nseg, N):
+    """The 3-CTA-per-SM build of the backward kernel (which keeps each step's Abar from the slot's
+    recomputation) gives the 4-CTA build's gradients, unsplit and split, one and two state
+    blocks, and both match the oracle.  The per-(channel, step) gradients and dh0 come from one
+    lane each and agree bit for bit; dA, dB, dC, dD and the bias gradient are sums that CTAs add
+    into with atomics, whose order varies from run to run, so they agree to rounding."""
+    cfg = synth.CONFIGS["m130"].replace(batch=2, dim=72, dstate=N, seqlen=1600, dtype=dtype, seed=230 + N)
+    inp = _inputs(cfg)
+    got = {}
+    for minb in ("3", "4"):
+        with _env(MAMBA_SCAN_BWD_MINB=minb, MAMBA_SCAN_BWD_NSEG=nseg):
+            got[minb] = _gpu(ms, inp, dtype)
+    for k in ("du", "ddelta", "dz", "dh0"):
+        assert np.array_equal(got["3"][k], got["4"][k]), k
+    for k in ("dA", "dB", "dC", "dD", "ddelta_bias"):
+        assert rel_err(got["3"][k], got["4"][k]) <= 1e-5, k
+    _compare(got["3"], _oracle(inp, dtype), dtype)

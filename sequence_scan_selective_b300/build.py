@@ -13,7 +13,7 @@ LIB = os.path.join(HERE, "libmambascan.so")
 # One translation unit per kernel family (each becomes its own device module), compiled in
 # parallel and linked into one shared library.
 SOURCES = ["mamba_scan.cu", "fwd_lane_f32.cu", "fwd_lane_bf16.cu", "fwd_warp_f32.cu", "fwd_warp_bf16.cu", "bwd.cu",
-           "conv.cu", "step.cu"]
+           "conv.cu", "step.cu", "fwd_plan.cu"]
 HEADERS = ["host.cuh", "fwd_common.cuh", "fwd_lane.cuh", "fwd_warp.cuh", "ptx.cuh", "common.cuh", "scan_fwd.cuh", "scan_fwd_cl.cuh", "scan_fix.cuh",
            "scan_bwd.cuh", "state_step.cuh", "conv.cuh"]
 OBJDIR = os.path.join(HERE, "_build")

@@ -1,7 +1,7 @@
 // Forward scan, channel-per-lane kernel (N <= 16): planner, TMA descriptors and launches of
 // scan_fwd_cl_kernel, and for a split time axis the second launch, scan_fix_kernel.  Included by
 // one translation unit per input type (fwd_lane_f32.cu, fwd_lane_bf16.cu), which instantiates
-// fwd_lane_run_t, fwd_lane_nseg_t and fwd_lane_status_t for that type.
+// fwd_lane_run_t and fwd_lane_status_t for that type.
 #pragma once
 #include <cstring>
 
@@ -225,14 +225,6 @@ int fwd_lane_run_t(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, f
     if (s->dstate > 16) return fail(MAMBA_ERR_ARG, "the channel-per-lane kernel takes N <= 16");
     if (s->dstate <= 8) return run<TIn, 8>(s, a, softplus, scratch, cap, st);
     return run<TIn, 16>(s, a, softplus, scratch, cap, st);
-}
-
-template <typename TIn>
-int fwd_lane_nseg_t(const mamba_scan_shape* s) {
-    if (s->dstate > 16) return fail(MAMBA_ERR_ARG, "the channel-per-lane kernel takes N <= 16");
-    FwdPlan p;
-    const int rc = s->dstate <= 8 ? plan_cl<TIn, 8>(s, sm_count(), p) : plan_cl<TIn, 16>(s, sm_count(), p);
-    return rc ? rc : p.nseg;
 }
 
 template <typename TIn>

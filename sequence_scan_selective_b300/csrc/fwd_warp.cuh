@@ -1,7 +1,7 @@
 // Forward scan, four-lanes-per-channel kernel (any N <= 64; also the exact hold and the fused
 // convolution): planner, TMA descriptors and launches of scan_fwd_kernel.  Included by one
 // translation unit per input type (fwd_warp_f32.cu, fwd_warp_bf16.cu), which instantiates
-// fwd_warp_run_t, fwd_warp_nseg_t and fwd_warp_status_t for that type.
+// fwd_warp_run_t and fwd_warp_status_t for that type.
 #pragma once
 #include <cstring>
 
@@ -191,15 +191,6 @@ int fwd_warp_run_t(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, b
     if (s->dstate <= 16) return run<TIn, 16>(s, a, softplus, gate, scratch, cap, st);
     if (s->dstate <= 32) return run<TIn, 32>(s, a, softplus, gate, scratch, cap, st);
     return run<TIn, 64>(s, a, softplus, gate, scratch, cap, st);
-}
-
-template <typename TIn>
-int fwd_warp_nseg_t(const mamba_scan_shape* s) {
-    FwdPlan p;
-    const int nsm = sm_count();
-    const int rc = s->dstate <= 16 ? plan_warp<TIn, 16>(s, nsm, p)
-                   : s->dstate <= 32 ? plan_warp<TIn, 32>(s, nsm, p) : plan_warp<TIn, 64>(s, nsm, p);
-    return rc ? rc : p.nseg;
 }
 
 template <typename TIn>

@@ -3,6 +3,5 @@
 
 namespace mscan {
 template int fwd_warp_run_t<float>(const mamba_scan_shape*, const FwdArgs&, bool, bool, float2*, size_t, cudaStream_t);
-template int fwd_warp_nseg_t<float>(const mamba_scan_shape*);
 template int fwd_warp_status_t<float>(bool);
 }  // namespace mscan

@@ -3,8 +3,9 @@
 //
 // Units: mamba_scan.cu (C ABI, argument checks, kernel choice), fwd_lane_{f32,bf16}.cu
 // (channel-per-lane forward scan and its split-sequence second launch), fwd_warp_{f32,bf16}.cu
-// (four-lanes-per-channel forward scan), bwd.cu (backward pass), conv.cu (causal convolution for
-// the block's backward pass), step.cu (decoding step).  Each compiles to its own device module.
+// (four-lanes-per-channel forward scan), fwd_plan.cu (the forward planners' segment counts,
+// host-side), bwd.cu (backward pass), conv.cu (causal convolution for the block's backward pass),
+// step.cu (decoding step).  Each compiles to its own device module.
 #pragma once
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -88,7 +89,7 @@ template <typename TIn>
 int fwd_warp_run_t(const mamba_scan_shape* s, const FwdArgs& a, bool softplus, bool gate, float2* scratch,
                    size_t cap, cudaStream_t st);
 // Segments of the time axis that the forward planner of each kernel picks for a shape (negative:
-// an error code).  Host-only: no launch, no allocation.
+// an error code).  Host-only: no launch, no allocation.  In fwd_plan.cu.
 template <typename TIn>
 int fwd_lane_nseg_t(const mamba_scan_shape* s);
 template <typename TIn>

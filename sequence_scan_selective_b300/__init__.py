@@ -11,9 +11,14 @@ Entry points (names as in include/mamba_scan.h):
   mamba_scan_fwd_noalloc(...)   same arguments; the library allocates no device memory
   mamba_scan_fwd_pipelined(...)  the scan of host-resident inputs, batch rows pipelined over streams
   mamba_state_step(state, x, delta, A, B, C, D, z, delta_bias, softplus, y=None)
-  mamba_scan_bwd(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0=None, dlast_state=None)
-  selective_scan(u, delta, A, B, C, D, z, delta_bias, softplus, h0=None, disc="simple")
-                                 the scan as an autograd operation (forward + backward above)
+  mamba_scan_bwd(u, delta, A, B, C, dy, D, z, delta_bias, softplus, h0=None, dlast_state=None,
+                 ckpt=None)     (ckpt -> mamba_scan_bwd_ckpt)
+  mamba_scan_fwd_train(...)     mamba_scan_fwd that also returns the backward pass's checkpoints
+  train_checkpoint_bytes(u, A)  their size (mamba_scan_fwd_train_ckpt_bytes; 0: none kept)
+  mamba_scan_fwd_conv(...), mamba_scan_bwd_conv(...)   with the block's causal convolution
+  selective_scan(u, delta, A, B, C, D, z, delta_bias, softplus, h0=None, disc="simple",
+                 checkpoints=True)   the scan as an autograd operation (forward + backward above)
+  selective_scan_conv(...)      the same with the convolution in front
 """
 from __future__ import annotations
 
@@ -275,7 +280,6 @@ def mamba_scan_fwd_train(u, delta, A, B, C, D=None, z=None, delta_bias=None, sof
     Returns (y, last_state, ckpt), with ckpt None when the library splits the sequence along L and
     keeps no checkpoints (then no buffer is allocated for them)."""
     bsz, dim, L = u.shape
-    N = A.shape[1]
     if ckpt is None:
         if train_checkpoint_bytes(u, A) == 0:
             y, last_state = _scan(_lib.mamba_scan_fwd_ex, u, delta, A, B, C, D, z, delta_bias, softplus, y,

@@ -206,14 +206,16 @@ int mamba_scan_fwd_noalloc(const mamba_scan_shape* s, const void* u, const void*
  * that writes exactly these one-in-eight states before its reverse sweep.  Writing them here
  * instead (8 bytes per channel and step, while the forward kernel is bound by arithmetic, not
  * HBM) lets mamba_scan_bwd_ckpt skip that sweep.
- *   ckpt          [b, ceil(L/8), d, 16] fp32, 16-byte aligned, written for slots 1.. (slot 0 is
- *                 h0); states past N are written as zero.  Must not overlap any input or output.
- *                 dstate must be <= 16.
- *   ckpt_written  set to 1 when ckpt was written, 0 when it was not: a sequence the library splits
- *                 along L (few channels, long sequences) gets no checkpoints, and
+ *   ckpt          [b, ceil(L/8), d, 16] fp32 device memory, caller-owned, 16-byte aligned;
+ *                 written for slots 1.. (slot 0 is h0), with the states past N as zero.  Must not
+ *                 overlap any input or output.
+ *   ckpt_written  host int: set to 1 when ckpt was written, 0 when it was not.  A sequence the
+ *                 library splits along L (few channels, long sequences) gets no checkpoints, and
  *                 mamba_scan_bwd_ckpt then makes its own.  mamba_scan_fwd_train_ckpt_bytes
  *                 tells beforehand (0 bytes: none).
- * Everything else as for mamba_scan_fwd_ex (no fused convolution).  Errors: as mamba_scan_fwd_ex.
+ * Everything else as for mamba_scan_fwd_ex (no fused convolution).  Errors: as mamba_scan_fwd_ex,
+ * and MAMBA_ERR_ARG for a NULL ckpt or ckpt_written, dstate > 16, a misaligned or overlapping ckpt
+ * (then nothing is launched, and ckpt_written, when not NULL, is 0).
  */
 int mamba_scan_fwd_train(const mamba_scan_shape* s, int discretization, const void* u, const void* delta,
                          const float* A, const void* B, const void* C, const float* D, const void* z,

@@ -256,10 +256,10 @@ extern "C" int mamba_scan_fwd_train(const mamba_scan_shape* s, int discretizatio
                                     const float* delta_bias, int softplus_flag, const float* h0, void* y,
                                     float* last_state, float* ckpt, int* ckpt_written, void* stream) {
     t_err.clear();
+    if (ckpt_written) *ckpt_written = 0;
     int rc = check_shape(s, true);
     if (rc) return rc;
     if (!ckpt || !ckpt_written) return fail(MAMBA_ERR_ARG, "ckpt and ckpt_written are required");
-    *ckpt_written = 0;
     if (!aligned16(ckpt)) return fail(MAMBA_ERR_ARG, "ckpt must be 16-byte aligned");
     if (s->dstate > 16) return fail(MAMBA_ERR_ARG, "checkpoints are kept for dstate <= 16");
     const long long chans = (long long)s->batch * s->dim;

@@ -227,3 +227,37 @@ def test_train_checkpoint_bytes_host_query(ms, monkeypatch):
     assert q(batch=2, dim=64, dstate=16, seqlen=-1)[0] == -1
     monkeypatch.setenv("MAMBA_SCAN_NSEG", "1")  # read by the planners at every call
     assert q(batch=1, dim=1536, dstate=16, seqlen=1 << 20) == (0, 1536 * (1 << 17) * 64)
+
+
+def test_plain_c_client(ms, tmp_path):
+    """The header and library serve a C99 program with no Python or torch in between: version,
+    the checkpoint size query at the 1.4B layer shape, an argument error and its message, and no
+    kernel launched."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    inc = os.path.join(os.path.dirname(here), "include")
+    libdir = os.path.dirname(ms.LIB_PATH)
+    exe = str(tmp_path / "c_client")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", inc, os.path.join(here, "c_client.c"),
+                    "-L", libdir, "-lmambascan", f"-Wl,-rpath,{libdir}", "-o", exe], check=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split("\n")
+    assert out[0] == f"version {ms.lib().mamba_scan_version()} {ms.lib().mamba_scan_version()}"
+    assert out[1] == f"ckpt_bytes 0 {4 * 256 * 4096 * 64}"
+    assert out[2].startswith("bad_shape -1 ") and "dstate" in out[2]
+    assert out[3] == "null_shape -1"
+    assert out[4] == "launches 0"
+
+
+def test_header_is_valid_cxx(tmp_path):
+    import shutil
+    import subprocess
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("no C++ compiler")
+    here = os.path.dirname(os.path.abspath(__file__))
+    hdr = os.path.join(os.path.dirname(here), "include", "mamba_scan.h")
+    subprocess.run([gxx, "-std=c++17", "-Wall", "-Werror", "-fsyntax-only", "-x", "c++", hdr], check=True)

@@ -10,7 +10,10 @@ times the million-token scan (batch 1, d_inner 1536, N 16, L 2^20, fp32) and rep
 per-element rate next to the main workload's scan rate (`long_sequence`).
 
 Prints one JSON line (rank 0).  `value` = elements (batch * d_inner * (L + 1)) per second over all
-ranks, device-timed with CUDA events, inputs resident in HBM.  `e2e` = the same metric through the
+ranks, device-timed with CUDA events, inputs resident in HBM; the timed steps follow the warm-up
+steps and an untimed settle phase (`--settle-ms`, reported as `clock_settle`).  `--pass bwd` times
+the backward pass instead and, for N <= 16, the training step both ways (`train_step`: forward +
+backward recomputing the checkpoints, or the training forward pass keeping them).  `e2e` = the same metric through the
 public API with the inputs copied from pinned host memory and the outputs read back inside the
 timed region.  `--impl reference` times the fp64 CPU oracle on the host cores instead.
 
